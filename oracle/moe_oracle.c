@@ -1,0 +1,262 @@
+/*
+ * moe_oracle.c -- CPU oracle for routed Mixture-of-Experts expert execution.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may include, link or
+ * call this file: only tests/, __graft_entry__.smoke() and the CPU-baseline
+ * leg of bench.py use it. It shares no code, header, table or helper with the
+ * CUDA library under moe_routed_expert_routing_gb300/csrc.
+ *
+ * What it computes (plain definitions, written out loop by loop, in fp32):
+ *
+ *  1. Local dispatch -- TileOps PR #1738 "Separate dispatched expert compute",
+ *     Summary ("Compose routed expert execution from local dispatch, expert
+ *     compute, and combine") and Scope ("BF16 tight/no-pad expert compute";
+ *     consumers read the valid-row count from expert_offsets[-1:]).
+ *     A routed slot is s = t*k + j. Count the slots of each expert, take the
+ *     exclusive prefix sum as expert_offsets[E+1], then walk s = 0..R-1 in
+ *     ascending order and give each slot the next free row of its expert.
+ *     That walk is the definition of a stable scatter: inside one expert the
+ *     rows keep slot order. perm[row] = s, inv[s] = row.
+ *     Reading: an id of -1 marks a dropped slot (no row, contributes nothing);
+ *     any other id outside [0, E) is also dropped and counted as an error.
+ *
+ *  2. Expert MLP for one routed row (the dispatched-expert MLP of the same
+ *     page, Summary, with its fused-gated epilogue, Review follow-up):
+ *       g_n = sum_h x_h * W13[e, n, h]        n in [0, I)   (gate: rows 0..I-1)
+ *       u_n = sum_h x_h * W13[e, I + n, h]                  (up:   rows I..2I-1)
+ *       a_n = bf16( (g_n / (1 + exp(-g_n))) * u_n )         SiLU(gate) * up
+ *       y_m = sum_n a_n * W2[e, m, n]         m in [0, H)
+ *     All sums in fp32, index ascending. The activation is rounded to bf16
+ *     (round to nearest, ties to even); y stays fp32.
+ *
+ *  3. Combine -- same page, Summary ("Keep routing weights ... outside expert
+ *     compute"): out_acc[t, m] = sum_{j ascending} w[t, j] * y_{t,j}[m] in
+ *     fp32, then out[t, m] = bf16(out_acc[t, m]). Weights are used as given.
+ *
+ * Parity pins (tests/test_oracle_pins.py): dispatch invariants and a brute
+ * force restatement; bf16 rounding against an independent library cast; the
+ * one-expert k=1 special case against a dense MLP built from library matmuls;
+ * dispatch+combine with an identity expert against the closed form
+ * sum_j w[t,j] * x[t]; a naive fp64 restatement on tiny shapes.
+ *
+ * Build: gcc -O2 -fopenmp -ffp-contract=off -shared -fPIC (oracle/build.py).
+ * -ffp-contract=off keeps every multiply and add separately rounded, so the
+ * x86 container and the aarch64 GPU host give identical bits.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- bf16 <-> fp32 (bf16 is the top 16 bits of an IEEE-754 binary32) ---- */
+
+static float bf16_bits_to_f32(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round to nearest, ties to even: add half of the dropped range, plus one
+ * when the kept part is odd, then truncate. NaN stays a quiet NaN. */
+static uint16_t f32_to_bf16_bits_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep_lsb = (u >> 16) & 1u;
+    u += 0x7fffu + keep_lsb;
+    return (uint16_t)(u >> 16);
+}
+
+void oracle_round_bf16(int64_t n, const float *in, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = f32_to_bf16_bits_rne(in[i]);
+}
+
+/* ---- 1. dispatch ---------------------------------------------------------- */
+
+/* ids[R] -> counts[E], offsets[E+1], perm[R] (rows >= offsets[E] set to -1),
+ * inv[R] (-1 for a dropped slot). Returns the number of ids that were neither
+ * -1 nor inside [0, E). */
+int32_t oracle_dispatch(int32_t R, int32_t E, const int32_t *ids,
+                        int32_t *counts, int32_t *offsets, int32_t *perm,
+                        int32_t *inv)
+{
+    int32_t bad = 0;
+    for (int32_t e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int32_t s = 0; s < R; ++s) {
+        int32_t e = ids[s];
+        if (e >= 0 && e < E)
+            counts[e] += 1;
+        else if (e != -1)
+            bad += 1;
+    }
+    offsets[0] = 0;
+    for (int32_t e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + counts[e];
+
+    int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    for (int32_t e = 0; e < E; ++e)
+        cursor[e] = offsets[e];
+    for (int32_t r = 0; r < R; ++r)
+        perm[r] = -1;
+    for (int32_t s = 0; s < R; ++s) {
+        int32_t e = ids[s];
+        if (e >= 0 && e < E) {
+            int32_t row = cursor[e];
+            cursor[e] += 1;
+            perm[row] = s;
+            inv[s] = row;
+        } else {
+            inv[s] = -1;
+        }
+    }
+    free(cursor);
+    return bad;
+}
+
+/* ---- 2. expert MLP --------------------------------------------------------- */
+
+/* One routed row through one expert. x[H], W13e[2I, H], W2e[H, I] are bf16
+ * bit patterns; a_out[I] receives the bf16 activation, y_out[H] fp32. */
+static void expert_mlp_row(int32_t H, int32_t I, const uint16_t *x,
+                           const uint16_t *W13e, const uint16_t *W2e,
+                           uint16_t *a_out, float *y_out, float *a_scratch)
+{
+    for (int32_t n = 0; n < I; ++n) {
+        const uint16_t *wg = W13e + (size_t)n * (size_t)H;
+        const uint16_t *wu = W13e + (size_t)(I + n) * (size_t)H;
+        float g = 0.0f, u = 0.0f;
+        for (int32_t h = 0; h < H; ++h) {
+            float xh = bf16_bits_to_f32(x[h]);
+            g += xh * bf16_bits_to_f32(wg[h]);
+            u += xh * bf16_bits_to_f32(wu[h]);
+        }
+        float silu = g / (1.0f + expf(-g));
+        uint16_t a = f32_to_bf16_bits_rne(silu * u);
+        if (a_out)
+            a_out[n] = a;
+        a_scratch[n] = bf16_bits_to_f32(a);
+    }
+    for (int32_t m = 0; m < H; ++m) {
+        const uint16_t *w2 = W2e + (size_t)m * (size_t)I;
+        float y = 0.0f;
+        for (int32_t n = 0; n < I; ++n)
+            y += a_scratch[n] * bf16_bits_to_f32(w2[n]);
+        y_out[m] = y;
+    }
+}
+
+/* Several rows through one expert: rows are independent, so they may run on
+ * separate threads. x_rows[n_rows, H] -> a_rows[n_rows, I] (nullable),
+ * y_rows[n_rows, H]. */
+void oracle_expert_rows(int32_t H, int32_t I, const uint16_t *W13e,
+                        const uint16_t *W2e, int32_t n_rows,
+                        const uint16_t *x_rows, uint16_t *a_rows, float *y_rows)
+{
+#pragma omp parallel
+    {
+        float *scratch = (float *)malloc(sizeof(float) * (size_t)I);
+#pragma omp for schedule(dynamic, 1)
+        for (int32_t r = 0; r < n_rows; ++r)
+            expert_mlp_row(H, I, x_rows + (size_t)r * H, W13e, W2e,
+                           a_rows ? a_rows + (size_t)r * I : NULL,
+                           y_rows + (size_t)r * H, scratch);
+        free(scratch);
+    }
+}
+
+/* ---- 3. combine ------------------------------------------------------------ */
+
+/* y_slot[n_tok, k, H] holds each routed slot's expert output (fp32); valid[n_tok,
+ * k] is 0 for a dropped slot. out_acc[n_tok, H] fp32, out[n_tok, H] bf16. */
+void oracle_combine_slots(int32_t n_tok, int32_t k, int32_t H,
+                          const float *y_slot, const float *w,
+                          const int32_t *valid, float *out_acc, uint16_t *out)
+{
+    for (int32_t t = 0; t < n_tok; ++t) {
+        for (int32_t m = 0; m < H; ++m) {
+            float acc = 0.0f;
+            for (int32_t j = 0; j < k; ++j) {
+                size_t s = (size_t)t * k + j;
+                if (valid[s])
+                    acc += w[s] * y_slot[s * (size_t)H + m];
+            }
+            out_acc[(size_t)t * H + m] = acc;
+            out[(size_t)t * H + m] = f32_to_bf16_bits_rne(acc);
+        }
+    }
+}
+
+/* Combine from the expert-major (sorted) batch: y_sorted[rows, H] bf16 bits,
+ * inv[T*k] maps slot -> row (-1 = dropped). This is the form the dispatched
+ * batch takes between expert compute and combine. */
+void oracle_combine_sorted(int32_t T, int32_t k, int32_t H,
+                           const uint16_t *y_sorted, const int32_t *inv,
+                           const float *w, float *out_acc, uint16_t *out)
+{
+    for (int32_t t = 0; t < T; ++t) {
+        for (int32_t m = 0; m < H; ++m) {
+            float acc = 0.0f;
+            for (int32_t j = 0; j < k; ++j) {
+                size_t s = (size_t)t * k + j;
+                int32_t row = inv[s];
+                if (row >= 0)
+                    acc += w[s] * bf16_bits_to_f32(y_sorted[(size_t)row * H + m]);
+            }
+            out_acc[(size_t)t * H + m] = acc;
+            out[(size_t)t * H + m] = f32_to_bf16_bits_rne(acc);
+        }
+    }
+}
+
+/* ---- whole forward over a token subset ------------------------------------ */
+
+/* Loops over the listed tokens and their k experts: steps 2 and 3 above.
+ * x[T, H], ids[T, k], w[T, k], W13[E, 2I, H], W2[E, H, I]. tok[n_tok] lists
+ * the tokens to evaluate; out_acc / out are [n_tok, H]. Returns the number of
+ * ids that were neither -1 nor inside [0, E). */
+int32_t oracle_moe_tokens(int32_t T, int32_t E, int32_t k, int32_t H, int32_t I,
+                          const uint16_t *x, const int32_t *ids, const float *w,
+                          const uint16_t *W13, const uint16_t *W2, int32_t n_tok,
+                          const int32_t *tok, float *out_acc, uint16_t *out)
+{
+    (void)T;
+    int32_t bad = 0;
+    size_t per13 = (size_t)2 * I * H, per2 = (size_t)H * I;
+#pragma omp parallel reduction(+ : bad)
+    {
+        float *scratch = (float *)malloc(sizeof(float) * (size_t)I);
+        float *y = (float *)malloc(sizeof(float) * (size_t)H);
+#pragma omp for schedule(dynamic, 1)
+        for (int32_t q = 0; q < n_tok; ++q) {
+            int32_t t = tok[q];
+            float *acc = out_acc + (size_t)q * H;
+            for (int32_t m = 0; m < H; ++m)
+                acc[m] = 0.0f;
+            for (int32_t j = 0; j < k; ++j) {
+                int32_t e = ids[(size_t)t * k + j];
+                if (e < 0 || e >= E) {
+                    if (e != -1)
+                        bad += 1;
+                    continue;
+                }
+                expert_mlp_row(H, I, x + (size_t)t * H, W13 + (size_t)e * per13,
+                               W2 + (size_t)e * per2, NULL, y, scratch);
+                float wj = w[(size_t)t * k + j];
+                for (int32_t m = 0; m < H; ++m)
+                    acc[m] += wj * y[m];
+            }
+            for (int32_t m = 0; m < H; ++m)
+                out[(size_t)q * H + m] = f32_to_bf16_bits_rne(acc[m]);
+        }
+        free(y);
+        free(scratch);
+    }
+    return bad;
+}

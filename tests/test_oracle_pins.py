@@ -1,0 +1,380 @@
+"""Pins for the CPU oracle: each check compares it with something other than itself.
+
+* bf16 rounding     -- against torch's float32 -> bfloat16 cast (a library
+                       routine), on ties, subnormals, infinities and NaN.
+* dispatch          -- a worked example derived by hand from the definition
+                       (stable scatter by flat slot index; TileOps PR #1738,
+                       Summary "local dispatch" and Scope "tight/no-pad"),
+                       plus a brute-force restatement and its invariants
+                       (``expert_offsets[-1] == R``, bijection, stability).
+* expert MLP        -- the one-expert, k=1, weight-1 special case is a dense
+                       gated MLP, computed with torch fp64 matmuls and
+                       ``torch.nn.functional.silu``.
+* dispatch+combine  -- with an identity expert, dispatch then combine equals
+                       ``(sum_j w[t,j]) * x[t]`` (closed form).
+* whole forward     -- a naive fp64 restatement in pure Python loops on tiny
+                       shapes, several experts, dropped slots included.
+
+``test_planted_mistakes`` then builds mutated copies of ``moe_oracle.c``
+(a dropped term, a swapped operand, a wrong sign, a wrong index ...) and
+checks that at least one pin fails for each, so that the pins are known to
+bite.
+"""
+from __future__ import annotations
+
+import math
+import os
+import shutil
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import oracle  # noqa: E402
+from oracle import Oracle, bf16_bits_to_f32
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ORACLE_SRC = os.path.join(os.path.dirname(HERE), "oracle", "moe_oracle.c")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def torch_bf16_bits(x_f32: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(x_f32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def rand_bf16(shape, std, seed):
+    g = torch.Generator().manual_seed(seed)
+    t = (torch.randn(shape, generator=g) * std).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def near_bf16_midpoint(v64: np.ndarray, rel: float = 1e-4, tol_abs=0.0) -> np.ndarray:
+    """True where a float64 value lies within ``rel`` (relative) or ``tol_abs``
+    (absolute) of a bf16 rounding midpoint."""
+    v = np.asarray(v64, dtype=np.float64)
+    lo = bf16_bits_to_f32(torch_bf16_bits(v.astype(np.float32))).astype(np.float64)
+    # neighbour on the other side of v
+    bits = torch_bf16_bits(v.astype(np.float32)).astype(np.int32)
+    step = np.where((lo <= v) == (v >= 0), 1, -1)
+    other = bf16_bits_to_f32((bits + step).astype(np.uint16)).astype(np.float64)
+    mid = 0.5 * (lo + other)
+    return np.abs(v - mid) <= np.maximum(rel * np.abs(v), tol_abs)
+
+
+def silu64(g):
+    return g / (1.0 + np.exp(-g))
+
+
+# ----------------------------------------------------------------------------- pins
+
+def pin_round_bf16(o: Oracle):
+    rng = np.random.default_rng(0)
+    vals = [rng.standard_normal(20000).astype(np.float32) * 10.0 ** rng.integers(-30, 30, 20000)]
+    # exact ties: low 16 bits == 0x8000, both parities of the kept part
+    base = rng.integers(0, 2 ** 31, 4000, dtype=np.int64).astype(np.uint32)
+    ties = ((base & 0xFFFF0000) | 0x8000).view(np.float32)
+    vals.append(ties[np.isfinite(ties)])
+    vals.append(np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, 1e-40, -1e-40, 3.3895e38, 65504.0,
+                          np.float32(1.0) + np.float32(2 ** -8), np.float32(1.0) + np.float32(3 * 2 ** -9)],
+                         dtype=np.float32))
+    x = np.concatenate(vals).astype(np.float32)
+    got = o.round_bf16(x)
+    want = torch_bf16_bits(x)
+    assert np.array_equal(got, want), f"bf16 rounding differs at {np.count_nonzero(got != want)} values"
+    nan = o.round_bf16(np.array([np.nan], dtype=np.float32))
+    assert np.isnan(bf16_bits_to_f32(nan))[0]
+
+
+def pin_dispatch_hand(o: Oracle):
+    # ids[T=3, k=2] with E=3. Slots s = t*k + j: s0:e2 s1:e0 s2:e0 s3:e1 s4:e2 s5:e1.
+    # counts = [2, 2, 2] -> offsets = [0, 2, 4, 6].
+    # Walking s ascending: e0 gets s1, s2 (rows 0, 1); e1 gets s3, s5 (rows 2, 3);
+    # e2 gets s0, s4 (rows 4, 5). perm[row] = slot, inv[slot] = row.
+    ids = np.array([[2, 0], [0, 1], [2, 1]], dtype=np.int32)
+    counts, offsets, perm, inv, bad = o.dispatch(ids, 3)
+    assert counts.tolist() == [2, 2, 2]
+    assert offsets.tolist() == [0, 2, 4, 6]
+    assert perm.tolist() == [1, 2, 3, 5, 0, 4]
+    assert inv.tolist() == [4, 0, 1, 2, 5, 3]
+    assert bad == 0
+    # a dropped slot (-1) and an invalid id (7): neither gets a row.
+    ids2 = np.array([[1, -1], [7, 1], [0, 1]], dtype=np.int32)
+    counts, offsets, perm, inv, bad = o.dispatch(ids2, 3)
+    # valid slots: s0:e1 s3:e1 s4:e0 s5:e1 -> e0: s4 (row 0); e1: s0, s3, s5 (rows 1..3)
+    assert offsets.tolist() == [0, 1, 4, 4]
+    assert perm.tolist() == [4, 0, 3, 5, -1, -1]
+    assert inv.tolist() == [1, -1, -1, 2, 0, 3]
+    assert bad == 1
+
+
+def brute_dispatch(ids_flat: np.ndarray, E: int):
+    """O(R * E) restatement: expert e's rows are its slots in ascending order."""
+    ids_flat = [int(v) for v in ids_flat]
+    offsets = [0]
+    perm = []
+    for e in range(E):
+        mine = [s for s, v in enumerate(ids_flat) if v == e]
+        perm.extend(mine)
+        offsets.append(offsets[-1] + len(mine))
+    inv = [-1] * len(ids_flat)
+    for r, s in enumerate(perm):
+        inv[s] = r
+    return offsets, perm, inv
+
+
+def pin_dispatch_brute(o: Oracle):
+    rng = np.random.default_rng(1)
+    for (T, k, E) in [(37, 3, 5), (1, 6, 384), (0, 2, 4), (50, 1, 1), (64, 8, 16)]:
+        ids = rng.integers(0, E, (T, k)).astype(np.int32)
+        if T > 2:
+            ids[1, 0] = -1
+        counts, offsets, perm, inv, bad = o.dispatch(ids, E)
+        b_off, b_perm, b_inv = brute_dispatch(ids.reshape(-1), E)
+        assert offsets.tolist() == b_off, (T, k, E)
+        R = T * k
+        n_valid = b_off[-1]
+        assert perm[:n_valid].tolist() == b_perm
+        assert np.all(perm[n_valid:] == -1)
+        assert inv.tolist() == b_inv
+        # invariants
+        assert offsets[-1] == int(np.count_nonzero(ids >= 0))
+        assert np.all(np.diff(offsets) >= 0)
+        flat = ids.reshape(-1)
+        for e in range(E):
+            seg = perm[offsets[e]:offsets[e + 1]]
+            assert np.all(flat[seg] == e)
+            assert np.all(np.diff(seg) > 0)          # stable
+        assert sorted(perm[:n_valid].tolist()) == sorted(np.nonzero(flat >= 0)[0].tolist())
+        for r in range(n_valid):
+            assert inv[perm[r]] == r
+        assert R == flat.size
+
+
+def pin_dense_mlp(o: Oracle):
+    """One expert, k = 1, weight 1: the oracle must be a dense gated MLP."""
+    T, H, I = 16, 64, 96
+    x = rand_bf16((T, H), 1.0, 2)
+    W13 = rand_bf16((1, 2 * I, H), 0.1, 3)
+    W2 = rand_bf16((1, H, I), 0.1, 4)
+    ids = np.zeros((T, 1), dtype=np.int32)
+    w = np.ones((T, 1), dtype=np.float32)
+
+    xf = torch.from_numpy(bf16_bits_to_f32(x).astype(np.float64))
+    W1 = torch.from_numpy(bf16_bits_to_f32(W13[0, :I]).astype(np.float64))
+    W3 = torch.from_numpy(bf16_bits_to_f32(W13[0, I:]).astype(np.float64))
+    W2d = torch.from_numpy(bf16_bits_to_f32(W2[0]).astype(np.float64))
+    g64, u64 = xf @ W1.T, xf @ W3.T
+    act64 = (F.silu(g64) * u64).numpy()
+    # forward-error bound of the fp32 sums (H terms each) propagated through SiLU(g) * u
+    eps = 2.0 ** -24
+    dg = H * eps * (xf.abs() @ W1.abs().T).numpy()
+    du = H * eps * (xf.abs() @ W3.abs().T).numpy()
+    dact = 1.1 * dg * np.abs(u64.numpy()) + np.abs(F.silu(g64).numpy()) * du + 4 * eps * np.abs(act64)
+
+    a, y = o.expert_rows(x, W13[0], W2[0])
+    a_ref = torch_bf16_bits(act64.astype(np.float32))
+    diff = a != a_ref
+    assert np.count_nonzero(diff) <= max(2, diff.size // 100), "activation differs from dense MLP"
+    assert np.all(near_bf16_midpoint(act64[diff], tol_abs=dact[diff])), \
+        "activation differs away from a rounding midpoint"
+    assert np.all(np.abs(a.astype(np.int32) - a_ref.astype(np.int32))[diff] == 1), "more than one ulp apart"
+
+    y_ref = (torch.from_numpy(bf16_bits_to_f32(a).astype(np.float64)) @ W2d.T).numpy()
+    scale = np.sqrt(np.mean(y_ref ** 2))
+    assert np.max(np.abs(y - y_ref)) <= 1e-5 * scale + 1e-7, "down projection differs from a @ W2^T"
+
+    out_acc, out, bad = o.moe_tokens(x, ids, w, W13, W2)
+    assert bad == 0
+    assert np.max(np.abs(out_acc - y_ref)) <= 1e-5 * scale + 1e-7
+    assert np.array_equal(out, torch_bf16_bits(out_acc))
+
+
+def pin_identity_expert(o: Oracle):
+    """dispatch -> identity expert (y_sorted = x_sorted) -> combine == (sum_j w) * x."""
+    rng = np.random.default_rng(5)
+    T, k, E, H = 50, 3, 7, 32
+    x = rand_bf16((T, H), 1.0, 6)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    ids[3, 1] = -1
+    ids[10, 0] = -1
+    w = rng.uniform(0.05, 1.5, (T, k)).astype(np.float32)
+    counts, offsets, perm, inv, bad = o.dispatch(ids, E)
+    n_rows = int(offsets[-1])
+    x_sorted = x[perm[:n_rows] // k]                     # gather: row -> token of its slot
+    out_acc, out = o.combine_sorted(x_sorted, inv, w)
+    wsum = np.where(ids >= 0, w.astype(np.float64), 0.0).sum(axis=1)
+    ref = wsum[:, None] * bf16_bits_to_f32(x).astype(np.float64)
+    assert np.max(np.abs(out_acc - ref)) <= 1e-6 * np.max(np.abs(ref))
+    # softmax-normalised weights: out reproduces x to within one bf16 ulp
+    wn = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    ids_full = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    _, _, perm, inv, _ = o.dispatch(ids_full, E)
+    _, out = o.combine_sorted(x[perm // k], inv, wn)
+    xf = bf16_bits_to_f32(x)
+    of = bf16_bits_to_f32(out)
+    assert np.all(np.abs(of - xf) <= np.abs(xf) * 2.0 ** -7 + 1e-30)
+
+
+def naive_forward64(x, ids, w, W13, W2, a_bits_hint=None):
+    """Pure-Python fp64 restatement: loops over tokens, slots, outputs, inputs."""
+    T, H = x.shape
+    E, twoI, _ = W13.shape
+    I = twoI // 2
+    k = ids.shape[1]
+    xf = bf16_bits_to_f32(x).astype(np.float64)
+    W13f = bf16_bits_to_f32(W13).astype(np.float64)
+    W2f = bf16_bits_to_f32(W2).astype(np.float64)
+    out = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            e = int(ids[t, j])
+            if e < 0 or e >= E:
+                continue
+            a = [0.0] * I
+            for n in range(I):
+                g = 0.0
+                u = 0.0
+                for h in range(H):
+                    g += xf[t, h] * W13f[e, n, h]
+                    u += xf[t, h] * W13f[e, I + n, h]
+                act = g / (1.0 + math.exp(-g)) * u
+                ab = torch_bf16_bits(np.array([act], dtype=np.float32))[0]
+                if a_bits_hint is not None:
+                    hint = a_bits_hint.get((t, j, n))
+                    if hint is not None and ab != hint and abs(int(ab) - int(hint)) == 1:
+                        ab = hint
+                a[n] = float(bf16_bits_to_f32(np.array([ab], dtype=np.uint16))[0])
+            for m in range(H):
+                y = 0.0
+                for n in range(I):
+                    y += a[n] * W2f[e, m, n]
+                out[t, m] += float(w[t, j]) * y
+    return out
+
+
+def pin_naive_fp64(o: Oracle):
+    T, E, k, H, I = 5, 3, 2, 8, 12
+    rng = np.random.default_rng(7)
+    x = rand_bf16((T, H), 1.0, 8)
+    W13 = rand_bf16((E, 2 * I, H), 0.3, 9)
+    W2 = rand_bf16((E, H, I), 0.3, 10)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    ids[2, 1] = -1
+    w = rng.uniform(0.1, 1.0, (T, k)).astype(np.float32)
+    hint = {}
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            if e >= 0:
+                a, _ = o.expert_rows(x[t:t + 1], W13[e], W2[e])
+                for n in range(I):
+                    hint[(t, j, n)] = a[0, n]
+    ref = naive_forward64(x, ids, w, W13, W2, hint)
+    out_acc, out, bad = o.moe_tokens(x, ids, w, W13, W2)
+    assert bad == 0
+    assert np.max(np.abs(out_acc - ref)) <= 1e-5 * np.max(np.abs(ref)) + 1e-7
+
+
+def pin_streamed_equals_tokens(o: Oracle):
+    T, E, k, H, I = 9, 4, 3, 16, 24
+    rng = np.random.default_rng(11)
+    x = rand_bf16((T, H), 1.0, 12)
+    W13 = rand_bf16((E, 2 * I, H), 0.2, 13)
+    W2 = rand_bf16((E, H, I), 0.2, 14)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    w = rng.uniform(0.1, 1.0, (T, k)).astype(np.float32)
+    acc_a, out_a, _ = o.moe_tokens(x, ids, w, W13, W2)
+    acc_b, out_b = o.moe_forward_streamed(x, ids, w, lambda e: (W13[e], W2[e]), E)
+    assert np.array_equal(acc_a.view(np.uint32), acc_b.view(np.uint32))
+    sub = np.array([1, 4, 7], dtype=np.int32)
+    acc_c, _, _ = o.moe_tokens(x, ids, w, W13, W2, tokens=sub)
+    assert np.array_equal(acc_c.view(np.uint32), acc_a[sub].view(np.uint32))
+
+
+PINS = [pin_round_bf16, pin_dispatch_hand, pin_dispatch_brute, pin_dense_mlp,
+        pin_identity_expert, pin_naive_fp64, pin_streamed_equals_tokens]
+
+
+# ----------------------------------------------------------------------------- tests
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(orc, pin):
+    pin(orc)
+
+
+# Each entry: (name, text in moe_oracle.c, replacement). Every mutation is a
+# plausible slip: a dropped term, a swapped or transposed operand, a wrong
+# sign, a wrong index or stride, a missing rounding, an unstable scatter.
+MUTATIONS = [
+    ("gate_up_swapped",
+     "const uint16_t *wg = W13e + (size_t)n * (size_t)H;\n        const uint16_t *wu = W13e + (size_t)(I + n) * (size_t)H;",
+     "const uint16_t *wu = W13e + (size_t)n * (size_t)H;\n        const uint16_t *wg = W13e + (size_t)(I + n) * (size_t)H;"),
+    ("silu_sign", "g / (1.0f + expf(-g))", "g / (1.0f + expf(g))"),
+    ("dropped_last_h_term", "for (int32_t h = 0; h < H; ++h) {", "for (int32_t h = 0; h < H - 1; ++h) {"),
+    ("activation_not_rounded", "a_scratch[n] = bf16_bits_to_f32(a);", "a_scratch[n] = silu * u;"),
+    ("w2_transposed", "y += a_scratch[n] * bf16_bits_to_f32(w2[n]);",
+     "y += a_scratch[n] * bf16_bits_to_f32(W2e[(size_t)n * (size_t)H + m]);"),
+    ("expert_stride", "W13 + (size_t)e * per13", "W13 + (size_t)e * per2"),
+    ("combine_weight_dropped", "acc[m] += wj * y[m];", "acc[m] += y[m];"),
+    ("combine_sorted_weight_dropped", "acc += w[s] * bf16_bits_to_f32(y_sorted[(size_t)row * H + m]);",
+     "acc += bf16_bits_to_f32(y_sorted[(size_t)row * H + m]);"),
+    ("scatter_unstable", "for (int32_t s = 0; s < R; ++s) {\n        int32_t e = ids[s];\n        if (e >= 0 && e < E) {\n            int32_t row",
+     "for (int32_t s = R - 1; s >= 0; --s) {\n        int32_t e = ids[s];\n        if (e >= 0 && e < E) {\n            int32_t row"),
+    ("offsets_inclusive", "offsets[e + 1] = offsets[e] + counts[e];", "offsets[e + 1] = offsets[e] + counts[e] + (e == 0);"),
+    ("round_half_up", "u += 0x7fffu + keep_lsb;", "u += 0x8000u;"),
+    ("round_truncate", "u += 0x7fffu + keep_lsb;", "u += 0u * keep_lsb;"),
+    ("invalid_id_kept", "if (e >= 0 && e < E)\n            counts[e] += 1;", "if (e >= 0 && e < E + 1 && e != E)\n            counts[e] += 1;\n        if (e == E) counts[0] += 1;"),
+]
+
+
+def run_pins(path: str) -> list:
+    """Run every pin against the oracle build at ``path``; return the names that failed."""
+    lib = Oracle(path)
+    failed = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+        except Exception as ex:  # a shape error or the like also counts as caught
+            failed.append(f"{pin.__name__}:{type(ex).__name__}")
+    return failed
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="gcc not available")
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistakes(tmp_path, name, old, new):
+    src = open(ORACLE_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    c = tmp_path / "mut.c"
+    c.write_text(src.replace(old, new))
+    so = tmp_path / "libmut.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-ffp-contract=off", "-shared", "-fPIC",
+                    "-o", str(so), str(c), "-lm"], check=True)
+    # A mutant may write out of bounds, so it runs in a child process: a crash
+    # there (non-zero exit without our marker) also counts as caught.
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--run-pins", str(so)],
+                       capture_output=True, text=True, env=env, timeout=300)
+    if r.returncode == 0:
+        assert "CAUGHT" in r.stdout, r.stdout + r.stderr
+    else:
+        assert "NOT CAUGHT" not in r.stdout, f"no pin caught the planted mistake {name}"
+
+
+if __name__ == "__main__":
+    if len(sys.argv) == 3 and sys.argv[1] == "--run-pins":
+        failed = run_pins(sys.argv[2])
+        print(("CAUGHT " + ",".join(failed)) if failed else "NOT CAUGHT")
+        sys.exit(0 if failed else 3)
