@@ -1,0 +1,536 @@
+#!/usr/bin/env python
+"""Benchmark of routed-MoE expert execution on one GB300 (or N replicas).
+
+One step = one pass of the whole path (dispatch -> gate-up GEMM with fused
+SiLU*up -> down GEMM -> combine) over each batch of the chosen workload; the
+default workload is the decode configuration: a T=1 batch and a T=8 batch
+(E=384, k=6, H=7168, I=3072), back to back. Weights, routing and activations
+are synthetic (seeded generators in workloads.py) and resident in HBM.
+
+Timing: the step is captured in a CUDA graph (10 steps per graph, each
+forward recording 6 stage events as external graph nodes); W warm-up steps,
+then K steps between two CUDA events, barrier + synchronize on both sides,
+max over ranks. The touched expert weights of one step (~6.8 GB for decode)
+are far larger than the 129 MB L2, so no flush is needed between steps.
+
+Printed: one JSON line (rank 0) with the throughput (TFLOP/s), us/call, the
+roofline of the dominant kernel (the gate-up GEMM) from its event-timed
+duration, an end-to-end number through the public C-ABI call with pinned host
+buffers, SM clocks sampled during the timed region and the CPU oracle's
+throughput on a bounded sample.
+
+``--impl reference`` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wlm  # noqa: E402
+
+WORKLOAD_SETS = {
+    "decode": ["decode1", "decode8"],
+    "tiny": ["tiny"],
+    "decode1": ["decode1"],
+    "decode8": ["decode8"],
+    "small": ["small"],
+    "prefill": ["prefill"],
+    "large": ["large"],
+}
+STAGES = ["dispatch", "gather", "gemm_gate_up", "gemm_down", "combine"]
+LAUNCHES_PER_FORWARD = 7   # count, scan, scatter, gather, gate-up GEMM, down GEMM, combine
+GRAPH_STEPS = 10
+
+# DRAM bytes per launch of the dominant kernel (gate-up GEMM) from an ncu capture:
+# (sha256 of grouped_gemm.cu when captured, {workload: bytes per launch}).
+# A mismatching hash reports traffic as null (kernel changed since the capture).
+NCU_TRAFFIC = {"kernel_sha256": None, "bytes_per_launch": {}}
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def call_accounting(wl: wlm.Workload, ids_np: np.ndarray) -> dict:
+    """FLOPs and algorithmic bytes of one forward over this routing."""
+    R = int(np.count_nonzero(ids_np >= 0))
+    touched = int(np.unique(ids_np[ids_np >= 0]).size)
+    T, H, I = wl.T, wl.H, wl.I
+    return {
+        "flops": 6.0 * R * H * I,
+        "bytes": touched * 6.0 * H * I + 2.0 * T * H * 2 + 8.0 * R,
+        "gemm1_flops": 4.0 * R * H * I,
+        "gemm1_bytes": touched * 4.0 * I * H + 2.0 * R * H + 2.0 * R * I,
+        "gemm2_bytes": touched * 2.0 * H * I + 2.0 * R * I + 2.0 * R * H,
+        "touched_experts": touched,
+        "R": R,
+    }
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_sha() -> str:
+    p = os.path.join(ROOT, "moe_routed_expert_routing_gb300", "csrc", "grouped_gemm.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, local: int, backend: str = "nccl"):
+    if world <= 1:
+        return
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    if backend == "nccl":
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist.init_process_group(backend)
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return float(value)
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": float(max(power)) if power else None}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def time_oracle(inputs, seconds: float, tokens_cap: int | None = None) -> dict:
+    """The oracle, as it stands, on the host cores over a bounded sample."""
+    import oracle
+    oracle.load()
+    cores = len(os.sched_getaffinity(0))
+    flops_done, t_total, runs = 0.0, 0.0, 0
+    samples = []
+    for d in inputs:
+        wl = d["wl"]
+        T = wl.T
+        n_tok = T if tokens_cap is None else max(1, min(T, tokens_cap))
+        tok = np.arange(n_tok, dtype=np.int32) if n_tok == T else wlm.token_subset(wl, n_tok)
+        ids = d["ids_np"]
+        touched = np.unique(ids[tok][ids[tok] >= 0])
+        host_w = {int(e): (wlm.bf16_bits(d["W13"][e]), wlm.bf16_bits(d["W2"][e])) for e in touched}
+        x_bits = wlm.bf16_bits(d["x"])
+        samples.append(dict(wl=wl, tok=tok, ids=ids, w=d["w_np"], x=x_bits, host_w=host_w,
+                            flops=6.0 * int(np.count_nonzero(ids[tok] >= 0)) * wl.H * wl.I))
+    t0 = time.perf_counter()
+    while True:
+        for s in samples:
+            ts = time.perf_counter()
+            oracle.moe_forward_streamed(s["x"], s["ids"], s["w"], lambda e, hw=s["host_w"]: hw[e], s["wl"].E,
+                                        s["tok"])
+            t_total += time.perf_counter() - ts
+            flops_done += s["flops"]
+        runs += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    sample_desc = "; ".join(f"{s['wl'].name}: {s['tok'].size}/{s['wl'].T} tokens" for s in samples)
+    return {"value": flops_done / t_total / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{sample_desc}; repeated {runs}x ({t_total:.1f} s of oracle time)",
+            "seconds": t_total, "flops": flops_done}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def make_inputs(names, device):
+    out = []
+    for n in names:
+        wl = wlm.WORKLOADS[n]
+        ids_np, w_np = wlm.make_routing(wl)
+        W13, W2 = wlm.make_weights(wl, device)
+        d = dict(wl=wl, ids_np=ids_np, w_np=w_np, x=wlm.make_x(wl, device), W13=W13, W2=W2,
+                 ids=torch.from_numpy(ids_np).to(device), w=torch.from_numpy(w_np).to(device))
+        d["acct"] = call_accounting(wl, ids_np)
+        out.append(d)
+    return out
+
+
+def run_ours(args, world, rank, local):
+    from moe_routed_expert_routing_gb300.build import build
+    build()
+    from moe_routed_expert_routing_gb300 import binding as B
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, local)
+    names = WORKLOAD_SETS[args.workload]
+    inputs = make_inputs(names, device)
+    for d in inputs:
+        wl = d["wl"]
+        d["problem"] = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
+        d["bufs"] = B.Buffers(d["problem"], device)
+        d["path"] = B.moe_resolve_path(d["problem"])
+    stream = torch.cuda.Stream(device)
+
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        for e in evs:
+            e.record(stream)   # creates the underlying cudaEvent_t
+        return evs
+
+    # first calls outside capture (function attributes), then capture GRAPH_STEPS steps
+    with torch.cuda.stream(stream):
+        for d in inputs:
+            B.moe_forward(d["problem"], d["x"], d["ids"], d["w"], d["W13"], d["W2"], d["bufs"].expert_offsets,
+                          d["bufs"].perm, d["bufs"].out, d["bufs"].ws, stream=stream)
+    stream.synchronize()
+    for d in inputs:
+        err = B.moe_last_device_error(d["bufs"].ws, stream)
+        if err:
+            raise RuntimeError(f"device error word {err} on {d['wl'].name}")
+
+    G = GRAPH_STEPS if args.steps % GRAPH_STEPS == 0 else 1
+    events = [[new_events() for _ in inputs] for _ in range(G)]
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for g in range(G):
+                for i, d in enumerate(inputs):
+                    B.moe_forward_profiled(d["problem"], d["x"], d["ids"], d["w"], d["W13"], d["W2"],
+                                           d["bufs"].expert_offsets, d["bufs"].perm, d["bufs"].out, d["bufs"].ws,
+                                           events[g][i], stream=stream)
+    n_replays = args.steps // G
+    warm_replays = max(1, math.ceil(args.warmup / G))
+    with torch.cuda.stream(stream):
+        for _ in range(warm_replays):
+            graph.replay()
+    stream.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    clocks.start()
+    time.sleep(0.25)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(n_replays):
+            graph.replay()
+        t_end.record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    barrier(world, device)
+    local_ms = t_start.elapsed_time(t_end)
+    max_ms = max_over_ranks(local_ms, world, device)
+    K = n_replays * G
+
+    # per-stage times of the last G steps of the timed region
+    stage_us = []
+    for i, d in enumerate(inputs):
+        per = np.array([[events[g][i][s].elapsed_time(events[g][i][s + 1]) * 1e3 for s in range(5)]
+                        for g in range(G)])
+        stage_us.append(per.mean(axis=0))
+    for d in inputs:
+        err = B.moe_last_device_error(d["bufs"].ws, stream)
+        if err:
+            raise RuntimeError(f"device error word {err} on {d['wl'].name}")
+
+    flops_step = sum(d["acct"]["flops"] for d in inputs)
+    bytes_step = sum(d["acct"]["bytes"] for d in inputs)
+    ms_per_step = max_ms / K
+    value = world * flops_step * K / (max_ms * 1e-3) / 1e12
+    peaks = load_peaks()
+
+    # dominant kernel: the gate-up GEMM (2/3 of the FLOPs and weight bytes)
+    g1_us = sum(float(s[2]) for s in stage_us)
+    g1_flops = sum(d["acct"]["gemm1_flops"] for d in inputs)
+    g1_bytes = sum(d["acct"]["gemm1_bytes"] for d in inputs)
+    t_tensor = g1_flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_hbm = g1_bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor > t_hbm:
+        achieved = g1_flops / (g1_us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "peak_kind": f"bf16 dense, sustained, {peaks['source']}"}
+    else:
+        achieved = g1_bytes / (g1_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "peak_kind": f"HBM copy, {peaks['source']}"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = "grouped_gemm_kernel (gate-up, SiLU*up epilogue)"
+    roof["algorithmic_per_step"] = g1_flops if roof["bound"] == "tensor" else g1_bytes
+    traffic = None
+    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha():
+        per = [NCU_TRAFFIC["bytes_per_launch"].get(d["wl"].name) for d in inputs]
+        if all(v is not None for v in per):
+            traffic = float(sum(per)) / len(per)
+    roof["traffic"] = traffic
+    # whole-call roofline: slower of FLOPs at tensor peak and touched bytes at HBM bandwidth
+    t_roof = sum(max(d["acct"]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12),
+                     d["acct"]["bytes"] / (peaks["hbm_gbs"] * 1e9)) for d in inputs)
+
+    e2e = run_e2e(B, inputs, stream, device, args, world)
+
+    result = {
+        "metric": "routed-MoE us/call & TFLOPS (dispatch+GEMMs+combine) vs roofline, 1 GB300",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": warm_replays * G,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": " + ".join(d["wl"].describe() for d in inputs),
+            "batches_per_step": [d["wl"].name for d in inputs],
+            "paths": {d["wl"].name: {"path": "small_m" if d["path"][0] == 2 else "tiled", "tile_rows": d["path"][1]}
+                      for d in inputs},
+            "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB of touched weights+activations per step",
+            "timing": f"CUDA graph of {G} step(s) replayed {n_replays}x between CUDA events",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "us_per_call": {d["wl"].name: float(sum(s)) for d, s in zip(inputs, stage_us)},
+        "stages_us": {d["wl"].name: {k: float(v) for k, v in zip(STAGES, s)} for d, s in zip(inputs, stage_us)},
+        "tflops_per_call": {d["wl"].name: d["acct"]["flops"] / (float(sum(s)) * 1e-6) / 1e12
+                            for d, s in zip(inputs, stage_us)},
+        "call_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": ms_per_step * 1e3,
+                          "frac": t_roof * 1e3 / ms_per_step,
+                          "touched_expert_weights_gb": {d["wl"].name: d["acct"]["touched_experts"] * 6 * d["wl"].H
+                                                        * d["wl"].I / 1e9 for d in inputs}},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": LAUNCHES_PER_FORWARD * len(inputs) * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = time_oracle(inputs, args.cpu_seconds,
+                                             tokens_cap=args.cpu_tokens if args.cpu_tokens > 0 else None)
+        result["cpu_baseline"]["value_note"] = "oracle FLOP rate on the sample; a baseline, not the target"
+    elif rank == 0:
+        result["cpu_baseline"] = None
+    return result
+
+
+def run_e2e(B, inputs, stream, device, args, world):
+    """Same metric through the public call with pinned host inputs/outputs copied every step."""
+    host = []
+    for d in inputs:
+        host.append(dict(x=d["x"].cpu().pin_memory(), ids=d["ids"].cpu().pin_memory(),
+                         w=d["w"].cpu().pin_memory(), out=torch.empty_like(d["bufs"].out, device="cpu").pin_memory(),
+                         dx=torch.empty_like(d["x"]), dids=torch.empty_like(d["ids"]), dw=torch.empty_like(d["w"])))
+    steps = max(1, min(args.steps, args.e2e_steps))
+    h2d = sum(h["x"].numel() * 2 + h["ids"].numel() * 4 + h["w"].numel() * 4 for h in host)
+    d2h = sum(h["out"].numel() * 2 for h in host)
+
+    def one_step():
+        for d, h in zip(inputs, host):
+            h["dx"].copy_(h["x"], non_blocking=True)
+            h["dids"].copy_(h["ids"], non_blocking=True)
+            h["dw"].copy_(h["w"], non_blocking=True)
+            B.moe_forward(d["problem"], h["dx"], h["dids"], h["dw"], d["W13"], d["W2"], d["bufs"].expert_offsets,
+                          d["bufs"].perm, d["bufs"].out, d["bufs"].ws, stream=stream)
+            h["out"].copy_(d["bufs"].out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one_step()
+    stream.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(steps):
+            one_step()
+        t1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = max_over_ranks(t0.elapsed_time(t1), world, device)
+    flops_step = sum(d["acct"]["flops"] for d in inputs)
+    return {"value": world * flops_step * steps / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": ms / steps, "api": "moe_forward (eager, C ABI) with pinned host copies each step"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank, local):
+    """The CPU oracle as the reference arm: same workload, metric and unit."""
+    names = WORKLOAD_SETS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    if dev == "cuda":
+        torch.cuda.set_device(local)
+    inputs = make_inputs(names, dev)
+    # size each step so that warmup + steps finish within ~2 minutes
+    budget = max(0.02, 120.0 / (args.steps + args.warmup))
+    calib = time_oracle(inputs, 0.0, tokens_cap=1)
+    per_token = calib["seconds"] / max(1, len(inputs))
+    tokens = max(1, int(budget / max(per_token * len(inputs), 1e-9)))
+    for _ in range(args.warmup):
+        time_oracle(inputs, 0.0, tokens_cap=tokens)
+    flops, secs = 0.0, 0.0
+    for _ in range(args.steps):
+        r = time_oracle(inputs, 0.0, tokens_cap=tokens)
+        flops += r["flops"]
+        secs += r["seconds"]
+    value = flops / secs / 1e12
+    full_flops = sum(d["acct"]["flops"] for d in inputs)
+    ms_per_step = full_flops / (value * 1e12) * 1e3
+    return {
+        "impl": "reference",
+        "metric": "routed-MoE us/call & TFLOPS (dispatch+GEMMs+combine) vs roofline, 1 GB300",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": " + ".join(d["wl"].describe() for d in inputs),
+                   "note": "ms_per_step extrapolated to the full step from the oracle's FLOP rate"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
+                         "sample": f"{tokens} token(s) of each batch per step ({r['sample']})"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_SETS), default="decode")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens per batch in the CPU sample (0 = auto)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_env()
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("--steps must be >= 1 and --warmup >= 0")
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        if args.cpu_tokens == 0:
+            args.cpu_tokens = 1
+        line = run_reference(args, world, rank, local)
+        print(json.dumps(line), flush=True)
+        return 0
+    if args.cpu_tokens == 0:
+        wl_T = max(wlm.WORKLOADS[n].T for n in WORKLOAD_SETS[args.workload])
+        args.cpu_tokens = wl_T if wl_T <= 8 else 16
+    line = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,190 @@
+/*
+ * moe.h -- C ABI of libmoe.so: routed Mixture-of-Experts expert execution on
+ * one NVIDIA GB300 (sm_103a), BF16 weights and activations, fp32 accumulation.
+ *
+ * The operation is the one the TileOps page "[Refactor][MoE] Separate
+ * dispatched expert compute" (PR #1738) composes in its Summary: routed
+ * expert execution = local dispatch -> dispatched-expert MLP compute on a
+ * tight (no-pad) expert-major batch -> combine with the routing weights.
+ * Its Scope fixes BF16 tight/no-pad expert compute and leaves the rows past
+ * the valid-row count unspecified; its Summary keeps valid-row counts on the
+ * GPU behind a static capacity so that a whole call replays under a CUDA
+ * Graph.
+ *
+ * Notation: T tokens (T <= T_max), E experts, k experts per token, H hidden
+ * size, I intermediate size, R = T*k routed slots, slot s = t*k + j,
+ * cap = capacity (rows of the sorted batch, >= T_max*k).
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument except `problem`, `bytes` and `host_code` is a
+ *    DEVICE pointer on the current CUDA device, owned by the caller. The
+ *    library never allocates or frees device memory and keeps no pointer
+ *    after a call returns.
+ *  - bf16 buffers are passed as `void*`: IEEE bfloat16, 2 bytes an element,
+ *    row-major, rows contiguous. Every device buffer must be 16-byte aligned;
+ *    the workspace 256-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls
+ *    only enqueue work on it: they never synchronise the host, never read a
+ *    device value on the host, and are legal inside CUDA stream capture
+ *    (after the first call on a device, which sets up function attributes;
+ *    make that first call outside capture).
+ *  - Host validation fails closed: a status other than MOE_OK means nothing
+ *    was enqueued (DeepGEMM page "MegaMoE: add cluster-paired FP4 weight
+ *    packets", Scope and fallback: unsupported shapes fail closed during host
+ *    validation). MOE_ERR_CUDA means a launch failed; the stream may then
+ *    hold part of the call.
+ *  - Problems seen on the device (an expert id outside [0, E) other than -1,
+ *    a pipeline wait that gave up) never stop a call: they set bits in a
+ *    sticky error word at the start of the workspace, read with
+ *    moe_last_device_error().
+ *  - The path of the expert GEMMs (large-tile or M-small weight streaming)
+ *    is chosen on the host from the static shape only (TileOps page, Review
+ *    follow-up: one effective grouped-GEMM kernel resolved up front, no
+ *    runtime row-policy branch), never from device row counts.
+ */
+#ifndef MOE_GB300_MOE_H
+#define MOE_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_NULL = 1,        /* a required pointer is NULL */
+    MOE_ERR_SHAPE = 2,       /* a size is out of range or inconsistent */
+    MOE_ERR_ALIGN = 3,       /* H or I not a multiple of the tile, or a misaligned buffer */
+    MOE_ERR_WORKSPACE = 4,   /* ws_bytes smaller than moe_workspace_size() */
+    MOE_ERR_UNSUPPORTED = 5, /* no GB300-class device, or a path this build lacks */
+    MOE_ERR_CUDA = 6         /* a CUDA call failed */
+} moe_status_t;
+
+/* Bits of the device error word (moe_last_device_error). */
+#define MOE_DEVERR_BAD_EXPERT_ID 0x1 /* an id outside [0, E) and not -1: slot dropped */
+#define MOE_DEVERR_WAIT_TIMEOUT 0x2  /* a pipeline wait gave up: results of that call are invalid */
+
+/* Expert-GEMM path. AUTO picks from the static shape: M-small when
+ * T_max*k/E <= 16 rows per expert on average, large-tile otherwise. */
+typedef enum moe_path {
+    MOE_PATH_AUTO = 0,
+    MOE_PATH_TILED = 1,   /* 128-row activation tiles x 256-wide weight tiles */
+    MOE_PATH_SMALL_M = 2  /* weights on the MMA M side, token tiles of 16..64 rows */
+} moe_path_t;
+
+typedef struct moe_problem {
+    int32_t T_max;    /* maximum tokens of one call, >= 1 (static) */
+    int32_t E;        /* experts, 1..1024 */
+    int32_t k;        /* experts per token, 1..E */
+    int32_t H;        /* hidden size, multiple of 256 */
+    int32_t I;        /* intermediate size, multiple of 128 */
+    int32_t capacity; /* rows of the sorted batch; 0 means T_max*k; else >= T_max*k */
+    int32_t path;     /* moe_path_t */
+    int32_t reserved; /* must be 0 */
+} moe_problem_t;
+
+/* Bytes of workspace every entry point below needs for `problem` (pure host
+ * arithmetic, no CUDA call). The same workspace serves all entry points; it
+ * holds the device error word, dispatch scratch, the activation h[cap, I]
+ * and, for moe_forward, the sorted batches. */
+moe_status_t moe_workspace_size(const moe_problem_t *problem, size_t *bytes);
+
+/* Which expert-GEMM path `problem` resolves to (MOE_PATH_TILED or
+ * MOE_PATH_SMALL_M) and its token-tile height. Pure host. */
+moe_status_t moe_resolve_path(const moe_problem_t *problem, int32_t *path, int32_t *tile_rows);
+
+/*
+ * Local dispatch: routing -> tight expert-major batch (TileOps page,
+ * Summary: local dispatch; Scope: tight/no-pad batch, valid rows read from
+ * expert_offsets[-1:]).
+ *   topk_ids[T_max, k] int32  expert of each slot; -1 = dropped slot.
+ *   d_num_tokens       int32* device scalar T (<= T_max) read on the GPU, so
+ *                      a captured graph can replay with a new token count;
+ *                      NULL means T = T_max.
+ *   expert_offsets[E+1] int32 out: exclusive prefix sum of the per-expert
+ *                      slot counts; expert_offsets[E] = valid rows.
+ *   perm[cap]   int32  out: perm[row] = slot, for row < expert_offsets[E]
+ *                      (later rows unspecified). Inside one expert the rows
+ *                      follow ascending slot order (stable scatter).
+ *   inv[T_max*k] int32 out: inv[slot] = row, -1 for a dropped slot (slots of
+ *                      tokens >= T are not written).
+ *   x[T_max, H], x_sorted[cap, H] bf16: optional (both NULL or both set);
+ *                      when set, x_sorted[row] = x[perm[row] / k].
+ * Results are bit-exact and deterministic.
+ */
+moe_status_t moe_dispatch(const moe_problem_t *problem, const int32_t *topk_ids,
+                          const int32_t *d_num_tokens, int32_t *expert_offsets,
+                          int32_t *perm, int32_t *inv, const void *x, void *x_sorted,
+                          void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Dispatched-expert MLP on the tight batch (TileOps page, Summary: expert
+ * compute for tight expert-major batches; Review follow-up: fused-gated
+ * epilogue). For every expert e and row r in [expert_offsets[e],
+ * expert_offsets[e+1]):
+ *   h[r, n]  = bf16( SiLU(sum_h x_sorted[r,h] W13[e,n,h]) * sum_h x_sorted[r,h] W13[e,I+n,h] )
+ *   y_sorted[r, m] = sum_n h[r,n] W2[e,m,n]                       (fp32)
+ * with fp32 accumulation on the tensor cores; h lives in the workspace.
+ *   x_sorted[cap, H] bf16, W13[E, 2I, H] bf16 (rows 0..I-1 gate, I..2I-1 up),
+ *   W2[E, H, I] bf16, y_sorted[cap, H] fp32 out (rows past the valid count
+ *   are not written), expert_offsets[E+1] as produced by moe_dispatch.
+ * y_sorted stays fp32 so that the combine rounds to bf16 once, at the end.
+ */
+moe_status_t moe_expert_compute(const moe_problem_t *problem, const void *x_sorted,
+                                const int32_t *expert_offsets, const void *W13, const void *W2,
+                                float *y_sorted, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Combine (TileOps page, Summary: routing weights kept outside expert
+ * compute): out[t, m] = bf16( sum_{j=0..k-1} w[t,j] * y_sorted[inv[t*k+j], m] ),
+ * fp32, j ascending, dropped slots (inv = -1) skipped; deterministic.
+ *   topk_weights[T_max, k] fp32, inv[T_max*k] int32, y_sorted[cap, H] fp32,
+ *   out[T_max, H] bf16 (rows >= T untouched), d_num_tokens as above.
+ */
+moe_status_t moe_combine(const moe_problem_t *problem, const float *y_sorted, const int32_t *inv,
+                         const float *topk_weights, const int32_t *d_num_tokens, void *out,
+                         void *stream);
+
+/*
+ * The whole routed expert execution in one call: dispatch (with the row
+ * gather) -> expert compute -> combine, all on `stream`, with the sorted
+ * batches and inv held in the workspace. Arguments as above; perm and
+ * expert_offsets are still returned to the caller.
+ */
+moe_status_t moe_forward(const moe_problem_t *problem, const void *x, const int32_t *topk_ids,
+                         const float *topk_weights, const int32_t *d_num_tokens, const void *W13,
+                         const void *W2, int32_t *expert_offsets, int32_t *perm, void *out,
+                         void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_forward with stage timestamps: identical work, plus a cudaEventRecord of
+ * stage_events[i] (cudaEvent_t, created by the caller with timing enabled)
+ * at the 6 stage boundaries on `stream`: [0] before dispatch, [1] after the
+ * dispatch kernels, [2] after the row gather, [3] after the gate-up GEMM,
+ * [4] after the down GEMM, [5] after combine. Inside stream capture the
+ * records become external event nodes of the graph (cudaEventRecordExternal),
+ * so a replayed graph still reports per-stage times. No counterpart on the
+ * pages: it exists to time each kernel from the host without a profiler.
+ */
+moe_status_t moe_forward_profiled(const moe_problem_t *problem, const void *x, const int32_t *topk_ids,
+                                  const float *topk_weights, const int32_t *d_num_tokens, const void *W13,
+                                  const void *W2, int32_t *expert_offsets, int32_t *perm, void *out,
+                                  void *ws, size_t ws_bytes, void *stream, void *const *stage_events);
+
+/* Read the sticky device error word of `ws` into *host_code (0 = none).
+ * Synchronises `stream` (the only entry point that does). */
+moe_status_t moe_last_device_error(const void *ws, void *stream, int32_t *host_code);
+
+/* Clear the device error word (enqueued on `stream`). */
+moe_status_t moe_clear_device_error(void *ws, void *stream);
+
+/* Human-readable name of a status. Never NULL. */
+const char *moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_MOE_H */

@@ -1,0 +1,220 @@
+"""Thin ctypes binding of libmoe.so (the C ABI in include/moe.h).
+
+Argument marshalling only: every step of routed expert execution runs in the
+library's CUDA kernels. Torch tensors supply device memory and the current
+stream; their pointers go straight to the C entry points, which keep the same
+names here. If libmoe.so is missing this module raises at load time -- there
+is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import lib_path
+
+MOE_OK = 0
+MOE_PATH_AUTO = 0
+MOE_PATH_TILED = 1
+MOE_PATH_SMALL_M = 2
+MOE_DEVERR_BAD_EXPERT_ID = 0x1
+MOE_DEVERR_WAIT_TIMEOUT = 0x2
+
+#: every symbol include/moe.h declares
+EXPORTED_SYMBOLS = (
+    "moe_workspace_size",
+    "moe_resolve_path",
+    "moe_dispatch",
+    "moe_expert_compute",
+    "moe_combine",
+    "moe_forward",
+    "moe_forward_profiled",
+    "moe_last_device_error",
+    "moe_clear_device_error",
+    "moe_status_string",
+)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+class Problem(ctypes.Structure):
+    """``moe_problem_t``: T_max, E, k, H, I, capacity (0 = T_max*k), path."""
+
+    _fields_ = [
+        ("T_max", ctypes.c_int32),
+        ("E", ctypes.c_int32),
+        ("k", ctypes.c_int32),
+        ("H", ctypes.c_int32),
+        ("I", ctypes.c_int32),
+        ("capacity", ctypes.c_int32),
+        ("path", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+    @classmethod
+    def make(cls, T_max, E, k, H, I, capacity=0, path=MOE_PATH_AUTO):
+        return cls(int(T_max), int(E), int(k), int(H), int(I), int(capacity), int(path), 0)
+
+    @property
+    def cap(self) -> int:
+        return self.capacity or self.T_max * self.k
+
+    def __repr__(self):
+        return (f"Problem(T_max={self.T_max}, E={self.E}, k={self.k}, H={self.H}, I={self.I}, "
+                f"capacity={self.capacity}, path={self.path})")
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_P = ctypes.POINTER(Problem)
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libmoe.so (built by ``build.build()``); raise if it is absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or lib_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"libmoe.so not found at {p}: run moe_routed_expert_routing_gb300.build.build() "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(p)
+    st = ctypes.c_int
+    lib.moe_workspace_size.argtypes = [_P, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_workspace_size.restype = st
+    lib.moe_resolve_path.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+    lib.moe_resolve_path.restype = st
+    lib.moe_dispatch.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.moe_dispatch.restype = st
+    lib.moe_expert_compute.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.moe_expert_compute.restype = st
+    lib.moe_combine.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.moe_combine.restype = st
+    lib.moe_forward.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.moe_forward.restype = st
+    lib.moe_forward_profiled.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                                         _vp, ctypes.POINTER(_vp)]
+    lib.moe_forward_profiled.restype = st
+    lib.moe_last_device_error.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.moe_last_device_error.restype = st
+    lib.moe_clear_device_error.argtypes = [_vp, _vp]
+    lib.moe_clear_device_error.restype = st
+    lib.moe_status_string.argtypes = [ctypes.c_int]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().moe_status_string(int(status)).decode()
+    except Exception:  # pragma: no cover - library absent
+        return f"status {status}"
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libmoe must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def moe_workspace_size(problem: Problem) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().moe_workspace_size(ctypes.byref(problem), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_resolve_path(problem: Problem):
+    path = ctypes.c_int32(0)
+    rows = ctypes.c_int32(0)
+    _check(load_library().moe_resolve_path(ctypes.byref(problem), ctypes.byref(path), ctypes.byref(rows)),
+           "moe_resolve_path")
+    return path.value, rows.value
+
+
+def moe_dispatch(problem, topk_ids, expert_offsets, perm, inv, ws, x=None, x_sorted=None, d_num_tokens=None,
+                 stream=None):
+    _check(load_library().moe_dispatch(ctypes.byref(problem), _ptr(topk_ids), _ptr(d_num_tokens),
+                                       _ptr(expert_offsets), _ptr(perm), _ptr(inv), _ptr(x), _ptr(x_sorted),
+                                       _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "moe_dispatch")
+
+
+def moe_expert_compute(problem, x_sorted, expert_offsets, W13, W2, y_sorted, ws, stream=None):
+    _check(load_library().moe_expert_compute(ctypes.byref(problem), _ptr(x_sorted), _ptr(expert_offsets), _ptr(W13),
+                                             _ptr(W2), _ptr(y_sorted), _ptr(ws), ws.numel() * ws.element_size(),
+                                             _stream(stream)), "moe_expert_compute")
+
+
+def moe_combine(problem, y_sorted, inv, topk_weights, out, d_num_tokens=None, stream=None):
+    _check(load_library().moe_combine(ctypes.byref(problem), _ptr(y_sorted), _ptr(inv), _ptr(topk_weights),
+                                      _ptr(d_num_tokens), _ptr(out), _stream(stream)), "moe_combine")
+
+
+def moe_forward(problem, x, topk_ids, topk_weights, W13, W2, expert_offsets, perm, out, ws, d_num_tokens=None,
+                stream=None):
+    _check(load_library().moe_forward(ctypes.byref(problem), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
+                                      _ptr(d_num_tokens), _ptr(W13), _ptr(W2), _ptr(expert_offsets), _ptr(perm),
+                                      _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_forward")
+
+
+def moe_forward_profiled(problem, x, topk_ids, topk_weights, W13, W2, expert_offsets, perm, out, ws, events,
+                         d_num_tokens=None, stream=None):
+    """moe_forward plus 6 stage events (torch.cuda.Event(enable_timing=True), already recorded once)."""
+    arr = (_vp * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(load_library().moe_forward_profiled(ctypes.byref(problem), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
+                                               _ptr(d_num_tokens), _ptr(W13), _ptr(W2), _ptr(expert_offsets),
+                                               _ptr(perm), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                               _stream(stream), arr), "moe_forward_profiled")
+
+
+def moe_last_device_error(ws, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(load_library().moe_last_device_error(_ptr(ws), _stream(stream), ctypes.byref(code)),
+           "moe_last_device_error")
+    return code.value
+
+
+def moe_clear_device_error(ws, stream=None):
+    _check(load_library().moe_clear_device_error(_ptr(ws), _stream(stream)), "moe_clear_device_error")
+
+
+class Buffers:
+    """Caller-owned device buffers for one problem (plumbing for tests and bench)."""
+
+    def __init__(self, problem: Problem, device="cuda"):
+        p = problem
+        dev = torch.device(device)
+        self.problem = p
+        self.ws = torch.empty(moe_workspace_size(p), dtype=torch.uint8, device=dev)
+        self.expert_offsets = torch.empty(p.E + 1, dtype=torch.int32, device=dev)
+        self.perm = torch.empty(p.cap, dtype=torch.int32, device=dev)
+        self.inv = torch.empty(p.T_max * p.k, dtype=torch.int32, device=dev)
+        self.x_sorted = torch.empty((p.cap, p.H), dtype=torch.bfloat16, device=dev)
+        self.y_sorted = torch.empty((p.cap, p.H), dtype=torch.float32, device=dev)
+        self.out = torch.empty((p.T_max, p.H), dtype=torch.bfloat16, device=dev)
+        self.ws.zero_()

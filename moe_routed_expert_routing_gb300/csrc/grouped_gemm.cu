@@ -1,0 +1,527 @@
+// grouped_gemm.cu -- persistent tcgen05/TMEM grouped GEMM over a tight
+// expert-major batch, for sm_103a.
+//
+// TileOps PR #1738 "Separate dispatched expert compute": Summary (expert
+// MLP compute for tight expert-major batches, GPU-resident row counts);
+// Review follow-up (one effective grouped-GEMM kernel resolved up front; a
+// device-bounded persistent row loop instead of a runtime row-policy branch;
+// one fused-gated epilogue). DeepGEMM PR #394 "MegaMoE: add cluster-paired
+// FP4 weight packets", Motivation: for sparse small-token work, mark one-use
+// routed weight loads EVICT_FIRST.
+//
+// One kernel template, two placements of the operands:
+//
+//  * tiled (large batches): A = 128 activation rows, B = 256 weight rows
+//    (gate-up: 128 gate rows + the 128 matching up rows, so SiLU(gate)*up is
+//    formed in the epilogue of the same CTA; down: 256 output columns).
+//    One tcgen05.mma of M=128, N=256, K=16 per K step.
+//  * M-small (decode, skewed small batches): the weights go on the MMA M
+//    side (128 weight rows) and a tile of 16/32/64 activation rows on N, so
+//    a handful of routed rows still streams whole 128-row weight tiles at
+//    full width. Gate-up issues two MMAs per K step (gate, up) into two TMEM
+//    accumulators. Weight loads carry an L2 evict-first policy.
+//
+// Work unit = (row tile of one expert, output-column tile). Row tiles come
+// from the device-resident expert_offsets: every CTA rebuilds the per-expert
+// tile prefix in shared memory at start, so no host sync and no extra launch
+// is needed and the schedule is identical in every CTA. Units are dealt out
+// round-robin over a persistent grid (one CTA per SM).
+//
+// Warp roles (256 threads): warp 0 = TMA producer, warp 1 = MMA issuer,
+// warp 2 = TMEM allocator, warps 4..7 = epilogue (TMEM lanes 0..127).
+// Shared-memory ring of kStages stages (full/empty mbarriers); two TMEM
+// accumulators so the epilogue of one unit overlaps the main loop of the
+// next. Every wait is bounded: on give-up the CTA raises an abort flag,
+// drains what it has in flight, frees TMEM and sets MOE_DEVERR_WAIT_TIMEOUT.
+//
+// Rows of a tile past the end of its expert belong to the next expert (or
+// are zero-filled by TMA past the capacity): they are computed and never
+// stored.
+//
+// Outputs: the gate-up GEMM stores h in bf16 (the rounding the MLP defines);
+// the down GEMM stores y in fp32, so the only rounding between the fp32
+// accumulators and the combine's fp32 sum is the final one to bf16.
+#include <cuda_bf16.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBK = 64;          // K elements per stage: one 128-byte swizzle row
+constexpr int kUmmaK = 16;       // K of one tcgen05.mma kind::f16
+constexpr unsigned kFull = 0xffffffffu;
+
+struct GemmArgs {
+    const int32_t *expert_offsets;
+    void *out;          // gate-up: bf16 h[cap, n_out]; down: fp32 y[cap, n_out]
+    int32_t *err;
+    uint64_t wait_limit_ns;
+    int E, cap, K, n_out;
+    int w_rows_per_expert;
+    int up_row_offset;
+};
+
+__host__ __device__ constexpr int pow2_at_least(int v)
+{
+    int p = 32;
+    while (p < v)
+        p <<= 1;
+    return p;
+}
+
+template <bool kSmallM, bool kGated, int kTileRows, int kStages>
+struct Cfg {
+    static constexpr int kActRows = kTileRows;
+    static constexpr int kWRows = kSmallM ? (kGated ? 256 : 128) : 256;
+    static constexpr int kActBytes = kActRows * 128;
+    static constexpr int kWBytes = kWRows * 128;
+    static constexpr int kStageBytes = kActBytes + kWBytes;
+    static constexpr int kOutCols = (kSmallM || kGated) ? 128 : 256;    // output columns per unit
+    static constexpr int kAccCols = kSmallM ? (kGated ? 2 * kTileRows : kTileRows) : 256;
+    static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);
+    static constexpr uint32_t kIdesc = kSmallM ? idesc_bf16_f32(128, kTileRows) : idesc_bf16_f32(128, 256);
+    static constexpr int kDynSmem = 1024 + kStages * kStageBytes;
+    static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0, "tiles must keep 1024-byte alignment");
+    static_assert(kTmemCols <= 512, "TMEM has 512 columns");
+    static_assert(!kSmallM || (kTileRows % 16 == 0 && kTileRows >= 16 && kTileRows <= 256), "MMA N");
+};
+
+struct Unit {
+    int e, row0, rows, n0;
+};
+
+// Largest e in [0, E) with tp[e] * scale <= u (tp non-decreasing, tp[0] = 0).
+__device__ __forceinline__ int find_expert(const int *tp, int E, int u, int scale)
+{
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tp[mid] * scale <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+template <bool kSmallM, int kTileRows, int kOutCols>
+__device__ __forceinline__ Unit decode_unit(int u, const int *s_off, const int *s_tp, int E, int NT)
+{
+    Unit t;
+    int rt_local, nt;
+    if (!kSmallM) {
+        // row-tile major, column tiles inner: CTAs running together share A tiles
+        const int rt = u / NT;
+        nt = u - rt * NT;
+        t.e = find_expert(s_tp, E, rt, 1);
+        rt_local = rt - s_tp[t.e];
+    } else {
+        // expert, then column tile, then token tile: the token tiles of one
+        // weight tile are dealt to neighbouring CTAs, which share it in L2
+        t.e = find_expert(s_tp, E, u, NT);
+        const int local = u - s_tp[t.e] * NT;
+        const int tiles = s_tp[t.e + 1] - s_tp[t.e];
+        nt = local / tiles;
+        rt_local = local - nt * tiles;
+    }
+    t.row0 = s_off[t.e] + rt_local * kTileRows;
+    const int left = s_off[t.e + 1] - t.row0;
+    t.rows = left < kTileRows ? left : kTileRows;
+    t.n0 = nt * kOutCols;
+    return t;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u)
+{
+    return (g / (1.0f + expf(-g))) * u;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&p);
+}
+
+template <bool kSmallM, bool kGated, int kTileRows, int kStages>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
+                        const GemmArgs args)
+{
+    using C = Cfg<kSmallM, kGated, kTileRows, kStages>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[kStages];
+    __shared__ __align__(8) uint64_t bar_empty[kStages];
+    __shared__ __align__(8) uint64_t bar_tfull[2];
+    __shared__ __align__(8) uint64_t bar_tempty[2];
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_abort;
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ int s_tp[kMaxExperts + 1];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int E = args.E;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    volatile int *abort_flag = &s_abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&bar_full[s]), 1);
+            mbar_init(smem_u32(&bar_empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bar_tfull[b]), 1);
+            mbar_init(smem_u32(&bar_tempty[b]), 128);
+        }
+        mbar_init(smem_u32(&bar_drain), 1);
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_act);
+        tma_prefetch_desc(&tm_w);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(&s_tmem_base), C::kTmemCols);
+        tmem_relinquish();
+    }
+    for (int i = threadIdx.x; i <= E; i += kThreads)
+        s_off[i] = args.expert_offsets[i];
+    __syncthreads();
+    if (warp == 3) {
+        // per-expert row-tile prefix: s_tp[e] = sum_{e' < e} ceil(rows(e') / kTileRows)
+        int carry = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            int tiles = 0;
+            if (e < E) {
+                int c = s_off[e + 1] - s_off[e];
+                c = c < 0 ? 0 : c;
+                tiles = (c + kTileRows - 1) / kTileRows;
+            }
+            int v = tiles;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(kFull, v, o);
+                if (lane >= o)
+                    v += n;
+            }
+            if (e < E)
+                s_tp[e] = carry + v - tiles;
+            carry += __shfl_sync(kFull, v, 31);
+        }
+        if (lane == 0)
+            s_tp[E] = carry;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = s_tmem_base;
+    const int NT = args.n_out / C::kOutCols;
+    const int total_units = s_tp[E] * NT;
+    const int k_blocks = args.K / kBK;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = kSmallM ? l2_policy_evict_first() : l2_policy_evict_normal();
+            const uint64_t pol_a = l2_policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load in flight, and its phase parity
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+                const Unit t = decode_unit<kSmallM, kTileRows, C::kOutCols>(u, s_off, s_tp, E, NT);
+                const int w_row0 = t.e * args.w_rows_per_expert + t.n0;
+                const int w_row1 = kGated ? t.e * args.w_rows_per_expert + args.up_row_offset + t.n0 : w_row0 + 128;
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, abort_flag, args.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = smem_u32(&bar_full[stage]);
+                    const uint32_t w_dst = smem_u32(smem + stage * C::kStageBytes);
+                    const uint32_t a_dst = w_dst + C::kWBytes;
+                    mbar_arrive_expect_tx(full, C::kStageBytes);
+                    tma_load_2d(w_dst, &tm_w, full, kb * kBK, w_row0, pol_w);
+                    if (C::kWRows == 256)
+                        tma_load_2d(w_dst + 128 * 128, &tm_w, full, kb * kBK, w_row1, pol_w);
+                    tma_load_2d(a_dst, &tm_act, full, kb * kBK, t.row0, pol_a);
+                    issued_mask |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // give-up path: let every load still in flight land before the CTA exits
+                for (int s = 0; s < kStages; ++s)
+                    if (issued_mask & (1u << s)) {
+                        const uint64_t t0 = global_timer_ns();
+                        while (!mbar_try_wait(smem_u32(&bar_full[s]), (issued_parity >> s) & 1u) &&
+                               global_timer_ns() - t0 < args.wait_limit_ns) {
+                        }
+                    }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int local = 0;
+            for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++local) {
+                const int buf = local & 1;
+                const uint32_t use = (local >> 1) & 1;
+                if (!mbar_wait_bounded(smem_u32(&bar_tempty[buf]), use ^ 1u, abort_flag, args.wait_limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * C::kAccCols;
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(smem_u32(&bar_full[stage]), phase, abort_flag, args.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t w_addr = smem_u32(smem + stage * C::kStageBytes);
+                    const uint32_t a_addr = w_addr + C::kWBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                        const uint64_t a_desc = smem_desc_kmajor_sw128(a_addr + kk * 32);
+                        const uint64_t w_desc = smem_desc_kmajor_sw128(w_addr + kk * 32);
+                        if (!kSmallM) {
+                            umma_bf16(d_tmem, a_desc, w_desc, C::kIdesc, acc);
+                        } else {
+                            umma_bf16(d_tmem, w_desc, a_desc, C::kIdesc, acc);
+                            if (kGated) {
+                                const uint64_t up_desc = smem_desc_kmajor_sw128(w_addr + 128 * 128 + kk * 32);
+                                umma_bf16(d_tmem + kTileRows, up_desc, a_desc, C::kIdesc, acc);
+                            }
+                        }
+                    }
+                    umma_commit(smem_u32(&bar_empty[stage]));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok)
+                    umma_commit(smem_u32(&bar_tfull[buf]));
+            }
+            // every MMA this thread issued must be complete before TMEM is freed
+            umma_commit(smem_u32(&bar_drain));
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(smem_u32(&bar_drain), 0) && global_timer_ns() - t0 < args.wait_limit_ns) {
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp - 4;  // TMEM lanes [32q, 32q + 32)
+        int local = 0;
+        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++local) {
+            const Unit t = decode_unit<kSmallM, kTileRows, C::kOutCols>(u, s_off, s_tp, E, NT);
+            const int buf = local & 1;
+            const uint32_t use = (local >> 1) & 1;
+            int ok = 0;
+            if (lane == 0)
+                ok = mbar_wait_bounded(smem_u32(&bar_tfull[buf]), use, abort_flag, args.wait_limit_ns) ? 1 : 0;
+            ok = __shfl_sync(kFull, ok, 0);
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + buf * C::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
+            if (!kSmallM) {
+                const int r = q * 32 + lane;
+                const int row = t.row0 + r;
+                const bool valid = r < t.rows && row >= 0 && row < args.cap;
+                if (kGated) {
+                    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(args.out) + static_cast<size_t>(row) * args.n_out + t.n0;
+#pragma unroll 1
+                    for (int c = 0; c < 128; c += 32) {
+                        uint32_t g[32], v[32];
+                        tmem_ld_32x32b_x32(t_row + c, g);
+                        tmem_ld_32x32b_x32(t_row + 128 + c, v);
+                        tmem_wait_ld();
+                        if (valid) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                uint4 o;
+                                o.x = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 0]), __uint_as_float(v[8 * i + 0])),
+                                                  silu_mul(__uint_as_float(g[8 * i + 1]), __uint_as_float(v[8 * i + 1])));
+                                o.y = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 2]), __uint_as_float(v[8 * i + 2])),
+                                                  silu_mul(__uint_as_float(g[8 * i + 3]), __uint_as_float(v[8 * i + 3])));
+                                o.z = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 4]), __uint_as_float(v[8 * i + 4])),
+                                                  silu_mul(__uint_as_float(g[8 * i + 5]), __uint_as_float(v[8 * i + 5])));
+                                o.w = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 6]), __uint_as_float(v[8 * i + 6])),
+                                                  silu_mul(__uint_as_float(g[8 * i + 7]), __uint_as_float(v[8 * i + 7])));
+                                dst[i] = o;
+                            }
+                        }
+                    }
+                } else {
+                    float *orow = static_cast<float *>(args.out) + static_cast<size_t>(row) * args.n_out + t.n0;
+#pragma unroll 1
+                    for (int c = 0; c < 256; c += 32) {
+                        uint32_t d[32];
+                        tmem_ld_32x32b_x32(t_row + c, d);
+                        tmem_wait_ld();
+                        if (valid) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                dst[i] = make_uint4(d[4 * i + 0], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
+                        }
+                    }
+                }
+            } else {
+                // lane = weight row = output column t.n0 + 32q + lane; TMEM column = token row of the tile
+                const int col = t.n0 + q * 32 + lane;
+#pragma unroll 1
+                for (int c = 0; c < kTileRows; c += 16) {
+                    uint32_t g[16], v[16];
+                    tmem_ld_32x32b_x16(t_row + c, g);
+                    if (kGated)
+                        tmem_ld_32x32b_x16(t_row + kTileRows + c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int rr = c + i;
+                        const int row = t.row0 + rr;
+                        if (rr < t.rows && row >= 0 && row < args.cap) {
+                            const size_t o = static_cast<size_t>(row) * args.n_out + col;
+                            if (kGated)
+                                static_cast<__nv_bfloat16 *>(args.out)[o] =
+                                    __float2bfloat16_rn(silu_mul(__uint_as_float(g[i]), __uint_as_float(v[i])));
+                            else
+                                static_cast<float *>(args.out)[o] = __uint_as_float(g[i]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_tempty[buf]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+    if (threadIdx.x == 0 && s_abort)
+        atomicOr(args.err, MOE_DEVERR_WAIT_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous), box of 64 columns x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <bool kSmallM, bool kGated, int kTileRows, int kStages>
+cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
+{
+    using C = Cfg<kSmallM, kGated, kTileRows, kStages>;
+    auto kern = grouped_gemm_kernel<kSmallM, kGated, kTileRows, kStages>;
+    static int attr_done_for_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (attr_done_for_device != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
+        if (e != cudaSuccess)
+            return e;
+        attr_done_for_device = dev;
+    }
+    CUtensorMap tm_act, tm_w;
+    if (!make_map(&tm_act, p.act, static_cast<uint64_t>(p.cap), static_cast<uint64_t>(p.K), kTileRows) ||
+        !make_map(&tm_w, p.w, static_cast<uint64_t>(p.E) * p.w_rows_per_expert, static_cast<uint64_t>(p.K), 128))
+        return cudaErrorInvalidValue;
+    GemmArgs a;
+    a.expert_offsets = p.expert_offsets;
+    a.out = p.out;
+    a.err = p.err;
+    a.wait_limit_ns = kWaitLimitNs;
+    a.E = p.E;
+    a.cap = p.cap;
+    a.K = p.K;
+    a.n_out = p.n_out;
+    a.w_rows_per_expert = p.w_rows_per_expert;
+    a.up_row_offset = p.up_row_offset;
+    // Upper bound of the units any routing can produce; no more CTAs than that.
+    const long long max_row_tiles = (static_cast<long long>(p.cap) + kTileRows - 1) / kTileRows + p.E;
+    const long long max_units = max_row_tiles * (p.n_out / C::kOutCols);
+    const int grid = static_cast<int>(max_units < num_sms ? (max_units < 1 ? 1 : max_units) : num_sms);
+    kern<<<grid, kThreads, C::kDynSmem, stream>>>(tm_act, tm_w, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream)
+{
+    if (!p.small_m) {
+        if (p.tile_rows != 128)
+            return cudaErrorInvalidValue;
+        return p.gated ? run<false, true, 128, 4>(p, num_sms, stream) : run<false, false, 128, 4>(p, num_sms, stream);
+    }
+    switch (p.tile_rows) {
+    case 16:
+        return p.gated ? run<true, true, 16, 6>(p, num_sms, stream) : run<true, false, 16, 10>(p, num_sms, stream);
+    case 32:
+        return p.gated ? run<true, true, 32, 5>(p, num_sms, stream) : run<true, false, 32, 9>(p, num_sms, stream);
+    case 64:
+        return p.gated ? run<true, true, 64, 5>(p, num_sms, stream) : run<true, false, 64, 8>(p, num_sms, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace moe

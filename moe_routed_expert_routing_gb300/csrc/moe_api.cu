@@ -1,0 +1,402 @@
+// moe_api.cu -- the C ABI of libmoe.so (declared and documented in include/moe.h).
+//
+// Host side only: validation (fails closed before any launch), workspace
+// layout, the static choice of the expert-GEMM path, and the launches.
+// TileOps PR #1738 "Separate dispatched expert compute", Review follow-up:
+// resolve one effective grouped-GEMM kernel up front, before building the
+// gate-up and down steps, so nothing later can undo that choice.
+#include <cstring>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+    size_t err, block_counts, block_base, h, x_sorted, y_sorted, inv, total;
+};
+
+int capacity_of(const moe_problem_t &p) { return p.capacity ? p.capacity : p.T_max * p.k; }
+
+Layout layout_of(const moe_problem_t &p)
+{
+    const size_t cap = static_cast<size_t>(capacity_of(p));
+    const size_t R = static_cast<size_t>(p.T_max) * p.k;
+    const size_t n_blocks = (R + kDispatchSlotsPerBlock - 1) / kDispatchSlotsPerBlock;
+    Layout L;
+    size_t o = 0;
+    L.err = o;
+    o += kAlign;
+    L.block_counts = o;
+    o = align_up(o + sizeof(int32_t) * n_blocks * p.E);
+    L.block_base = o;
+    o = align_up(o + sizeof(int32_t) * n_blocks * p.E);
+    L.h = o;
+    o = align_up(o + 2 * cap * p.I);
+    L.x_sorted = o;
+    o = align_up(o + 2 * cap * p.H);
+    L.y_sorted = o;
+    o = align_up(o + 4 * cap * p.H);
+    L.inv = o;
+    o = align_up(o + sizeof(int32_t) * R);
+    L.total = o;
+    return L;
+}
+
+moe_status_t check_problem(const moe_problem_t *p)
+{
+    if (!p)
+        return MOE_ERR_NULL;
+    if (p->T_max < 1 || p->E < 1 || p->E > kMaxExperts || p->k < 1 || p->k > p->E || p->k > kMaxTopK ||
+        p->H < 1 || p->I < 1 || p->reserved != 0)
+        return MOE_ERR_SHAPE;
+    if (p->path < MOE_PATH_AUTO || p->path > MOE_PATH_SMALL_M)
+        return MOE_ERR_SHAPE;
+    const long long R = static_cast<long long>(p->T_max) * p->k;
+    if (R > (1LL << 28))
+        return MOE_ERR_SHAPE;
+    if (p->capacity != 0 && p->capacity < R)
+        return MOE_ERR_SHAPE;
+    if (static_cast<long long>(p->E) * 2 * p->I > (1LL << 31) || static_cast<long long>(p->E) * p->H > (1LL << 31))
+        return MOE_ERR_SHAPE;
+    if (p->H % 256 != 0 || p->I % 128 != 0)
+        return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+bool aligned256(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 255u) == 0; }
+
+void resolve(const moe_problem_t &p, int *path, int *tile_rows)
+{
+    const double avg_rows = static_cast<double>(p.T_max) * p.k / p.E;
+    int chosen = p.path;
+    if (chosen == MOE_PATH_AUTO)
+        chosen = avg_rows > 16.0 ? MOE_PATH_TILED : MOE_PATH_SMALL_M;
+    *path = chosen;
+    if (chosen == MOE_PATH_TILED)
+        *tile_rows = 128;
+    else
+        *tile_rows = avg_rows <= 2.0 ? 16 : (avg_rows <= 8.0 ? 32 : 64);
+}
+
+// The binary carries sm_103a code only: refuse any other device up front.
+moe_status_t check_device()
+{
+    static int checked_device = -1;
+    static bool ok = false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (checked_device != dev) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        ok = (major == 10 && minor == 3);
+        checked_device = dev;
+    }
+    return ok ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+template <typename T>
+T *at(void *ws, size_t off)
+{
+    return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status_t check_ws(const moe_problem_t &p, const void *ws, size_t ws_bytes)
+{
+    if (!ws)
+        return MOE_ERR_NULL;
+    if (!aligned256(ws))
+        return MOE_ERR_ALIGN;
+    if (ws_bytes < layout_of(p).total)
+        return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status_t record_stage(void *const *stage_events, int i, cudaStream_t s)
+{
+    if (!stage_events)
+        return MOE_OK;
+    return cuda_status(
+        cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), s, cudaEventRecordExternal));
+}
+
+moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *x_sorted, const int32_t *expert_offsets,
+                                    const void *W13, const void *W2, void *y_sorted, void *ws, cudaStream_t s,
+                                    void *const *stage_events = nullptr)
+{
+    const Layout L = layout_of(p);
+    int path = 0, tile_rows = 0;
+    resolve(p, &path, &tile_rows);
+    const int sms = device_sm_count();
+    if (sms <= 0)
+        return MOE_ERR_CUDA;
+    GemmProblem g;
+    g.expert_offsets = expert_offsets;
+    g.err = at<int32_t>(ws, L.err);
+    g.E = p.E;
+    g.cap = capacity_of(p);
+    g.small_m = path == MOE_PATH_SMALL_M;
+    g.tile_rows = tile_rows;
+    // gate-up with the fused SiLU(gate) * up epilogue: x_sorted[cap, H] x W13[E, 2I, H] -> h[cap, I]
+    g.act = x_sorted;
+    g.w = W13;
+    g.out = at<void>(ws, L.h);
+    g.K = p.H;
+    g.n_out = p.I;
+    g.w_rows_per_expert = 2 * p.I;
+    g.up_row_offset = p.I;
+    g.gated = true;
+    moe_status_t st = cuda_status(launch_grouped_gemm(g, sms, s));
+    if (st != MOE_OK)
+        return st;
+    if ((st = record_stage(stage_events, 3, s)) != MOE_OK)
+        return st;
+    // down: h[cap, I] x W2[E, H, I] -> y_sorted[cap, H]
+    g.act = at<void>(ws, L.h);
+    g.w = W2;
+    g.out = y_sorted;
+    g.K = p.I;
+    g.n_out = p.H;
+    g.w_rows_per_expert = p.H;
+    g.up_row_offset = 0;
+    g.gated = false;
+    return cuda_status(launch_grouped_gemm(g, sms, s));
+}
+
+}  // namespace
+
+int device_sm_count()
+{
+    static int cached_dev = -1;
+    static int cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    if (dev != cached_dev) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cached = n;
+        cached_dev = dev;
+    }
+    return cached;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status_t moe_workspace_size(const moe_problem_t *problem, size_t *bytes)
+{
+    if (!bytes)
+        return MOE_ERR_NULL;
+    const moe_status_t st = check_problem(problem);
+    if (st != MOE_OK)
+        return st;
+    *bytes = layout_of(*problem).total;
+    return MOE_OK;
+}
+
+moe_status_t moe_resolve_path(const moe_problem_t *problem, int32_t *path, int32_t *tile_rows)
+{
+    if (!path || !tile_rows)
+        return MOE_ERR_NULL;
+    const moe_status_t st = check_problem(problem);
+    if (st != MOE_OK)
+        return st;
+    int p = 0, t = 0;
+    resolve(*problem, &p, &t);
+    *path = p;
+    *tile_rows = t;
+    return MOE_OK;
+}
+
+moe_status_t moe_dispatch(const moe_problem_t *problem, const int32_t *topk_ids, const int32_t *d_num_tokens,
+                          int32_t *expert_offsets, int32_t *perm, int32_t *inv, const void *x, void *x_sorted,
+                          void *ws, size_t ws_bytes, void *stream)
+{
+    moe_status_t st = check_problem(problem);
+    if (st != MOE_OK)
+        return st;
+    const moe_problem_t &p = *problem;
+    if (!topk_ids || !expert_offsets || !perm || !inv)
+        return MOE_ERR_NULL;
+    if ((x == nullptr) != (x_sorted == nullptr))
+        return MOE_ERR_NULL;
+    if (x && (!aligned16(x) || !aligned16(x_sorted)))
+        return MOE_ERR_ALIGN;
+    if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK)
+        return st;
+    if ((st = check_device()) != MOE_OK)
+        return st;
+    const Layout L = layout_of(p);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = cuda_status(launch_dispatch(topk_ids, d_num_tokens, p.T_max, p.k, p.E, at<int32_t>(ws, L.block_counts),
+                                     at<int32_t>(ws, L.block_base), expert_offsets, perm, inv,
+                                     at<int32_t>(ws, L.err), s));
+    if (st != MOE_OK || !x)
+        return st;
+    return cuda_status(
+        launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, capacity_of(p), x_sorted, device_sm_count(), s));
+}
+
+moe_status_t moe_expert_compute(const moe_problem_t *problem, const void *x_sorted, const int32_t *expert_offsets,
+                                const void *W13, const void *W2, float *y_sorted, void *ws, size_t ws_bytes,
+                                void *stream)
+{
+    moe_status_t st = check_problem(problem);
+    if (st != MOE_OK)
+        return st;
+    const moe_problem_t &p = *problem;
+    if (!x_sorted || !expert_offsets || !W13 || !W2 || !y_sorted)
+        return MOE_ERR_NULL;
+    if (!aligned16(x_sorted) || !aligned16(W13) || !aligned16(W2) || !aligned16(y_sorted))
+        return MOE_ERR_ALIGN;
+    if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK)
+        return st;
+    if ((st = check_device()) != MOE_OK)
+        return st;
+    return enqueue_expert_compute(p, x_sorted, expert_offsets, W13, W2, y_sorted, ws,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_combine(const moe_problem_t *problem, const float *y_sorted, const int32_t *inv,
+                         const float *topk_weights, const int32_t *d_num_tokens, void *out, void *stream)
+{
+    moe_status_t st = check_problem(problem);
+    if (st != MOE_OK)
+        return st;
+    const moe_problem_t &p = *problem;
+    if (!y_sorted || !inv || !topk_weights || !out)
+        return MOE_ERR_NULL;
+    if (!aligned16(y_sorted) || !aligned16(out))
+        return MOE_ERR_ALIGN;
+    if ((st = check_device()) != MOE_OK)
+        return st;
+    return cuda_status(launch_combine(y_sorted, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out,
+                                      device_sm_count(), static_cast<cudaStream_t>(stream)));
+}
+
+static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, const int32_t *topk_ids,
+                                 const float *topk_weights, const int32_t *d_num_tokens, const void *W13,
+                                 const void *W2, int32_t *expert_offsets, int32_t *perm, void *out, void *ws,
+                                 size_t ws_bytes, void *stream, void *const *stage_events)
+{
+    moe_status_t st = check_problem(problem);
+    if (st != MOE_OK)
+        return st;
+    const moe_problem_t &p = *problem;
+    if (!x || !topk_ids || !topk_weights || !W13 || !W2 || !expert_offsets || !perm || !out)
+        return MOE_ERR_NULL;
+    if (!aligned16(x) || !aligned16(W13) || !aligned16(W2) || !aligned16(out))
+        return MOE_ERR_ALIGN;
+    if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK)
+        return st;
+    if ((st = check_device()) != MOE_OK)
+        return st;
+    const Layout L = layout_of(p);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int sms = device_sm_count();
+    int32_t *inv = at<int32_t>(ws, L.inv);
+    void *x_sorted = at<void>(ws, L.x_sorted);
+    float *y_sorted = at<float>(ws, L.y_sorted);
+    auto mark = [&](int i) { return record_stage(stage_events, i, s); };
+    if ((st = mark(0)) != MOE_OK)
+        return st;
+    st = cuda_status(launch_dispatch(topk_ids, d_num_tokens, p.T_max, p.k, p.E, at<int32_t>(ws, L.block_counts),
+                                     at<int32_t>(ws, L.block_base), expert_offsets, perm, inv,
+                                     at<int32_t>(ws, L.err), s));
+    if (st != MOE_OK || (st = mark(1)) != MOE_OK)
+        return st;
+    st = cuda_status(launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, capacity_of(p), x_sorted, sms, s));
+    if (st != MOE_OK || (st = mark(2)) != MOE_OK)
+        return st;
+    st = enqueue_expert_compute(p, x_sorted, expert_offsets, W13, W2, y_sorted, ws, s, stage_events);
+    if (st != MOE_OK || (st = mark(4)) != MOE_OK)
+        return st;
+    st = cuda_status(launch_combine(y_sorted, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out, sms, s));
+    if (st != MOE_OK)
+        return st;
+    return mark(5);
+}
+
+moe_status_t moe_forward(const moe_problem_t *problem, const void *x, const int32_t *topk_ids,
+                         const float *topk_weights, const int32_t *d_num_tokens, const void *W13, const void *W2,
+                         int32_t *expert_offsets, int32_t *perm, void *out, void *ws, size_t ws_bytes, void *stream)
+{
+    return forward_impl(problem, x, topk_ids, topk_weights, d_num_tokens, W13, W2, expert_offsets, perm, out, ws,
+                        ws_bytes, stream, nullptr);
+}
+
+moe_status_t moe_forward_profiled(const moe_problem_t *problem, const void *x, const int32_t *topk_ids,
+                                  const float *topk_weights, const int32_t *d_num_tokens, const void *W13,
+                                  const void *W2, int32_t *expert_offsets, int32_t *perm, void *out, void *ws,
+                                  size_t ws_bytes, void *stream, void *const *stage_events)
+{
+    if (!stage_events)
+        return MOE_ERR_NULL;
+    for (int i = 0; i < 6; ++i)
+        if (!stage_events[i])
+            return MOE_ERR_NULL;
+    return forward_impl(problem, x, topk_ids, topk_weights, d_num_tokens, W13, W2, expert_offsets, perm, out, ws,
+                        ws_bytes, stream, stage_events);
+}
+
+moe_status_t moe_last_device_error(const void *ws, void *stream, int32_t *host_code)
+{
+    if (!ws || !host_code)
+        return MOE_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    *host_code = v;
+    return MOE_OK;
+}
+
+moe_status_t moe_clear_device_error(void *ws, void *stream)
+{
+    if (!ws)
+        return MOE_ERR_NULL;
+    return cudaMemsetAsync(ws, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK
+                                                                                                    : MOE_ERR_CUDA;
+}
+
+const char *moe_status_string(moe_status_t status)
+{
+    switch (status) {
+    case MOE_OK:
+        return "MOE_OK";
+    case MOE_ERR_NULL:
+        return "MOE_ERR_NULL: a required pointer is NULL";
+    case MOE_ERR_SHAPE:
+        return "MOE_ERR_SHAPE: a size is out of range or inconsistent";
+    case MOE_ERR_ALIGN:
+        return "MOE_ERR_ALIGN: H % 256, I % 128 or buffer alignment violated";
+    case MOE_ERR_WORKSPACE:
+        return "MOE_ERR_WORKSPACE: workspace smaller than moe_workspace_size()";
+    case MOE_ERR_UNSUPPORTED:
+        return "MOE_ERR_UNSUPPORTED: device is not sm_103 (GB300)";
+    case MOE_ERR_CUDA:
+        return "MOE_ERR_CUDA: a CUDA call failed";
+    }
+    return "unknown moe_status_t";
+}
+
+}  // extern "C"

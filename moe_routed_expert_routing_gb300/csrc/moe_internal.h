@@ -1,0 +1,58 @@
+// moe_internal.h -- declarations shared by the translation units of libmoe.so
+// (kernels + launchers). Not part of the public ABI (include/moe.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---- limits of this build (checked by host validation) ----
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 64;
+constexpr int kDispatchThreads = 256;
+constexpr int kDispatchSlotsPerBlock = 1024;  // routed slots counted/scattered by one block
+
+// Pipeline waits inside the GEMM kernels give up after this long (the device
+// error word then carries MOE_DEVERR_WAIT_TIMEOUT).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// ---- dispatch (dispatch.cu) ----
+cudaError_t launch_dispatch(const int32_t *topk_ids, const int32_t *d_num_tokens, int T_max, int k, int E,
+                            int32_t *block_counts, int32_t *block_base, int32_t *expert_offsets,
+                            int32_t *perm, int32_t *inv, int32_t *err, cudaStream_t stream);
+
+cudaError_t launch_gather_rows(const void *x, const int32_t *perm, const int32_t *expert_offsets, int E, int k,
+                               int H, int cap, void *x_sorted, int num_sms, cudaStream_t stream);
+
+// ---- combine (combine.cu) ----
+cudaError_t launch_combine(const float *y_sorted, const int32_t *inv, const float *topk_weights,
+                           const int32_t *d_num_tokens, int T_max, int k, int H, void *out, int num_sms,
+                           cudaStream_t stream);
+
+// ---- expert GEMMs (grouped_gemm.cu) ----
+struct GemmProblem {
+    const void *act;          // [cap, K] bf16, rows grouped by expert
+    const void *w;            // [E, w_rows_per_expert, K] bf16
+    void *out;                // [cap, n_out]: bf16 h (gated) or fp32 y (down)
+    const int32_t *expert_offsets;
+    int32_t *err;
+    int E, cap, K, n_out;
+    int w_rows_per_expert;
+    int up_row_offset;        // gated: row offset of the up half inside one expert
+    bool gated;               // fused SiLU(gate) * up epilogue
+    bool small_m;             // weights on the MMA M side (M-small path)
+    int tile_rows;            // activation rows per tile: 128 (tiled) or 16/32/64 (M-small)
+};
+
+cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);
+
+// number of SMs of the current device (cached)
+int device_sm_count();
+
+}  // namespace moe

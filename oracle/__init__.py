@@ -81,7 +81,7 @@ class Oracle:
         lib.oracle_combine_slots.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _f32p, _f32p,
                                              _i32p, _f32p, _u16p]
         lib.oracle_combine_slots.restype = None
-        lib.oracle_combine_sorted.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _u16p, _i32p,
+        lib.oracle_combine_sorted.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _f32p, _i32p,
                                               _f32p, _f32p, _u16p]
         lib.oracle_combine_sorted.restype = None
         lib.oracle_moe_tokens.argtypes = [ctypes.c_int32] * 5 + [_u16p, _i32p, _f32p, _u16p, _u16p,
@@ -148,8 +148,8 @@ class Oracle:
         return out_acc, out
 
     def combine_sorted(self, y_sorted: np.ndarray, inv: np.ndarray, w: np.ndarray):
-        """Combine from the expert-major batch ``y_sorted[rows, H]`` (bf16 bits) via ``inv[T*k]``."""
-        y_sorted = _c(y_sorted, np.uint16)
+        """Combine from the expert-major batch ``y_sorted[rows, H]`` (fp32) via ``inv[T*k]``."""
+        y_sorted = _c(y_sorted, np.float32)
         w = _c(w, np.float32)
         T, k = w.shape
         H = y_sorted.shape[1]
@@ -158,7 +158,7 @@ class Oracle:
         out_acc = np.empty((T, H), dtype=np.float32)
         out = np.empty((T, H), dtype=np.uint16)
         if T:
-            self.lib.oracle_combine_sorted(T, k, H, _p(y_sorted, _u16p), _p(inv, _i32p), _p(w, _f32p),
+            self.lib.oracle_combine_sorted(T, k, H, _p(y_sorted, _f32p), _p(inv, _i32p), _p(w, _f32p),
                                            _p(out_acc, _f32p), _p(out, _u16p))
         return out_acc, out
 

@@ -122,53 +122,66 @@ int32_t oracle_dispatch(int32_t R, int32_t E, const int32_t *ids,
 
 /* ---- 2. expert MLP --------------------------------------------------------- */
 
-/* One routed row through one expert. x[H], W13e[2I, H], W2e[H, I] are bf16
- * bit patterns; a_out[I] receives the bf16 activation, y_out[H] fp32. */
-static void expert_mlp_row(int32_t H, int32_t I, const uint16_t *x,
-                           const uint16_t *W13e, const uint16_t *W2e,
-                           uint16_t *a_out, float *y_out, float *a_scratch)
+/* Gate/up sums for output n of one row, then the rounded activation. */
+static uint16_t gate_up_one(int32_t H, int32_t I, const uint16_t *x, const uint16_t *W13e, int32_t n)
 {
-    for (int32_t n = 0; n < I; ++n) {
-        const uint16_t *wg = W13e + (size_t)n * (size_t)H;
-        const uint16_t *wu = W13e + (size_t)(I + n) * (size_t)H;
-        float g = 0.0f, u = 0.0f;
-        for (int32_t h = 0; h < H; ++h) {
-            float xh = bf16_bits_to_f32(x[h]);
-            g += xh * bf16_bits_to_f32(wg[h]);
-            u += xh * bf16_bits_to_f32(wu[h]);
-        }
-        float silu = g / (1.0f + expf(-g));
-        uint16_t a = f32_to_bf16_bits_rne(silu * u);
-        if (a_out)
-            a_out[n] = a;
-        a_scratch[n] = bf16_bits_to_f32(a);
+    const uint16_t *wg = W13e + (size_t)n * (size_t)H;
+    const uint16_t *wu = W13e + (size_t)(I + n) * (size_t)H;
+    float g = 0.0f, u = 0.0f;
+    for (int32_t h = 0; h < H; ++h) {
+        float xh = bf16_bits_to_f32(x[h]);
+        g += xh * bf16_bits_to_f32(wg[h]);
+        u += xh * bf16_bits_to_f32(wu[h]);
     }
-    for (int32_t m = 0; m < H; ++m) {
-        const uint16_t *w2 = W2e + (size_t)m * (size_t)I;
-        float y = 0.0f;
-        for (int32_t n = 0; n < I; ++n)
-            y += a_scratch[n] * bf16_bits_to_f32(w2[n]);
-        y_out[m] = y;
-    }
+    float silu = g / (1.0f + expf(-g));
+    return f32_to_bf16_bits_rne(silu * u);
 }
 
-/* Several rows through one expert: rows are independent, so they may run on
- * separate threads. x_rows[n_rows, H] -> a_rows[n_rows, I] (nullable),
- * y_rows[n_rows, H]. */
+/* Down-projection sum for output m of one row, from the activation a[I]. */
+static float down_one(int32_t I, const float *a, const uint16_t *W2e, int32_t m)
+{
+    const uint16_t *w2 = W2e + (size_t)m * (size_t)I;
+    float y = 0.0f;
+    for (int32_t n = 0; n < I; ++n)
+        y += a[n] * bf16_bits_to_f32(w2[n]);
+    return y;
+}
+
+/* One routed row through one expert. x[H], W13e[2I, H], W2e[H, I] are bf16
+ * bit patterns; y_out[H] fp32; a_scratch[I] holds the activation. */
+static void expert_mlp_row(int32_t H, int32_t I, const uint16_t *x, const uint16_t *W13e,
+                           const uint16_t *W2e, float *y_out, float *a_scratch)
+{
+    for (int32_t n = 0; n < I; ++n)
+        a_scratch[n] = bf16_bits_to_f32(gate_up_one(H, I, x, W13e, n));
+    for (int32_t m = 0; m < H; ++m)
+        y_out[m] = down_one(I, a_scratch, W2e, m);
+}
+
+/* Several rows through one expert: x_rows[n_rows, H] -> a_rows[n_rows, I]
+ * (bf16 bits, required), y_rows[n_rows, H]. Every output element is independent and
+ * computed exactly as in expert_mlp_row, so the work is spread over
+ * (row, output) pairs; the bits do not depend on the thread count. */
 void oracle_expert_rows(int32_t H, int32_t I, const uint16_t *W13e,
                         const uint16_t *W2e, int32_t n_rows,
                         const uint16_t *x_rows, uint16_t *a_rows, float *y_rows)
 {
-#pragma omp parallel
-    {
-        float *scratch = (float *)malloc(sizeof(float) * (size_t)I);
-#pragma omp for schedule(dynamic, 1)
-        for (int32_t r = 0; r < n_rows; ++r)
-            expert_mlp_row(H, I, x_rows + (size_t)r * H, W13e, W2e,
-                           a_rows ? a_rows + (size_t)r * I : NULL,
-                           y_rows + (size_t)r * H, scratch);
-        free(scratch);
+    float *a = (float *)malloc(sizeof(float) * (size_t)I * (size_t)(n_rows > 0 ? n_rows : 1));
+    int64_t n_ru = (int64_t)n_rows * I;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < n_ru; ++i) {
+        int32_t r = (int32_t)(i / I), n = (int32_t)(i % I);
+        uint16_t ab = gate_up_one(H, I, x_rows + (size_t)r * H, W13e, n);
+        a_rows[i] = ab;
+        a[i] = bf16_bits_to_f32(ab);
     }
+    int64_t n_rm = (int64_t)n_rows * H;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < n_rm; ++i) {
+        int32_t r = (int32_t)(i / H), m = (int32_t)(i % H);
+        y_rows[i] = down_one(I, a + (size_t)r * I, W2e, m);
+    }
+    free(a);
 }
 
 /* ---- 3. combine ------------------------------------------------------------ */
@@ -193,11 +206,11 @@ void oracle_combine_slots(int32_t n_tok, int32_t k, int32_t H,
     }
 }
 
-/* Combine from the expert-major (sorted) batch: y_sorted[rows, H] bf16 bits,
+/* Combine from the expert-major (sorted) batch: y_sorted[rows, H] fp32,
  * inv[T*k] maps slot -> row (-1 = dropped). This is the form the dispatched
  * batch takes between expert compute and combine. */
 void oracle_combine_sorted(int32_t T, int32_t k, int32_t H,
-                           const uint16_t *y_sorted, const int32_t *inv,
+                           const float *y_sorted, const int32_t *inv,
                            const float *w, float *out_acc, uint16_t *out)
 {
     for (int32_t t = 0; t < T; ++t) {
@@ -207,7 +220,7 @@ void oracle_combine_sorted(int32_t T, int32_t k, int32_t H,
                 size_t s = (size_t)t * k + j;
                 int32_t row = inv[s];
                 if (row >= 0)
-                    acc += w[s] * bf16_bits_to_f32(y_sorted[(size_t)row * H + m]);
+                    acc += w[s] * y_sorted[(size_t)row * H + m];
             }
             out_acc[(size_t)t * H + m] = acc;
             out[(size_t)t * H + m] = f32_to_bf16_bits_rne(acc);
@@ -247,7 +260,7 @@ int32_t oracle_moe_tokens(int32_t T, int32_t E, int32_t k, int32_t H, int32_t I,
                     continue;
                 }
                 expert_mlp_row(H, I, x + (size_t)t * H, W13 + (size_t)e * per13,
-                               W2 + (size_t)e * per2, NULL, y, scratch);
+                               W2 + (size_t)e * per2, y, scratch);
                 float wj = w[(size_t)t * k + j];
                 for (int32_t m = 0; m < H; ++m)
                     acc[m] += wj * y[m];

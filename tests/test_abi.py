@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every symbol include/moe.h
+declares; host-side validation fails closed before any CUDA call (no GPU
+needed: every case below returns before the library touches the device)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_routed_expert_routing_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    from moe_routed_expert_routing_gb300 import binding
+    return binding
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    syms = declared_symbols()
+    for s in ("moe_dispatch", "moe_expert_compute", "moe_combine", "moe_forward", "moe_workspace_size"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(build_mod.lib_path())
+    missing = [s for s in declared_symbols() if not hasattr(so, s)]
+    assert not missing, missing
+    assert set(declared_symbols()) == set(lib.EXPORTED_SYMBOLS)
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.status_string(s).startswith("MOE_")
+
+
+def test_workspace_size_and_path(lib):
+    P = lib.Problem.make
+    for (T, E, k, H, I) in [(64, 8, 2, 256, 512), (1, 384, 6, 7168, 3072), (8192, 128, 8, 4096, 1536)]:
+        p = P(T, E, k, H, I)
+        n = lib.moe_workspace_size(p)
+        cap = T * k
+        assert n >= 2 * cap * (I + 2 * H) + 4 * cap
+        assert n % 256 == 0
+    assert lib.moe_resolve_path(P(1, 384, 6, 7168, 3072)) == (lib.MOE_PATH_SMALL_M, 16)
+    assert lib.moe_resolve_path(P(8, 384, 6, 7168, 3072)) == (lib.MOE_PATH_SMALL_M, 16)
+    assert lib.moe_resolve_path(P(128, 256, 8, 7168, 2048)) == (lib.MOE_PATH_SMALL_M, 32)
+    assert lib.moe_resolve_path(P(2048, 384, 6, 7168, 3072)) == (lib.MOE_PATH_TILED, 128)
+    assert lib.moe_resolve_path(P(8192, 128, 8, 4096, 1536)) == (lib.MOE_PATH_TILED, 128)
+    assert lib.moe_resolve_path(P(8192, 128, 8, 4096, 1536, path=lib.MOE_PATH_SMALL_M)) == (lib.MOE_PATH_SMALL_M, 64)
+    assert lib.moe_resolve_path(P(1, 384, 6, 7168, 3072, path=lib.MOE_PATH_TILED)) == (lib.MOE_PATH_TILED, 128)
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(T_max=0), 2), (dict(E=0), 2), (dict(E=1025), 2), (dict(k=0), 2), (dict(k=9, E=8), 2),
+    (dict(H=300), 3), (dict(I=100), 3), (dict(capacity=5), 2), (dict(path=7), 2),
+])
+def test_problem_validation(lib, bad, status):
+    args = dict(T_max=64, E=8, k=2, H=256, I=512, capacity=0, path=0)
+    args.update(bad)
+    p = lib.Problem.make(**args)
+    with pytest.raises(lib.MoeError) as ei:
+        lib.moe_workspace_size(p)
+    assert ei.value.status == status
+
+
+def test_entry_points_fail_closed_without_touching_the_device(lib):
+    so = lib.load_library()
+    p = lib.Problem.make(64, 8, 2, 256, 512)
+    need = lib.moe_workspace_size(p)
+    fake = 1 << 40  # never dereferenced: every call below fails validation first
+    P = ctypes.byref(p)
+    # NULL routing
+    assert so.moe_dispatch(P, None, None, fake, fake, fake, None, None, fake, need, None) == 1
+    # x without x_sorted
+    assert so.moe_dispatch(P, fake, None, fake, fake, fake, fake, None, fake, need, None) == 1
+    # misaligned workspace
+    assert so.moe_dispatch(P, fake, None, fake, fake, fake, None, None, fake + 8, need, None) == 3
+    # undersized workspace
+    assert so.moe_dispatch(P, fake, None, fake, fake, fake, None, None, fake, need - 256, None) == 4
+    assert so.moe_expert_compute(P, fake, fake, fake, fake, fake, fake, need - 1, None) == 4
+    assert so.moe_expert_compute(P, fake + 2, fake, fake, fake, fake, fake, need, None) == 3
+    assert so.moe_expert_compute(P, None, fake, fake, fake, fake, fake, need, None) == 1
+    assert so.moe_combine(P, fake, None, fake, None, fake, None) == 1
+    assert so.moe_combine(P, fake + 4, fake, fake, None, fake, None) == 3
+    assert so.moe_forward(P, fake, fake, fake, None, fake, fake, fake, fake, fake, fake, need - 256, None) == 4
+    assert so.moe_forward(P, fake, fake, None, None, fake, fake, fake, fake, fake, fake, need, None) == 1
+    assert so.moe_forward(None, fake, fake, fake, None, fake, fake, fake, fake, fake, fake, need, None) == 1
+    code = ctypes.c_int32(0)
+    assert so.moe_last_device_error(None, None, ctypes.byref(code)) == 1

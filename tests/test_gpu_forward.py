@@ -1,0 +1,142 @@
+"""GPU parity of the whole routed expert execution (moe_forward) on the five
+workloads against the oracle, plus the behaviours the TileOps page keeps
+tests for (Review follow-up): capacity tail, graph replay, repeated-call
+determinism, and a device-side token count behind a static capacity."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wlm
+from parity import DeviceWorkload, assert_within_tolerance, error_metrics
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from moe_routed_expert_routing_gb300.build import build
+    build()
+    from moe_routed_expert_routing_gb300 import binding
+    return binding
+
+
+def forward(B, p, dw, bufs=None, d_T=None, ids=None, w=None):
+    bufs = bufs or B.Buffers(p)
+    B.moe_forward(p, dw.x, dw.ids if ids is None else ids, dw.w if w is None else w, dw.W13, dw.W2,
+                  bufs.expert_offsets, bufs.perm, bufs.out, bufs.ws, d_num_tokens=d_T)
+    torch.cuda.synchronize()
+    return bufs
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode8", "small", "prefill", "large"])
+def test_forward_matches_oracle(B, name):
+    wl = wlm.WORKLOADS[name]
+    dw = DeviceWorkload(wl)
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
+    bufs = forward(B, p, dw)
+    assert B.moe_last_device_error(bufs.ws) == 0
+    tokens = wlm.token_subset(wl)
+    ref_acc, _ = dw.oracle_out(tokens)
+    got = wlm.bf16_bits(bufs.out)[tokens]
+    m = assert_within_tolerance(got, ref_acc, name)
+    print(name, m)
+
+
+@pytest.mark.parametrize("name,path", [("tiny", 1), ("tiny", 2), ("small", 1), ("decode8", 1)])
+def test_forward_both_paths(B, name, path):
+    wl = wlm.WORKLOADS[name]
+    dw = DeviceWorkload(wl)
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=path)
+    bufs = forward(B, p, dw)
+    tokens = wlm.token_subset(wl, 64 if wl.T > 64 else 0)
+    ref_acc, _ = dw.oracle_out(tokens)
+    assert_within_tolerance(wlm.bf16_bits(bufs.out)[tokens], ref_acc, f"{name} path {path}")
+
+
+def test_repeated_forward_bit_exact(B):
+    wl = wlm.custom("rep", 512, 32, 4, 512, 256, seed=8)
+    dw = DeviceWorkload(wl)
+    for path in (1, 2):
+        p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=path)
+        bufs = forward(B, p, dw)
+        first = bufs.out.clone()
+        for _ in range(3):
+            forward(B, p, dw, bufs)
+            assert torch.equal(first.view(torch.int16), bufs.out.view(torch.int16))
+
+
+def test_capacity_tail_poison_does_not_leak(B):
+    """capacity > T*k and a workspace full of NaN: out is unchanged (tail rows never read)."""
+    wl = wlm.custom("cap", 100, 8, 2, 256, 256, seed=9)
+    dw = DeviceWorkload(wl)
+    p0 = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
+    clean = forward(B, p0, dw).out.clone()
+    for path in (1, 2):
+        p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, capacity=wl.R + 300, path=path)
+        bufs = B.Buffers(p)
+        bufs.ws.fill_(0xFF)                      # every bf16 in the sorted batches = NaN
+        B.moe_clear_device_error(bufs.ws)
+        forward(B, p, dw, bufs)
+        assert torch.isfinite(bufs.out.float()).all()
+        ref_acc, _ = dw.oracle_out()
+        assert_within_tolerance(wlm.bf16_bits(bufs.out), ref_acc, f"capacity tail path {path}")
+        if path == B.moe_resolve_path(p0)[0]:
+            assert torch.equal(bufs.out.view(torch.int16), clean.view(torch.int16))
+
+
+def test_graph_replay_new_routing_and_token_count(B):
+    """Capture one forward with a device token count; replay with new routing
+    contents and other counts: bit-identical to eager calls (no host sync inside)."""
+    wl = wlm.custom("graph", 256, 16, 4, 512, 256, seed=10)
+    dw = DeviceWorkload(wl)
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
+    bufs = B.Buffers(p)
+    d_T = torch.tensor([wl.T], dtype=torch.int32, device="cuda")
+    ids = dw.ids.clone()
+    w = dw.w.clone()
+    forward(B, p, dw, bufs, d_T=d_T, ids=ids, w=w)       # first call outside capture (function attributes)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            B.moe_forward(p, dw.x, ids, w, dw.W13, dw.W2, bufs.expert_offsets, bufs.perm, bufs.out, bufs.ws,
+                          d_num_tokens=d_T, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for seed, T_dev in [(101, wl.T), (102, wl.T // 2), (103, 1)]:
+        ids_np, w_np = wlm.make_routing(wl, seed=seed)
+        ids.copy_(torch.from_numpy(ids_np))
+        w.copy_(torch.from_numpy(w_np))
+        d_T.fill_(T_dev)
+        bufs.out.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        got = bufs.out[:T_dev].clone()
+        eager = B.Buffers(p)
+        eager.out.fill_(0)
+        forward(B, p, dw, eager, d_T=d_T, ids=ids, w=w)
+        assert torch.equal(got.view(torch.int16), eager.out[:T_dev].view(torch.int16))
+        tokens = np.arange(T_dev, dtype=np.int32)
+        ref_acc, _ = dw.oracle_out(tokens, ids_np=ids_np, w_np=w_np)
+        assert_within_tolerance(wlm.bf16_bits(got), ref_acc, f"graph replay T={T_dev}")
+
+
+def test_prefill_dynamic_capacity_sampled(B):
+    """Prefill shape, graph-style static capacity T_max*k with device T in {2048, 1024, 1}."""
+    wl = wlm.WORKLOADS["prefill"]
+    dw = DeviceWorkload(wl)
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
+    bufs = B.Buffers(p)
+    d_T = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for T_dev in (1024, 1):
+        d_T.fill_(T_dev)
+        forward(B, p, dw, bufs, d_T=d_T)
+        off = bufs.expert_offsets.cpu().numpy()
+        assert off[-1] == T_dev * wl.k
+        tokens = np.sort(np.random.default_rng(T_dev).choice(T_dev, min(T_dev, 32), replace=False)).astype(np.int32)
+        ids_np = dw.ids_np[:T_dev]
+        ref_acc, _ = dw.oracle_out(tokens, ids_np=ids_np, w_np=dw.w_np[:T_dev])
+        m = error_metrics(wlm.bf16_bits(bufs.out)[tokens], ref_acc)
+        assert m["max_err_beyond_output_rounding"] <= m["bound"] and m["mean_rel_err"] <= 5e-3, m

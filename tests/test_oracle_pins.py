@@ -206,7 +206,7 @@ def pin_identity_expert(o: Oracle):
     w = rng.uniform(0.05, 1.5, (T, k)).astype(np.float32)
     counts, offsets, perm, inv, bad = o.dispatch(ids, E)
     n_rows = int(offsets[-1])
-    x_sorted = x[perm[:n_rows] // k]                     # gather: row -> token of its slot
+    x_sorted = bf16_bits_to_f32(x[perm[:n_rows] // k])    # gather: row -> token of its slot
     out_acc, out = o.combine_sorted(x_sorted, inv, w)
     wsum = np.where(ids >= 0, w.astype(np.float64), 0.0).sum(axis=1)
     ref = wsum[:, None] * bf16_bits_to_f32(x).astype(np.float64)
@@ -215,7 +215,7 @@ def pin_identity_expert(o: Oracle):
     wn = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
     ids_full = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
     _, _, perm, inv, _ = o.dispatch(ids_full, E)
-    _, out = o.combine_sorted(x[perm // k], inv, wn)
+    _, out = o.combine_sorted(bf16_bits_to_f32(x[perm // k]), inv, wn)
     xf = bf16_bits_to_f32(x)
     of = bf16_bits_to_f32(out)
     assert np.all(np.abs(of - xf) <= np.abs(xf) * 2.0 ** -7 + 1e-30)
@@ -318,17 +318,18 @@ def test_pin(orc, pin):
 # sign, a wrong index or stride, a missing rounding, an unstable scatter.
 MUTATIONS = [
     ("gate_up_swapped",
-     "const uint16_t *wg = W13e + (size_t)n * (size_t)H;\n        const uint16_t *wu = W13e + (size_t)(I + n) * (size_t)H;",
-     "const uint16_t *wu = W13e + (size_t)n * (size_t)H;\n        const uint16_t *wg = W13e + (size_t)(I + n) * (size_t)H;"),
+     "const uint16_t *wg = W13e + (size_t)n * (size_t)H;\n    const uint16_t *wu = W13e + (size_t)(I + n) * (size_t)H;",
+     "const uint16_t *wu = W13e + (size_t)n * (size_t)H;\n    const uint16_t *wg = W13e + (size_t)(I + n) * (size_t)H;"),
     ("silu_sign", "g / (1.0f + expf(-g))", "g / (1.0f + expf(g))"),
     ("dropped_last_h_term", "for (int32_t h = 0; h < H; ++h) {", "for (int32_t h = 0; h < H - 1; ++h) {"),
-    ("activation_not_rounded", "a_scratch[n] = bf16_bits_to_f32(a);", "a_scratch[n] = silu * u;"),
-    ("w2_transposed", "y += a_scratch[n] * bf16_bits_to_f32(w2[n]);",
-     "y += a_scratch[n] * bf16_bits_to_f32(W2e[(size_t)n * (size_t)H + m]);"),
+    ("activation_truncated", "return f32_to_bf16_bits_rne(silu * u);",
+     "{ uint32_t tb; float tv = silu * u; memcpy(&tb, &tv, 4); return (uint16_t)(tb >> 16); }"),
+    ("w2_row_stride", "const uint16_t *w2 = W2e + (size_t)m * (size_t)I;",
+     "const uint16_t *w2 = W2e + (size_t)m * (size_t)(I - 1);"),
     ("expert_stride", "W13 + (size_t)e * per13", "W13 + (size_t)e * per2"),
     ("combine_weight_dropped", "acc[m] += wj * y[m];", "acc[m] += y[m];"),
-    ("combine_sorted_weight_dropped", "acc += w[s] * bf16_bits_to_f32(y_sorted[(size_t)row * H + m]);",
-     "acc += bf16_bits_to_f32(y_sorted[(size_t)row * H + m]);"),
+    ("combine_sorted_weight_dropped", "acc += w[s] * y_sorted[(size_t)row * H + m];",
+     "acc += y_sorted[(size_t)row * H + m];"),
     ("scatter_unstable", "for (int32_t s = 0; s < R; ++s) {\n        int32_t e = ids[s];\n        if (e >= 0 && e < E) {\n            int32_t row",
      "for (int32_t s = R - 1; s >= 0; --s) {\n        int32_t e = ids[s];\n        if (e >= 0 && e < E) {\n            int32_t row"),
     ("offsets_inclusive", "offsets[e + 1] = offsets[e] + counts[e];", "offsets[e + 1] = offsets[e] + counts[e] + (e == 0);"),
