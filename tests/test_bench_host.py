@@ -1,0 +1,85 @@
+"""Host-side logic of bench.py on CPU: the replica aggregation over ranks
+(world size 2, gloo), FLOP/byte accounting, and the reference arm's line."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+import workloads as wlm
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    bench.init_dist(world, rank, backend="gloo")
+    local_ms = 10.0 + 5.0 * rank
+    mx = bench.max_over_ranks(local_ms, world)
+    sm = bench.sum_over_ranks(1.0, world)
+    bench.barrier(world)
+    import torch.distributed as dist
+    dist.destroy_process_group()
+    q.put((rank, mx, sm))
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == [(0, 15.0, 2.0), (1, 15.0, 2.0)]
+
+
+def test_single_rank_aggregation_is_identity():
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.sum_over_ranks(2.0, 1) == 2.0
+
+
+def test_call_accounting():
+    wl = wlm.custom("acc", 4, 8, 2, 256, 128)
+    ids = np.array([[0, 1], [1, 2], [2, 3], [3, -1]], dtype=np.int32)
+    a = bench.call_accounting(wl, ids)
+    assert a["R"] == 7 and a["touched_experts"] == 4
+    assert a["flops"] == 6 * 7 * 256 * 128
+    assert a["gemm1_flops"] == 4 * 7 * 256 * 128
+    assert a["bytes"] == 4 * 6 * 256 * 128 + 2 * 4 * 256 * 2 + 8 * 7
+    assert a["gemm1_bytes"] == 4 * 4 * 128 * 256 + 2 * 7 * 256 + 2 * 7 * 128
+
+
+def test_defaults():
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.impl == "ours" and a.workload == "decode" and a.warmup >= 3
+
+
+def test_reference_arm_line_on_tiny(capsys, monkeypatch):
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    assert bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "1"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+
+
+def test_reference_arm_other_ranks_exit_quietly(capsys, monkeypatch):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    assert bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "0"]) == 0
+    assert capsys.readouterr().out.strip() == ""
