@@ -237,10 +237,17 @@ def time_oracle(inputs, seconds: float, tokens_cap: int | None = None) -> dict:
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def make_inputs(names, device):
+def make_inputs(names, device, experts=0, tokens=0):
+    """Device inputs of the named workloads; experts/tokens > 0 shrink the
+    workload (same per-expert shape) for small profiler captures."""
+    import dataclasses
     out = []
     for n in names:
         wl = wlm.WORKLOADS[n]
+        if experts > 0:
+            wl = dataclasses.replace(wl, E=experts, name=f"{wl.name}_E{experts}")
+        if tokens > 0:
+            wl = dataclasses.replace(wl, T=tokens, name=f"{wl.name}_T{tokens}")
         ids_np, w_np = wlm.make_routing(wl)
         W13, W2 = wlm.make_weights(wl, device)
         d = dict(wl=wl, ids_np=ids_np, w_np=w_np, x=wlm.make_x(wl, device), W13=W13, W2=W2,
@@ -259,7 +266,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(device)
     init_dist(world, local)
     names = WORKLOAD_SETS[args.workload]
-    inputs = make_inputs(names, device)
+    inputs = make_inputs(names, device, args.experts, args.tokens)
     for d in inputs:
         wl = d["wl"]
         d["problem"] = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
@@ -461,7 +468,7 @@ def run_reference(args, world, rank, local):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     if dev == "cuda":
         torch.cuda.set_device(local)
-    inputs = make_inputs(names, dev)
+    inputs = make_inputs(names, dev, args.experts, args.tokens)
     # size each step so that warmup + steps finish within ~2 minutes
     budget = max(0.02, 120.0 / (args.steps + args.warmup))
     calib = time_oracle(inputs, 0.0, tokens_cap=1)
@@ -504,6 +511,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens per batch in the CPU sample (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=0, help="override E (small profiler cases)")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (small profiler cases)")
     return ap.parse_args(argv)
 
 
