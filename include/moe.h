@@ -173,6 +173,34 @@ moe_status_t moe_forward_profiled(const moe_problem_t *problem, const void *x, c
                                   const void *W2, int32_t *expert_offsets, int32_t *perm, void *out,
                                   void *ws, size_t ws_bytes, void *stream, void *const *stage_events);
 
+/*
+ * moe_dispatch for callers that cannot allocate device memory. No counterpart
+ * on the pages: some callers have no way to hand the library a workspace --
+ * a runtime whose device memory is planned once at start-up and may not grow,
+ * or code that runs under stream capture, where cudaMalloc is not allowed.
+ * This variant takes no workspace: its per-block counts live in a static
+ * device array of MOE_NOALLOC_SCRATCH_INTS int32 (1 MiB) inside libmoe.so,
+ * which every GPU that loads the library keeps until the process exits.
+ * Inputs and outputs are the caller's, exactly as in moe_dispatch, and the
+ * results are identical to moe_dispatch's. Differences:
+ *  - Returns MOE_ERR_WORKSPACE, before touching the device, when the problem
+ *    needs more than the static array: 64 + 2 * ceil(T_max*k / 1024) * E ints.
+ *  - The first call on a device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - All calls share the one array, which keeps the previous call's contents
+ *    (each call rewrites what it reads). Calls that overlap on the GPU --
+ *    different streams without ordering between them -- race on it: order
+ *    them on one stream.
+ *  - An invalid expert id is dropped as in moe_dispatch, but its error bit
+ *    goes to the static array and is not reported.
+ * It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define MOE_NOALLOC_SCRATCH_INTS 262144
+moe_status_t moe_dispatch_noalloc(const moe_problem_t *problem, const int32_t *topk_ids,
+                                  const int32_t *d_num_tokens, int32_t *expert_offsets,
+                                  int32_t *perm, int32_t *inv, const void *x, void *x_sorted,
+                                  void *stream);
+
 /* Read the sticky device error word of `ws` into *host_code (0 = none).
  * Synchronises `stream` (the only entry point that does). */
 moe_status_t moe_last_device_error(const void *ws, void *stream, int32_t *host_code);

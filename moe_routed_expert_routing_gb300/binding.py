@@ -31,6 +31,7 @@ EXPORTED_SYMBOLS = (
     "moe_combine",
     "moe_forward",
     "moe_forward_profiled",
+    "moe_dispatch_noalloc",
     "moe_last_device_error",
     "moe_clear_device_error",
     "moe_status_string",
@@ -101,6 +102,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.moe_forward_profiled.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                                          _vp, ctypes.POINTER(_vp)]
     lib.moe_forward_profiled.restype = st
+    lib.moe_dispatch_noalloc.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.moe_dispatch_noalloc.restype = st
     lib.moe_last_device_error.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
     lib.moe_last_device_error.restype = st
     lib.moe_clear_device_error.argtypes = [_vp, _vp]
@@ -161,6 +164,14 @@ def moe_dispatch(problem, topk_ids, expert_offsets, perm, inv, ws, x=None, x_sor
     _check(load_library().moe_dispatch(ctypes.byref(problem), _ptr(topk_ids), _ptr(d_num_tokens),
                                        _ptr(expert_offsets), _ptr(perm), _ptr(inv), _ptr(x), _ptr(x_sorted),
                                        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "moe_dispatch")
+
+
+def moe_dispatch_noalloc(problem, topk_ids, expert_offsets, perm, inv, x=None, x_sorted=None, d_num_tokens=None,
+                         stream=None):
+    """moe_dispatch with no workspace (library-owned static scratch); see include/moe.h."""
+    _check(load_library().moe_dispatch_noalloc(ctypes.byref(problem), _ptr(topk_ids), _ptr(d_num_tokens),
+                                               _ptr(expert_offsets), _ptr(perm), _ptr(inv), _ptr(x),
+                                               _ptr(x_sorted), _stream(stream)), "moe_dispatch_noalloc")
 
 
 def moe_expert_compute(problem, x_sorted, expert_offsets, W13, W2, y_sorted, ws, stream=None):

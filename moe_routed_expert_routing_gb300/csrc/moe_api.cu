@@ -194,6 +194,10 @@ int device_sm_count()
     return cached;
 }
 
+moe_status_t validate_problem(const moe_problem_t *problem) { return check_problem(problem); }
+
+moe_status_t validate_device() { return check_device(); }
+
 }  // namespace moe
 
 using namespace moe;

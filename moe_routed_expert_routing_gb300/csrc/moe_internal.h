@@ -55,4 +55,8 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t 
 // number of SMs of the current device (cached)
 int device_sm_count();
 
+// host validation shared by the entry points (moe_api.cu)
+moe_status_t validate_problem(const moe_problem_t *problem);
+moe_status_t validate_device();
+
 }  // namespace moe
