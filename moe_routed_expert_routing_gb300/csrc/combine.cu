@@ -10,9 +10,9 @@
 // y_sorted is the fp32 output of the down GEMM. fp32 products and sums in
 // ascending j (no fused multiply-add), one rounding at the end: the result
 // is deterministic (no atomics) and identical to a plain sequential loop.
-// One block per token (grid-stride); each thread owns 8 consecutive columns,
-// read as two 16-byte loads per routed row and written as one 16-byte store;
-// the k row indices and weights of the token sit in shared memory.
+// Work item = one token x 1024 columns, so even a single token spreads over
+// several SMs; each thread owns 8 consecutive columns, read as two 16-byte
+// loads per routed row and written as one 16-byte store.
 #include <cuda_bf16.h>
 
 #include "moe_internal.h"
@@ -27,46 +27,67 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&p);
 }
 
-__global__ void __launch_bounds__(128) combine_kernel(const float4 *__restrict__ y_sorted,
-                                                      const int32_t *__restrict__ inv,
-                                                      const float *__restrict__ w, const int32_t *d_num_tokens,
-                                                      int T_max, int k, int vec_per_row, uint4 *__restrict__ out)
+constexpr int kCombineThreads = 128;
+constexpr int kColsPerItem = kCombineThreads * 8;   // one work item = one token x 1024 columns
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float4 *__restrict__ y_sorted,
+                                                                  const int32_t *__restrict__ inv,
+                                                                  const float *__restrict__ w,
+                                                                  const int32_t *d_num_tokens, int T_max, int k,
+                                                                  int vec_per_row, uint4 *__restrict__ out)
 {
-    __shared__ int s_row[kMaxTopK];
-    __shared__ float s_w[kMaxTopK];
+    pdl_wait();
+    pdl_trigger();
     int T = T_max;
     if (d_num_tokens) {
         T = *d_num_tokens;
         T = T < 0 ? 0 : (T > T_max ? T_max : T);
     }
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
-        __syncthreads();
-        for (int j = threadIdx.x; j < k; j += blockDim.x) {
-            s_row[j] = inv[static_cast<size_t>(t) * k + j];
-            s_w[j] = w[static_cast<size_t>(t) * k + j];
-        }
-        __syncthreads();
-        for (int c = threadIdx.x; c < vec_per_row; c += blockDim.x) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int j = 0; j < k; ++j) {
-                const int row = s_row[j];
-                if (row < 0)
+    const int groups = (vec_per_row * 8 + kColsPerItem - 1) / kColsPerItem;
+    const long long items = static_cast<long long>(T) * groups;
+    for (long long item = blockIdx.x; item < items; item += gridDim.x) {
+        const int t = static_cast<int>(item / groups);
+        const int c = static_cast<int>(item % groups) * kCombineThreads + threadIdx.x;   // 8-column chunk
+        if (c >= vec_per_row)
+            continue;
+        const int32_t *inv_t = inv + static_cast<size_t>(t) * k;
+        const float *w_t = w + static_cast<size_t>(t) * k;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // loads of up to four routed rows are issued together, then summed in
+        // ascending j, so the sum is the same sequence of roundings as a plain loop
+        for (int j0 = 0; j0 < k; j0 += 4) {
+            float4 a[4], b[4];
+            int row[4];
+            float wj[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                row[q] = (j0 + q < k) ? __ldg(inv_t + j0 + q) : -1;
+                wj[q] = (j0 + q < k) ? __ldg(w_t + j0 + q) : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (row[q] >= 0) {
+                    const float4 *src = y_sorted + (static_cast<size_t>(row[q]) * vec_per_row + c) * 2;
+                    a[q] = __ldg(src);
+                    b[q] = __ldg(src + 1);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (row[q] < 0)
                     continue;
-                const float4 *src = y_sorted + (static_cast<size_t>(row) * vec_per_row + c) * 2;
-                const float4 a = __ldg(src), b = __ldg(src + 1);
-                const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                const float wj = s_w[j];
+                const float f[8] = {a[q].x, a[q].y, a[q].z, a[q].w, b[q].x, b[q].y, b[q].z, b[q].w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    acc[i] = __fadd_rn(acc[i], __fmul_rn(wj, f[i]));
+                    acc[i] = __fadd_rn(acc[i], __fmul_rn(wj[q], f[i]));
             }
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            out[static_cast<size_t>(t) * vec_per_row + c] = o;
         }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        out[static_cast<size_t>(t) * vec_per_row + c] = o;
     }
 }
 
@@ -76,12 +97,14 @@ cudaError_t launch_combine(const float *y_sorted, const int32_t *inv, const floa
                            const int32_t *d_num_tokens, int T_max, int k, int H, void *out, int num_sms,
                            cudaStream_t stream)
 {
-    int blocks = T_max < num_sms * 16 ? T_max : num_sms * 16;
+    const long long groups = (static_cast<long long>(H) + kColsPerItem - 1) / kColsPerItem;
+    const long long items = static_cast<long long>(T_max) * groups;
+    int blocks = static_cast<int>(items < num_sms * 16LL ? items : num_sms * 16LL);
     if (blocks < 1)
         blocks = 1;
-    combine_kernel<<<blocks, 128, 0, stream>>>(reinterpret_cast<const float4 *>(y_sorted), inv, topk_weights,
-                                               d_num_tokens, T_max, k, H / 8, static_cast<uint4 *>(out));
-    return cudaGetLastError();
+    return launch_k(combine_kernel, dim3(blocks), dim3(kCombineThreads), 0, stream,
+                    reinterpret_cast<const float4 *>(y_sorted), inv, topk_weights, d_num_tokens, T_max, k, H / 8,
+                    static_cast<uint4 *>(out));
 }
 
 }  // namespace moe

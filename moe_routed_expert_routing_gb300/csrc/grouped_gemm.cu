@@ -73,7 +73,7 @@ __host__ __device__ constexpr int pow2_at_least(int v)
     return p;
 }
 
-template <bool kSmallM, bool kGated, int kTileRows, int kStages>
+template <bool kSmallM, bool kGated, int kTileRows, int kStages, int kSplitK>
 struct Cfg {
     static constexpr int kActRows = kTileRows;
     static constexpr int kWRows = kSmallM ? (kGated ? 256 : 128) : 256;
@@ -88,6 +88,7 @@ struct Cfg {
     static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0, "tiles must keep 1024-byte alignment");
     static_assert(kTmemCols <= 512, "TMEM has 512 columns");
     static_assert(!kSmallM || (kTileRows % 16 == 0 && kTileRows >= 16 && kTileRows <= 256), "MMA N");
+    static_assert(kSplitK == 1 || (kSplitK == 2 && kSmallM && !kGated), "split-K: M-small down GEMM only");
 };
 
 struct Unit {
@@ -146,12 +147,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&p);
 }
 
-template <bool kSmallM, bool kGated, int kTileRows, int kStages>
+template <bool kSmallM, bool kGated, int kTileRows, int kStages, int kSplitK>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
                         const GemmArgs args)
 {
-    using C = Cfg<kSmallM, kGated, kTileRows, kStages>;
+    using C = Cfg<kSmallM, kGated, kTileRows, kStages, kSplitK>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
     __shared__ __align__(8) uint64_t bar_empty[kStages];
@@ -190,6 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(&s_tmem_base), C::kTmemCols);
         tmem_relinquish();
     }
+    // everything above overlaps the previous kernel's tail; its outputs
+    // (expert_offsets, the activation rows) are read only after this wait
+    pdl_wait();
+    pdl_trigger();
     for (int i = threadIdx.x; i <= E; i += kThreads)
         s_off[i] = args.expert_offsets[i];
     __syncthreads();
@@ -224,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t tmem_base = s_tmem_base;
     const int NT = args.n_out / C::kOutCols;
-    const int total_units = s_tp[E] * NT;
-    const int k_blocks = args.K / kBK;
+    const int total_units = s_tp[E] * NT * kSplitK;
+    const int k_blocks = args.K / kBK / kSplitK;   // K blocks of one unit
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -237,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load in flight, and its phase parity
             bool ok = true;
             for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-                const Unit t = decode_unit<kSmallM, kTileRows, C::kOutCols>(u, s_off, s_tp, E, NT);
+                const Unit t = decode_unit<kSmallM, kTileRows, C::kOutCols>(u / kSplitK, s_off, s_tp, E, NT);
+                const int kb0 = (u % kSplitK) * k_blocks;
                 const int w_row0 = t.e * args.w_rows_per_expert + t.n0;
                 const int w_row1 = kGated ? t.e * args.w_rows_per_expert + args.up_row_offset + t.n0 : w_row0 + 128;
                 for (int kb = 0; kb < k_blocks; ++kb) {
@@ -249,10 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t w_dst = smem_u32(smem + stage * C::kStageBytes);
                     const uint32_t a_dst = w_dst + C::kWBytes;
                     mbar_arrive_expect_tx(full, C::kStageBytes);
-                    tma_load_2d(w_dst, &tm_w, full, kb * kBK, w_row0, pol_w);
+                    const int kc = (kb0 + kb) * kBK;
+                    tma_load_2d(w_dst, &tm_w, full, kc, w_row0, pol_w);
                     if (C::kWRows == 256)
-                        tma_load_2d(w_dst + 128 * 128, &tm_w, full, kb * kBK, w_row1, pol_w);
-                    tma_load_2d(a_dst, &tm_act, full, kb * kBK, t.row0, pol_a);
+                        tma_load_2d(w_dst + 128 * 128, &tm_w, full, kc, w_row1, pol_w);
+                    tma_load_2d(a_dst, &tm_act, full, kc, t.row0, pol_a);
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
@@ -333,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp - 4;  // TMEM lanes [32q, 32q + 32)
         int local = 0;
         for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++local) {
-            const Unit t = decode_unit<kSmallM, kTileRows, C::kOutCols>(u, s_off, s_tp, E, NT);
+            const Unit t = decode_unit<kSmallM, kTileRows, C::kOutCols>(u / kSplitK, s_off, s_tp, E, NT);
             const int buf = local & 1;
             const uint32_t use = (local >> 1) & 1;
             int ok = 0;
@@ -407,8 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (kGated)
                                 static_cast<__nv_bfloat16 *>(args.out)[o] =
                                     __float2bfloat16_rn(silu_mul(__uint_as_float(g[i]), __uint_as_float(v[i])));
-                            else
+                            else if (kSplitK == 1)
                                 static_cast<float *>(args.out)[o] = __uint_as_float(g[i]);
+                            else  // two K halves into a zeroed output: 0 + a + b == 0 + b + a exactly
+                                atomicAdd(static_cast<float *>(args.out) + o, __uint_as_float(g[i]));
                         }
                     }
                 }
@@ -464,11 +473,11 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
     return r == CUDA_SUCCESS;
 }
 
-template <bool kSmallM, bool kGated, int kTileRows, int kStages>
+template <bool kSmallM, bool kGated, int kTileRows, int kStages, int kSplitK = 1>
 cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
 {
-    using C = Cfg<kSmallM, kGated, kTileRows, kStages>;
-    auto kern = grouped_gemm_kernel<kSmallM, kGated, kTileRows, kStages>;
+    using C = Cfg<kSmallM, kGated, kTileRows, kStages, kSplitK>;
+    auto kern = grouped_gemm_kernel<kSmallM, kGated, kTileRows, kStages, kSplitK>;
     static int attr_done_for_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -497,16 +506,17 @@ cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
     a.up_row_offset = p.up_row_offset;
     // Upper bound of the units any routing can produce; no more CTAs than that.
     const long long max_row_tiles = (static_cast<long long>(p.cap) + kTileRows - 1) / kTileRows + p.E;
-    const long long max_units = max_row_tiles * (p.n_out / C::kOutCols);
+    const long long max_units = max_row_tiles * (p.n_out / C::kOutCols) * kSplitK;
     const int grid = static_cast<int>(max_units < num_sms ? (max_units < 1 ? 1 : max_units) : num_sms);
-    kern<<<grid, kThreads, C::kDynSmem, stream>>>(tm_act, tm_w, a);
-    return cudaGetLastError();
+    return launch_k(kern, dim3(grid), dim3(kThreads), C::kDynSmem, stream, tm_act, tm_w, a);
 }
 
 }  // namespace
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream)
 {
+    if (p.split_k != 1 && (p.split_k != 2 || !p.small_m || p.gated || p.tile_rows != 16 || (p.K / kBK) % 2 != 0))
+        return cudaErrorInvalidValue;
     if (!p.small_m) {
         if (p.tile_rows != 128)
             return cudaErrorInvalidValue;
@@ -514,6 +524,8 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t 
     }
     switch (p.tile_rows) {
     case 16:
+        if (!p.gated && p.split_k == 2)
+            return run<true, false, 16, 10, 2>(p, num_sms, stream);
         return p.gated ? run<true, true, 16, 6>(p, num_sms, stream) : run<true, false, 16, 10>(p, num_sms, stream);
     case 32:
         return p.gated ? run<true, true, 32, 5>(p, num_sms, stream) : run<true, false, 32, 9>(p, num_sms, stream);

@@ -132,15 +132,35 @@ moe_status_t record_stage(void *const *stage_events, int i, cudaStream_t s)
         cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), s, cudaEventRecordExternal));
 }
 
+// Split the M-small down GEMM's K in two when it would otherwise have too few
+// units to fill the GPU (decode: a handful of experts x H/128 weight tiles):
+// the two halves are added into a zeroed fp32 y, which is exact and
+// order-independent for two terms. Decided from static shapes only.
+bool down_split_k(const moe_problem_t &p, int path, int tile_rows, int sms)
+{
+    if (path != MOE_PATH_SMALL_M || tile_rows != 16 || (p.I / 64) % 2 != 0)
+        return false;
+    const long long R_max = static_cast<long long>(p.T_max) * p.k;
+    const long long max_experts = R_max < p.E ? R_max : p.E;
+    return max_experts * (p.H / 128) < 4LL * sms;
+}
+
+// Enqueue both GEMMs. With y_zeroed false and a split down GEMM, y is
+// cleared here first (moe_forward clears it at its start instead, so that the
+// kernels of the call stay back to back on the stream).
 moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *x_sorted, const int32_t *expert_offsets,
-                                    const void *W13, const void *W2, void *y_sorted, void *ws, cudaStream_t s,
-                                    void *const *stage_events = nullptr)
+                                    const void *W13, const void *W2, float *y_sorted, void *ws, cudaStream_t s,
+                                    void *const *stage_events = nullptr, bool y_zeroed = false)
 {
     const Layout L = layout_of(p);
     int path = 0, tile_rows = 0;
     resolve(p, &path, &tile_rows);
     const int sms = device_sm_count();
     if (sms <= 0)
+        return MOE_ERR_CUDA;
+    const bool split = down_split_k(p, path, tile_rows, sms);
+    if (split && !y_zeroed &&
+        cudaMemsetAsync(y_sorted, 0, sizeof(float) * static_cast<size_t>(capacity_of(p)) * p.H, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     GemmProblem g;
     g.expert_offsets = expert_offsets;
@@ -149,6 +169,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *x_sorted
     g.cap = capacity_of(p);
     g.small_m = path == MOE_PATH_SMALL_M;
     g.tile_rows = tile_rows;
+    g.split_k = 1;
     // gate-up with the fused SiLU(gate) * up epilogue: x_sorted[cap, H] x W13[E, 2I, H] -> h[cap, I]
     g.act = x_sorted;
     g.w = W13;
@@ -163,7 +184,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *x_sorted
         return st;
     if ((st = record_stage(stage_events, 3, s)) != MOE_OK)
         return st;
-    // down: h[cap, I] x W2[E, H, I] -> y_sorted[cap, H]
+    // down: h[cap, I] x W2[E, H, I] -> y_sorted[cap, H] (fp32)
     g.act = at<void>(ws, L.h);
     g.w = W2;
     g.out = y_sorted;
@@ -172,6 +193,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *x_sorted
     g.w_rows_per_expert = p.H;
     g.up_row_offset = 0;
     g.gated = false;
+    g.split_k = split ? 2 : 1;
     return cuda_status(launch_grouped_gemm(g, sms, s));
 }
 
@@ -319,6 +341,12 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
     void *x_sorted = at<void>(ws, L.x_sorted);
     float *y_sorted = at<float>(ws, L.y_sorted);
     auto mark = [&](int i) { return record_stage(stage_events, i, s); };
+    int path = 0, tile_rows = 0;
+    resolve(p, &path, &tile_rows);
+    const bool split = down_split_k(p, path, tile_rows, sms);
+    if (split && cudaMemsetAsync(y_sorted, 0, sizeof(float) * static_cast<size_t>(capacity_of(p)) * p.H, s) !=
+                     cudaSuccess)
+        return MOE_ERR_CUDA;
     if ((st = mark(0)) != MOE_OK)
         return st;
     st = cuda_status(launch_dispatch(topk_ids, d_num_tokens, p.T_max, p.k, p.E, at<int32_t>(ws, L.block_counts),
@@ -329,7 +357,7 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
     st = cuda_status(launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, capacity_of(p), x_sorted, sms, s));
     if (st != MOE_OK || (st = mark(2)) != MOE_OK)
         return st;
-    st = enqueue_expert_compute(p, x_sorted, expert_offsets, W13, W2, y_sorted, ws, s, stage_events);
+    st = enqueue_expert_compute(p, x_sorted, expert_offsets, W13, W2, y_sorted, ws, s, stage_events, true);
     if (st != MOE_OK || (st = mark(4)) != MOE_OK)
         return st;
     st = cuda_status(launch_combine(y_sorted, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out, sms, s));

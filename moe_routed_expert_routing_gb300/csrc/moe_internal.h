@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -21,6 +22,33 @@ constexpr int kDispatchSlotsPerBlock = 1024;  // routed slots counted/scattered 
 // Pipeline waits inside the GEMM kernels give up after this long (the device
 // error word then carries MOE_DEVERR_WAIT_TIMEOUT).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// ---- programmatic dependent launch ----
+// Every kernel of the library may start while the kernel before it on the
+// stream is still finishing (cudaLaunchAttributeProgrammaticStreamSerialization):
+// it runs its prologue, then waits (griddepcontrol.wait) for the previous
+// grid's completion and memory before touching any global data, and signals
+// its own dependents early (griddepcontrol.launch_dependents). Since every
+// kernel waits before it finishes, completion stays transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- dispatch (dispatch.cu) ----
 cudaError_t launch_dispatch(const int32_t *topk_ids, const int32_t *d_num_tokens, int T_max, int k, int E,
@@ -48,6 +76,7 @@ struct GemmProblem {
     bool gated;               // fused SiLU(gate) * up epilogue
     bool small_m;             // weights on the MMA M side (M-small path)
     int tile_rows;            // activation rows per tile: 128 (tiled) or 16/32/64 (M-small)
+    int split_k;              // 1, or 2 (M-small down GEMM only: two K halves added into a zeroed fp32 out)
 };
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);

@@ -68,9 +68,10 @@ def test_dispatch_dynamic_token_count(B, T_dev):
     check_dispatch_exact(ids_np, wl.E, offs, perm, inv, T=T_dev)
 
 
-def test_dispatch_dropped_and_invalid_ids(B):
+@pytest.mark.parametrize("T", [300, 900])   # one dispatch block / three blocks
+def test_dispatch_dropped_and_invalid_ids(B, T):
     rng = np.random.default_rng(4)
-    T, k, E = 300, 3, 10
+    k, E = 3, 10
     ids_np = rng.integers(0, E, (T, k)).astype(np.int32)
     ids_np[5, 1] = -1
     ids_np[17, 0] = -1

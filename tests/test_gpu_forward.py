@@ -55,8 +55,10 @@ def test_forward_both_paths(B, name, path):
     assert_within_tolerance(wlm.bf16_bits(bufs.out)[tokens], ref_acc, f"{name} path {path}")
 
 
-def test_repeated_forward_bit_exact(B):
-    wl = wlm.custom("rep", 512, 32, 4, 512, 256, seed=8)
+@pytest.mark.parametrize("shape", [(512, 32, 4, 512, 256), (4, 64, 4, 512, 256)])
+def test_repeated_forward_bit_exact(B, shape):
+    """Repeated calls give identical bits (the second shape takes the split-K down GEMM)."""
+    wl = wlm.custom("rep", *shape, seed=8)
     dw = DeviceWorkload(wl)
     for path in (1, 2):
         p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=path)
