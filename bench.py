@@ -294,9 +294,21 @@ def run_ours(args, world, rank, local):
     G = GRAPH_STEPS if args.steps % GRAPH_STEPS == 0 else 1
     events = [[new_events() for _ in inputs] for _ in range(G)]
     stream.synchronize()
+    # headline graph: G steps of plain moe_forward (kernels back to back, so
+    # programmatic dependent launch overlaps each kernel's prologue with the
+    # previous kernel's tail); profiled graph: the same steps with stage events
+    # (event nodes sit between the kernels and cut that overlap)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(graph, stream=stream):
+            for g in range(G):
+                for d in inputs:
+                    B.moe_forward(d["problem"], d["x"], d["ids"], d["w"], d["W13"], d["W2"],
+                                  d["bufs"].expert_offsets, d["bufs"].perm, d["bufs"].out, d["bufs"].ws,
+                                  stream=stream)
+    graph_prof = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph_prof, stream=stream):
             for g in range(G):
                 for i, d in enumerate(inputs):
                     B.moe_forward_profiled(d["problem"], d["x"], d["ids"], d["w"], d["W13"], d["W2"],
@@ -307,6 +319,7 @@ def run_ours(args, world, rank, local):
     with torch.cuda.stream(stream):
         for _ in range(warm_replays):
             graph.replay()
+            graph_prof.replay()
     stream.synchronize()
 
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
@@ -329,7 +342,20 @@ def run_ours(args, world, rank, local):
     max_ms = max_over_ranks(local_ms, world, device)
     K = n_replays * G
 
-    # per-stage times of the last G steps of the timed region
+    # kernel durations: the profiled graph over its own timed region (same
+    # steps, stage events between the kernels); the last G steps are read back
+    prof_replays = max(1, min(n_replays, 20))
+    p_start = torch.cuda.Event(enable_timing=True)
+    p_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        p_start.record(stream)
+        for _ in range(prof_replays):
+            graph_prof.replay()
+        p_end.record(stream)
+    torch.cuda.synchronize(device)
+    prof_ms_per_step = p_start.elapsed_time(p_end) / (prof_replays * G)
+
+    # per-stage times of the last G steps of the profiled region
     stage_us = []
     for i, d in enumerate(inputs):
         per = np.array([[events[g][i][s].elapsed_time(events[g][i][s + 1]) * 1e3 for s in range(5)]
@@ -394,10 +420,12 @@ def run_ours(args, world, rank, local):
             "paths": {d["wl"].name: {"path": "small_m" if d["path"][0] == 2 else "tiled", "tile_rows": d["path"][1]}
                       for d in inputs},
             "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB of touched weights+activations per step",
-            "timing": f"CUDA graph of {G} step(s) replayed {n_replays}x between CUDA events",
+            "timing": (f"CUDA graph of {G} step(s) replayed {n_replays}x between CUDA events; kernel and stage "
+                       f"times from a second graph of the same steps with stage events, replayed {prof_replays}x"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "us_per_call": {d["wl"].name: float(sum(s)) for d, s in zip(inputs, stage_us)},
+        "profiled_ms_per_step": prof_ms_per_step,
         "stages_us": {d["wl"].name: {k: float(v) for k, v in zip(STAGES, s)} for d, s in zip(inputs, stage_us)},
         "tflops_per_call": {d["wl"].name: d["acct"]["flops"] / (float(sum(s)) * 1e-6) / 1e12
                             for d, s in zip(inputs, stage_us)},

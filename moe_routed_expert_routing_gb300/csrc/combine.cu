@@ -95,14 +95,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float4 *
 
 cudaError_t launch_combine(const float *y_sorted, const int32_t *inv, const float *topk_weights,
                            const int32_t *d_num_tokens, int T_max, int k, int H, void *out, int num_sms,
-                           cudaStream_t stream)
+                           cudaStream_t stream, bool pdl)
 {
     const long long groups = (static_cast<long long>(H) + kColsPerItem - 1) / kColsPerItem;
     const long long items = static_cast<long long>(T_max) * groups;
     int blocks = static_cast<int>(items < num_sms * 16LL ? items : num_sms * 16LL);
     if (blocks < 1)
         blocks = 1;
-    return launch_k(combine_kernel, dim3(blocks), dim3(kCombineThreads), 0, stream,
+    return launch_k(combine_kernel, dim3(blocks), dim3(kCombineThreads), 0, stream, pdl,
                     reinterpret_cast<const float4 *>(y_sorted), inv, topk_weights, d_num_tokens, T_max, k, H / 8,
                     static_cast<uint4 *>(out));
 }

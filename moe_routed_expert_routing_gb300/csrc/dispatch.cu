@@ -261,23 +261,42 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_scatter_kernel(
     scatter_slots(ids, s0, s1, E, cursor, wcnt, perm, inv);
 }
 
-// x_sorted[row] = x[perm[row] / k] for row < expert_offsets[E]; one warp a row, 16-byte moves.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restrict__ x,
-                                                          const int32_t *__restrict__ perm,
-                                                          const int32_t *__restrict__ expert_offsets, int E, int k,
-                                                          int vec_per_row, int cap, uint4 *__restrict__ x_sorted)
+// x_sorted[row] = x[perm[row] / k] for row < expert_offsets[E]. Work item =
+// (row, 2048-column slice): a thread moves 16 bytes of each of the item's
+// columns groups, four loads in flight before the stores.
+constexpr int kGatherThreads = 256;
+constexpr int kGatherVecPerItem = kGatherThreads * 4;   // 16-byte vectors per work item
+
+__global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const uint4 *__restrict__ x,
+                                                                     const int32_t *__restrict__ perm,
+                                                                     const int32_t *__restrict__ expert_offsets,
+                                                                     int E, int k, int vec_per_row, int cap,
+                                                                     uint4 *__restrict__ x_sorted)
 {
     pdl_wait();
     pdl_trigger();
     const int n_rows = min(expert_offsets[E], cap);
-    const int lane = threadIdx.x & 31;
-    const int warps = blockDim.x >> 5;
-    for (int r = blockIdx.x * warps + (threadIdx.x >> 5); r < n_rows; r += gridDim.x * warps) {
+    const int slices = (vec_per_row + kGatherVecPerItem - 1) / kGatherVecPerItem;
+    const long long items = static_cast<long long>(n_rows) * slices;
+    for (long long item = blockIdx.x; item < items; item += gridDim.x) {
+        const int r = static_cast<int>(item / slices);
+        const int c0 = static_cast<int>(item % slices) * kGatherVecPerItem + threadIdx.x;
         const int t = perm[r] / k;
         const uint4 *src = x + static_cast<size_t>(t) * vec_per_row;
         uint4 *dst = x_sorted + static_cast<size_t>(r) * vec_per_row;
-        for (int c = lane; c < vec_per_row; c += 32)
-            dst[c] = __ldg(src + c);
+        uint4 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int c = c0 + q * kGatherThreads;
+            if (c < vec_per_row)
+                v[q] = __ldg(src + c);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int c = c0 + q * kGatherThreads;
+            if (c < vec_per_row)
+                dst[c] = v[q];
+        }
     }
 }
 
@@ -285,36 +304,36 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restric
 
 cudaError_t launch_dispatch(const int32_t *topk_ids, const int32_t *d_num_tokens, int T_max, int k, int E,
                             int32_t *block_counts, int32_t *block_base, int32_t *expert_offsets, int32_t *perm,
-                            int32_t *inv, int32_t *err, cudaStream_t stream)
+                            int32_t *inv, int32_t *err, cudaStream_t stream, bool pdl)
 {
     const int R_max = T_max * k;
     const int n_blocks = (R_max + kDispatchSlotsPerBlock - 1) / kDispatchSlotsPerBlock;
     const size_t scatter_smem = sizeof(int) * E * (1 + kWarps);
     if (n_blocks <= 1)
-        return launch_k(dispatch_single_block_kernel, dim3(1), dim3(kDispatchThreads), scatter_smem, stream, topk_ids,
-                        d_num_tokens, T_max, k, E, expert_offsets, perm, inv, err);
+        return launch_k(dispatch_single_block_kernel, dim3(1), dim3(kDispatchThreads), scatter_smem, stream, pdl,
+                        topk_ids, d_num_tokens, T_max, k, E, expert_offsets, perm, inv, err);
     const size_t count_smem = sizeof(int) * E;
-    cudaError_t e = launch_k(dispatch_count_kernel, dim3(n_blocks), dim3(kDispatchThreads), count_smem, stream,
+    cudaError_t e = launch_k(dispatch_count_kernel, dim3(n_blocks), dim3(kDispatchThreads), count_smem, stream, pdl,
                              topk_ids, d_num_tokens, T_max, k, E, block_counts, err);
     if (e != cudaSuccess)
         return e;
-    e = launch_k(dispatch_scan_kernel, dim3(1), dim3(1024), 0, stream, block_counts, n_blocks, E, block_base,
+    e = launch_k(dispatch_scan_kernel, dim3(1), dim3(1024), 0, stream, pdl, block_counts, n_blocks, E, block_base,
                  expert_offsets);
     if (e != cudaSuccess)
         return e;
-    return launch_k(dispatch_scatter_kernel, dim3(n_blocks), dim3(kDispatchThreads), scatter_smem, stream, topk_ids,
-                    d_num_tokens, T_max, k, E, block_base, perm, inv);
+    return launch_k(dispatch_scatter_kernel, dim3(n_blocks), dim3(kDispatchThreads), scatter_smem, stream, pdl,
+                    topk_ids, d_num_tokens, T_max, k, E, block_base, perm, inv);
 }
 
 cudaError_t launch_gather_rows(const void *x, const int32_t *perm, const int32_t *expert_offsets, int E, int k, int H,
-                               int cap, void *x_sorted, int num_sms, cudaStream_t stream)
+                               int cap, void *x_sorted, int num_sms, cudaStream_t stream, bool pdl)
 {
-    const int warps_per_block = 8;
-    int blocks = (cap + warps_per_block - 1) / warps_per_block;
-    blocks = blocks < num_sms * 8 ? blocks : num_sms * 8;
+    const long long slices = (H / 8 + kGatherVecPerItem - 1) / kGatherVecPerItem;
+    const long long items = static_cast<long long>(cap) * slices;
+    int blocks = static_cast<int>(items < num_sms * 8LL ? items : num_sms * 8LL);
     if (blocks < 1)
         blocks = 1;
-    return launch_k(gather_rows_kernel, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
+    return launch_k(gather_rows_kernel, dim3(blocks), dim3(kGatherThreads), 0, stream, pdl,
                     static_cast<const uint4 *>(x), perm, expert_offsets, E, k, H / 8, cap,
                     static_cast<uint4 *>(x_sorted));
 }

@@ -75,13 +75,13 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_problem_t *problem, const
     if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (moe::launch_dispatch(topk_ids, d_num_tokens, p.T_max, p.k, p.E, block_counts, block_base, expert_offsets,
-                             perm, inv, err, s) != cudaSuccess)
+                             perm, inv, err, s, moe::use_pdl(p)) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (!x)
         return MOE_OK;
     const int cap = p.capacity ? p.capacity : p.T_max * p.k;
-    if (moe::launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, cap, x_sorted, moe::device_sm_count(), s) !=
-        cudaSuccess)
+    if (moe::launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, cap, x_sorted, moe::device_sm_count(), s,
+                                moe::use_pdl(p)) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -192,9 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     // everything above overlaps the previous kernel's tail; its outputs
-    // (expert_offsets, the activation rows) are read only after this wait
+    // (expert_offsets, the activation rows) are read only after this wait.
+    // Dependents are released only when this CTA is done (end of kernel):
+    // released early, their CTAs would sit on the SMs next to this
+    // persistent grid and take issue slots from it.
     pdl_wait();
-    pdl_trigger();
     for (int i = threadIdx.x; i <= E; i += kThreads)
         s_off[i] = args.expert_offsets[i];
     __syncthreads();
@@ -429,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    pdl_trigger();
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
@@ -508,7 +511,7 @@ cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
     const long long max_row_tiles = (static_cast<long long>(p.cap) + kTileRows - 1) / kTileRows + p.E;
     const long long max_units = max_row_tiles * (p.n_out / C::kOutCols) * kSplitK;
     const int grid = static_cast<int>(max_units < num_sms ? (max_units < 1 ? 1 : max_units) : num_sms);
-    return launch_k(kern, dim3(grid), dim3(kThreads), C::kDynSmem, stream, tm_act, tm_w, a);
+    return launch_k(kern, dim3(grid), dim3(kThreads), C::kDynSmem, stream, p.pdl, tm_act, tm_w, a);
 }
 
 }  // namespace

@@ -170,6 +170,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *x_sorted
     g.small_m = path == MOE_PATH_SMALL_M;
     g.tile_rows = tile_rows;
     g.split_k = 1;
+    g.pdl = path == MOE_PATH_SMALL_M;
     // gate-up with the fused SiLU(gate) * up epilogue: x_sorted[cap, H] x W13[E, 2I, H] -> h[cap, I]
     g.act = x_sorted;
     g.w = W13;
@@ -219,6 +220,13 @@ int device_sm_count()
 moe_status_t validate_problem(const moe_problem_t *problem) { return check_problem(problem); }
 
 moe_status_t validate_device() { return check_device(); }
+
+bool use_pdl(const moe_problem_t &problem)
+{
+    int path = 0, tile_rows = 0;
+    resolve(problem, &path, &tile_rows);
+    return path == MOE_PATH_SMALL_M;
+}
 
 }  // namespace moe
 
@@ -273,11 +281,11 @@ moe_status_t moe_dispatch(const moe_problem_t *problem, const int32_t *topk_ids,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     st = cuda_status(launch_dispatch(topk_ids, d_num_tokens, p.T_max, p.k, p.E, at<int32_t>(ws, L.block_counts),
                                      at<int32_t>(ws, L.block_base), expert_offsets, perm, inv,
-                                     at<int32_t>(ws, L.err), s));
+                                     at<int32_t>(ws, L.err), s, use_pdl(p)));
     if (st != MOE_OK || !x)
         return st;
-    return cuda_status(
-        launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, capacity_of(p), x_sorted, device_sm_count(), s));
+    return cuda_status(launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, capacity_of(p), x_sorted,
+                                          device_sm_count(), s, use_pdl(p)));
 }
 
 moe_status_t moe_expert_compute(const moe_problem_t *problem, const void *x_sorted, const int32_t *expert_offsets,
@@ -314,7 +322,7 @@ moe_status_t moe_combine(const moe_problem_t *problem, const float *y_sorted, co
     if ((st = check_device()) != MOE_OK)
         return st;
     return cuda_status(launch_combine(y_sorted, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out,
-                                      device_sm_count(), static_cast<cudaStream_t>(stream)));
+                                      device_sm_count(), static_cast<cudaStream_t>(stream), use_pdl(p)));
 }
 
 static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, const int32_t *topk_ids,
@@ -351,16 +359,18 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
         return st;
     st = cuda_status(launch_dispatch(topk_ids, d_num_tokens, p.T_max, p.k, p.E, at<int32_t>(ws, L.block_counts),
                                      at<int32_t>(ws, L.block_base), expert_offsets, perm, inv,
-                                     at<int32_t>(ws, L.err), s));
+                                     at<int32_t>(ws, L.err), s, use_pdl(p)));
     if (st != MOE_OK || (st = mark(1)) != MOE_OK)
         return st;
-    st = cuda_status(launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, capacity_of(p), x_sorted, sms, s));
+    st = cuda_status(
+        launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, capacity_of(p), x_sorted, sms, s, use_pdl(p)));
     if (st != MOE_OK || (st = mark(2)) != MOE_OK)
         return st;
     st = enqueue_expert_compute(p, x_sorted, expert_offsets, W13, W2, y_sorted, ws, s, stage_events, true);
     if (st != MOE_OK || (st = mark(4)) != MOE_OK)
         return st;
-    st = cuda_status(launch_combine(y_sorted, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out, sms, s));
+    st = cuda_status(
+        launch_combine(y_sorted, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out, sms, s, use_pdl(p)));
     if (st != MOE_OK)
         return st;
     return mark(5);
