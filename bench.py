@@ -269,7 +269,7 @@ def run_ours(args, world, rank, local):
     inputs = make_inputs(names, device, args.experts, args.tokens)
     for d in inputs:
         wl = d["wl"]
-        d["problem"] = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
+        d["problem"] = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path)
         d["bufs"] = B.Buffers(d["problem"], device)
         d["path"] = B.moe_resolve_path(d["problem"])
     stream = torch.cuda.Stream(device)
@@ -417,8 +417,8 @@ def run_ours(args, world, rank, local):
         "config": {
             "workload": " + ".join(d["wl"].describe() for d in inputs),
             "batches_per_step": [d["wl"].name for d in inputs],
-            "paths": {d["wl"].name: {"path": "small_m" if d["path"][0] == 2 else "tiled", "tile_rows": d["path"][1]}
-                      for d in inputs},
+            "paths": {d["wl"].name: {"path": {1: "tiled (CTA pairs)", 2: "small_m", 3: "tiled (1 CTA)"}[d["path"][0]],
+                                     "tile_rows": d["path"][1]} for d in inputs},
             "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB of touched weights+activations per step",
             "timing": (f"CUDA graph of {G} step(s) replayed {n_replays}x between CUDA events; kernel and stage "
                        f"times from a second graph of the same steps with stage events, replayed {prof_replays}x"),
@@ -541,6 +541,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--experts", type=int, default=0, help="override E (small profiler cases)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (small profiler cases)")
+    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="expert-GEMM path: 0 auto, 1 tiled CTA pairs, 2 M-small, 3 tiled single CTA")
     return ap.parse_args(argv)
 
 

@@ -70,8 +70,9 @@ typedef enum moe_status {
  * T_max*k/E <= 16 rows per expert on average, large-tile otherwise. */
 typedef enum moe_path {
     MOE_PATH_AUTO = 0,
-    MOE_PATH_TILED = 1,   /* 128-row activation tiles x 256-wide weight tiles */
-    MOE_PATH_SMALL_M = 2  /* weights on the MMA M side, token tiles of 16..64 rows */
+    MOE_PATH_TILED = 1,       /* 256-row activation tiles x 256-row weight tiles on CTA pairs (cta_group::2) */
+    MOE_PATH_SMALL_M = 2,     /* weights on the MMA M side, token tiles of 16..64 rows */
+    MOE_PATH_TILED_1CTA = 3   /* 128 x 256 tiles on single CTAs; never chosen by AUTO (for comparison) */
 } moe_path_t;
 
 typedef struct moe_problem {
@@ -91,8 +92,9 @@ typedef struct moe_problem {
  * and, for moe_forward, the sorted batches. */
 moe_status_t moe_workspace_size(const moe_problem_t *problem, size_t *bytes);
 
-/* Which expert-GEMM path `problem` resolves to (MOE_PATH_TILED or
- * MOE_PATH_SMALL_M) and its token-tile height. Pure host. */
+/* Which expert-GEMM path `problem` resolves to (MOE_PATH_TILED,
+ * MOE_PATH_SMALL_M or MOE_PATH_TILED_1CTA) and its activation-tile height
+ * per CTA. Pure host. */
 moe_status_t moe_resolve_path(const moe_problem_t *problem, int32_t *path, int32_t *tile_rows);
 
 /*

@@ -19,6 +19,7 @@ MOE_OK = 0
 MOE_PATH_AUTO = 0
 MOE_PATH_TILED = 1
 MOE_PATH_SMALL_M = 2
+MOE_PATH_TILED_1CTA = 3
 MOE_DEVERR_BAD_EXPERT_ID = 0x1
 MOE_DEVERR_WAIT_TIMEOUT = 0x2
 

@@ -147,6 +147,81 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&p);
 }
 
+// Per-expert row-tile prefix (one warp): s_tp[e] = sum_{e' < e} ceil(rows(e') / tile_rows).
+__device__ __forceinline__ void build_tile_prefix(const int *s_off, int *s_tp, int E, int tile_rows, int lane)
+{
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        int tiles = 0;
+        if (e < E) {
+            int c = s_off[e + 1] - s_off[e];
+            c = c < 0 ? 0 : c;
+            tiles = (c + tile_rows - 1) / tile_rows;
+        }
+        int v = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(kFull, v, o);
+            if (lane >= o)
+                v += n;
+        }
+        if (e < E)
+            s_tp[e] = carry + v - tiles;
+        carry += __shfl_sync(kFull, v, 31);
+    }
+    if (lane == 0)
+        s_tp[E] = carry;
+}
+
+// Epilogue of a 128-row tiled unit: this thread owns accumulator row `row`
+// (TMEM lane base already in t_row). Gate-up: columns [0,128) gate, [128,256)
+// up -> bf16 SiLU(gate)*up into h; down: 256 fp32 columns into y.
+template <bool kGated>
+__device__ __forceinline__ void tiled_epilogue(uint32_t t_row, const GemmArgs &args, int row, bool valid, int n0)
+{
+    if (kGated) {
+        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(args.out) + static_cast<size_t>(row) * args.n_out + n0;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+            uint32_t g[32], v[32];
+            tmem_ld_32x32b_x32(t_row + c, g);
+            tmem_ld_32x32b_x32(t_row + 128 + c, v);
+            tmem_wait_ld();
+            if (valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint4 o;
+                    o.x = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 0]), __uint_as_float(v[8 * i + 0])),
+                                      silu_mul(__uint_as_float(g[8 * i + 1]), __uint_as_float(v[8 * i + 1])));
+                    o.y = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 2]), __uint_as_float(v[8 * i + 2])),
+                                      silu_mul(__uint_as_float(g[8 * i + 3]), __uint_as_float(v[8 * i + 3])));
+                    o.z = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 4]), __uint_as_float(v[8 * i + 4])),
+                                      silu_mul(__uint_as_float(g[8 * i + 5]), __uint_as_float(v[8 * i + 5])));
+                    o.w = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 6]), __uint_as_float(v[8 * i + 6])),
+                                      silu_mul(__uint_as_float(g[8 * i + 7]), __uint_as_float(v[8 * i + 7])));
+                    dst[i] = o;
+                }
+            }
+        }
+    } else {
+        float *orow = static_cast<float *>(args.out) + static_cast<size_t>(row) * args.n_out + n0;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+            uint32_t d[32];
+            tmem_ld_32x32b_x32(t_row + c, d);
+            tmem_wait_ld();
+            if (valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_uint4(d[4 * i + 0], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
+            }
+        }
+    }
+}
+
 template <bool kSmallM, bool kGated, int kTileRows, int kStages, int kSplitK>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
@@ -200,31 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i <= E; i += kThreads)
         s_off[i] = args.expert_offsets[i];
     __syncthreads();
-    if (warp == 3) {
-        // per-expert row-tile prefix: s_tp[e] = sum_{e' < e} ceil(rows(e') / kTileRows)
-        int carry = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            int tiles = 0;
-            if (e < E) {
-                int c = s_off[e + 1] - s_off[e];
-                c = c < 0 ? 0 : c;
-                tiles = (c + kTileRows - 1) / kTileRows;
-            }
-            int v = tiles;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(kFull, v, o);
-                if (lane >= o)
-                    v += n;
-            }
-            if (e < E)
-                s_tp[e] = carry + v - tiles;
-            carry += __shfl_sync(kFull, v, 31);
-        }
-        if (lane == 0)
-            s_tp[E] = carry;
-    }
+    if (warp == 3)
+        build_tile_prefix(s_off, s_tp, E, kTileRows, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -356,47 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!kSmallM) {
                 const int r = q * 32 + lane;
                 const int row = t.row0 + r;
-                const bool valid = r < t.rows && row >= 0 && row < args.cap;
-                if (kGated) {
-                    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(args.out) + static_cast<size_t>(row) * args.n_out + t.n0;
-#pragma unroll 1
-                    for (int c = 0; c < 128; c += 32) {
-                        uint32_t g[32], v[32];
-                        tmem_ld_32x32b_x32(t_row + c, g);
-                        tmem_ld_32x32b_x32(t_row + 128 + c, v);
-                        tmem_wait_ld();
-                        if (valid) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                uint4 o;
-                                o.x = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 0]), __uint_as_float(v[8 * i + 0])),
-                                                  silu_mul(__uint_as_float(g[8 * i + 1]), __uint_as_float(v[8 * i + 1])));
-                                o.y = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 2]), __uint_as_float(v[8 * i + 2])),
-                                                  silu_mul(__uint_as_float(g[8 * i + 3]), __uint_as_float(v[8 * i + 3])));
-                                o.z = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 4]), __uint_as_float(v[8 * i + 4])),
-                                                  silu_mul(__uint_as_float(g[8 * i + 5]), __uint_as_float(v[8 * i + 5])));
-                                o.w = pack_bf16x2(silu_mul(__uint_as_float(g[8 * i + 6]), __uint_as_float(v[8 * i + 6])),
-                                                  silu_mul(__uint_as_float(g[8 * i + 7]), __uint_as_float(v[8 * i + 7])));
-                                dst[i] = o;
-                            }
-                        }
-                    }
-                } else {
-                    float *orow = static_cast<float *>(args.out) + static_cast<size_t>(row) * args.n_out + t.n0;
-#pragma unroll 1
-                    for (int c = 0; c < 256; c += 32) {
-                        uint32_t d[32];
-                        tmem_ld_32x32b_x32(t_row + c, d);
-                        tmem_wait_ld();
-                        if (valid) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                dst[i] = make_uint4(d[4 * i + 0], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
-                        }
-                    }
-                }
+                tiled_epilogue<kGated>(t_row, args, row, r < t.rows && row >= 0 && row < args.cap, t.n0);
             } else {
                 // lane = weight row = output column t.n0 + 32q + lane; TMEM column = token row of the tile
                 const int col = t.n0 + q * 32 + lane;
@@ -435,6 +447,215 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+    if (threadIdx.x == 0 && s_abort)
+        atomicOr(args.err, MOE_DEVERR_WAIT_TIMEOUT);
+}
+
+
+// ------------------------------------------------------------------ CTA-pair tiled kernel
+//
+// Same work decomposition as the tiled path, on a 2-CTA cluster sharing one
+// tcgen05.mma.cta_group::2 of M=256, N=256: a unit is 256 activation rows of
+// one expert x 256 weight rows; each CTA of the pair loads its own 128
+// activation rows and half of the weight tile (gate-up: CTA 0 the 128 gate
+// rows, CTA 1 the 128 matching up rows; down: 128 output columns each), so a
+// stage is 32 KB per CTA instead of 48 KB and the ring is 6 deep. CTA 0 issues
+// the MMAs; each CTA's TMEM receives its 128 rows x 256 columns, so the
+// epilogue is the single-CTA one. Every TMA load of both CTAs completes on
+// CTA 0's full barrier (2 arrivals + both CTAs' bytes); CTA 0's commits are
+// multicast to both CTAs' empty / TMEM-full barriers; both epilogues release
+// the accumulator on CTA 0's TMEM-empty barrier.
+template <bool kGated, int kStages>
+struct PairCfg {
+    static constexpr int kHalfBytes = 128 * 128;                 // 128 rows x 64 bf16
+    static constexpr int kStageBytes = 2 * kHalfBytes;           // A half + B half
+    static constexpr int kPairRows = 256;
+    static constexpr int kOutCols = kGated ? 128 : 256;
+    static constexpr int kAccCols = 256;
+    static constexpr int kTmemCols = 512;
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(256, 256);
+    static constexpr int kDynSmem = 1024 + kStages * kStageBytes;
+};
+
+template <bool kGated, int kStages>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
+                             const GemmArgs args)
+{
+    using C = PairCfg<kGated, kStages>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[kStages];   // used in CTA 0
+    __shared__ __align__(8) uint64_t bar_empty[kStages];
+    __shared__ __align__(8) uint64_t bar_tfull[2];
+    __shared__ __align__(8) uint64_t bar_tempty[2];       // used in CTA 0
+    __shared__ __align__(8) uint64_t bar_drain;           // used in CTA 0
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_abort;
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ int s_tp[kMaxExperts + 1];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int E = args.E;
+    const uint32_t rank = cluster_ctarank();
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    volatile int *abort_flag = &s_abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&bar_full[s]), 2);
+            mbar_init(smem_u32(&bar_empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bar_tfull[b]), 1);
+            mbar_init(smem_u32(&bar_tempty[b]), 8);   // 4 epilogue warps x 2 CTAs
+        }
+        mbar_init(smem_u32(&bar_drain), 1);
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_act);
+        tma_prefetch_desc(&tm_w);
+    }
+    if (warp == 2) {
+        tmem_alloc_pair(smem_u32(&s_tmem_base), C::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    for (int i = threadIdx.x; i <= E; i += kThreads)
+        s_off[i] = args.expert_offsets[i];
+    __syncthreads();
+    if (warp == 3)
+        build_tile_prefix(s_off, s_tp, E, C::kPairRows, lane);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // both CTAs' barriers initialised before any remote arrive
+    tc_fence_after();
+
+    const uint32_t tmem_base = s_tmem_base;
+    const int NT = args.n_out / C::kOutCols;
+    const int cluster_id = blockIdx.x >> 1;
+    const int n_clusters = gridDim.x >> 1;
+    const int total_units = s_tp[E] * NT;
+    const int k_blocks = args.K / kBK;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_normal();
+            const uint64_t pol_a = l2_policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = cluster_id; ok && u < total_units; u += n_clusters) {
+                const Unit t = decode_unit<false, C::kPairRows, C::kOutCols>(u, s_off, s_tp, E, NT);
+                const int a_row = t.row0 + 128 * static_cast<int>(rank);
+                const int w_row = kGated ? t.e * args.w_rows_per_expert + (rank ? args.up_row_offset : 0) + t.n0
+                                         : t.e * args.w_rows_per_expert + t.n0 + 128 * static_cast<int>(rank);
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, abort_flag, args.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full0 = map_to_cta(smem_u32(&bar_full[stage]), 0);
+                    const uint32_t a_dst = smem_u32(smem + stage * C::kStageBytes);
+                    const uint32_t b_dst = a_dst + C::kHalfBytes;
+                    const int kc = kb * kBK;
+                    mbar_arrive_expect_tx_cluster(full0, C::kStageBytes);
+                    tma_load_2d_pair(a_dst, &tm_act, full0, kc, a_row, pol_a);
+                    tma_load_2d_pair(b_dst, &tm_w, full0, kc, w_row, pol_w);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (CTA 0 only)
+        if (lane == 0 && rank == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int local = 0;
+            for (int u = cluster_id; ok && u < total_units; u += n_clusters, ++local) {
+                const int buf = local & 1;
+                const uint32_t use = (local >> 1) & 1;
+                if (!mbar_wait_bounded(smem_u32(&bar_tempty[buf]), use ^ 1u, abort_flag, args.wait_limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * C::kAccCols;
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(smem_u32(&bar_full[stage]), phase, abort_flag, args.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
+                    const uint32_t b_addr = a_addr + C::kHalfBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                        umma_bf16_pair(d_tmem, smem_desc_kmajor_sw128(a_addr + kk * 32),
+                                       smem_desc_kmajor_sw128(b_addr + kk * 32), C::kIdesc, acc);
+                    }
+                    umma_commit_pair(smem_u32(&bar_empty[stage]), 0x3);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok)
+                    umma_commit_pair(smem_u32(&bar_tfull[buf]), 0x3);
+            }
+            umma_commit_pair(smem_u32(&bar_drain), 0x1);
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(smem_u32(&bar_drain), 0) && global_timer_ns() - t0 < args.wait_limit_ns) {
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp - 4;
+        int local = 0;
+        for (int u = cluster_id; u < total_units; u += n_clusters, ++local) {
+            const Unit t = decode_unit<false, C::kPairRows, C::kOutCols>(u, s_off, s_tp, E, NT);
+            const int buf = local & 1;
+            const uint32_t use = (local >> 1) & 1;
+            int ok = 0;
+            if (lane == 0)
+                ok = mbar_wait_bounded(smem_u32(&bar_tfull[buf]), use, abort_flag, args.wait_limit_ns) ? 1 : 0;
+            ok = __shfl_sync(kFull, ok, 0);
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + buf * C::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
+            const int r = 128 * static_cast<int>(rank) + q * 32 + lane;   // row within the 256-row pair tile
+            const int row = t.row0 + r;
+            tiled_epilogue<kGated>(t_row, args, row, r < t.rows && row >= 0 && row < args.cap, t.n0);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(map_to_cta(smem_u32(&bar_tempty[buf]), 0));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort) {
+        // give-up path: let loads and remote arrivals still in flight land first
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 2000000ull) {
+        }
+    }
+    cluster_sync();   // neither CTA leaves while its peer may still touch its shared memory
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, C::kTmemCols);
     }
     if (threadIdx.x == 0 && s_abort)
         atomicOr(args.err, MOE_DEVERR_WAIT_TIMEOUT);
@@ -514,6 +735,64 @@ cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
     return launch_k(kern, dim3(grid), dim3(kThreads), C::kDynSmem, stream, p.pdl, tm_act, tm_w, a);
 }
 
+
+template <bool kGated, int kStages>
+cudaError_t run_pair(const GemmProblem &p, int num_sms, cudaStream_t stream)
+{
+    using C = PairCfg<kGated, kStages>;
+    auto kern = grouped_gemm_pair_kernel<kGated, kStages>;
+    static int attr_done_for_device = -1;
+    static int max_clusters = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kDynSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (attr_done_for_device != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
+        if (e != cudaSuccess)
+            return e;
+        cfg.gridDim = dim3(2 * (num_sms / 2));
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess)
+            return e;
+        max_clusters = n > 0 ? n : 1;
+        attr_done_for_device = dev;
+    }
+    CUtensorMap tm_act, tm_w;
+    if (!make_map(&tm_act, p.act, static_cast<uint64_t>(p.cap), static_cast<uint64_t>(p.K), 128) ||
+        !make_map(&tm_w, p.w, static_cast<uint64_t>(p.E) * p.w_rows_per_expert, static_cast<uint64_t>(p.K), 128))
+        return cudaErrorInvalidValue;
+    GemmArgs a;
+    a.expert_offsets = p.expert_offsets;
+    a.out = p.out;
+    a.err = p.err;
+    a.wait_limit_ns = kWaitLimitNs;
+    a.E = p.E;
+    a.cap = p.cap;
+    a.K = p.K;
+    a.n_out = p.n_out;
+    a.w_rows_per_expert = p.w_rows_per_expert;
+    a.up_row_offset = p.up_row_offset;
+    const long long max_units = ((static_cast<long long>(p.cap) + 255) / 256 + p.E) * (p.n_out / C::kOutCols);
+    long long clusters = max_units < max_clusters ? max_units : max_clusters;
+    if (clusters < 1)
+        clusters = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, a);
+}
+
 }  // namespace
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream)
@@ -523,6 +802,8 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t 
     if (!p.small_m) {
         if (p.tile_rows != 128)
             return cudaErrorInvalidValue;
+        if (p.cta_pair)
+            return p.gated ? run_pair<true, 6>(p, num_sms, stream) : run_pair<false, 6>(p, num_sms, stream);
         return p.gated ? run<false, true, 128, 4>(p, num_sms, stream) : run<false, false, 128, 4>(p, num_sms, stream);
     }
     switch (p.tile_rows) {

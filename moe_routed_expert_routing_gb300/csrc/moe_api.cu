@@ -55,7 +55,7 @@ moe_status_t check_problem(const moe_problem_t *p)
     if (p->T_max < 1 || p->E < 1 || p->E > kMaxExperts || p->k < 1 || p->k > p->E || p->k > kMaxTopK ||
         p->H < 1 || p->I < 1 || p->reserved != 0)
         return MOE_ERR_SHAPE;
-    if (p->path < MOE_PATH_AUTO || p->path > MOE_PATH_SMALL_M)
+    if (p->path < MOE_PATH_AUTO || p->path > MOE_PATH_TILED_1CTA)
         return MOE_ERR_SHAPE;
     const long long R = static_cast<long long>(p->T_max) * p->k;
     if (R > (1LL << 28))
@@ -80,7 +80,7 @@ void resolve(const moe_problem_t &p, int *path, int *tile_rows)
     if (chosen == MOE_PATH_AUTO)
         chosen = avg_rows > 16.0 ? MOE_PATH_TILED : MOE_PATH_SMALL_M;
     *path = chosen;
-    if (chosen == MOE_PATH_TILED)
+    if (chosen == MOE_PATH_TILED || chosen == MOE_PATH_TILED_1CTA)
         *tile_rows = 128;
     else
         *tile_rows = avg_rows <= 2.0 ? 16 : (avg_rows <= 8.0 ? 32 : 64);
@@ -168,6 +168,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *x_sorted
     g.E = p.E;
     g.cap = capacity_of(p);
     g.small_m = path == MOE_PATH_SMALL_M;
+    g.cta_pair = path == MOE_PATH_TILED;
     g.tile_rows = tile_rows;
     g.split_k = 1;
     g.pdl = path == MOE_PATH_SMALL_M;

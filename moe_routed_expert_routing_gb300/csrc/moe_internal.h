@@ -82,6 +82,7 @@ struct GemmProblem {
     int tile_rows;            // activation rows per tile: 128 (tiled) or 16/32/64 (M-small)
     int split_k;              // 1, or 2 (M-small down GEMM only: two K halves added into a zeroed fp32 out)
     bool pdl;                 // programmatic dependent launch
+    bool cta_pair;            // tiled path on 2-CTA clusters (tcgen05 cta_group::2)
 };
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);

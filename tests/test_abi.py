@@ -61,11 +61,12 @@ def test_workspace_size_and_path(lib):
     assert lib.moe_resolve_path(P(8192, 128, 8, 4096, 1536)) == (lib.MOE_PATH_TILED, 128)
     assert lib.moe_resolve_path(P(8192, 128, 8, 4096, 1536, path=lib.MOE_PATH_SMALL_M)) == (lib.MOE_PATH_SMALL_M, 64)
     assert lib.moe_resolve_path(P(1, 384, 6, 7168, 3072, path=lib.MOE_PATH_TILED)) == (lib.MOE_PATH_TILED, 128)
+    assert lib.moe_resolve_path(P(64, 8, 2, 256, 512, path=lib.MOE_PATH_TILED_1CTA)) == (lib.MOE_PATH_TILED_1CTA, 128)
 
 
 @pytest.mark.parametrize("bad,status", [
     (dict(T_max=0), 2), (dict(E=0), 2), (dict(E=1025), 2), (dict(k=0), 2), (dict(k=9, E=8), 2),
-    (dict(H=300), 3), (dict(I=100), 3), (dict(capacity=5), 2), (dict(path=7), 2),
+    (dict(H=300), 3), (dict(I=100), 3), (dict(capacity=5), 2), (dict(path=7), 2), (dict(path=-1), 2),
 ])
 def test_problem_validation(lib, bad, status):
     args = dict(T_max=64, E=8, k=2, H=256, I=512, capacity=0, path=0)

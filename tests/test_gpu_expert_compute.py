@@ -59,6 +59,9 @@ CASES = [
     ("small_zipf", 128, 64, 8, 512, 256, 2, "zipf"),           # empty experts + heavy ones
     ("tiny_tiled", 64, 8, 2, 256, 512, 1, "uniform"),
     ("tiny_small", 64, 8, 2, 256, 512, 2, "uniform"),
+    ("tiled1_small", 96, 4, 2, 256, 256, 3, "uniform"),         # single-CTA tiles
+    ("tiled1_skew", 400, 8, 2, 256, 512, 3, "hot0"),
+    ("pair_multi", 700, 3, 2, 512, 384, 1, "uniform"),          # ~467 rows/expert: 2 pair tiles, ragged
 ]
 
 
@@ -76,7 +79,7 @@ def test_expert_compute_matches_oracle(B, case):
     assert_within_tolerance(ys[:n].cpu().numpy(), ref, name)
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_gate_up_stage_alone(B, path):
     """W2 = identity (H == I): y equals the activation h, so the gate-up GEMM and
     its SiLU(gate)*up epilogue are checked on their own, nearly bit for bit."""

@@ -44,7 +44,8 @@ def test_forward_matches_oracle(B, name):
     print(name, m)
 
 
-@pytest.mark.parametrize("name,path", [("tiny", 1), ("tiny", 2), ("small", 1), ("decode8", 1)])
+@pytest.mark.parametrize("name,path", [("tiny", 1), ("tiny", 2), ("tiny", 3), ("small", 1), ("small", 3),
+                                       ("decode8", 1), ("large", 3)])
 def test_forward_both_paths(B, name, path):
     wl = wlm.WORKLOADS[name]
     dw = DeviceWorkload(wl)
@@ -60,7 +61,7 @@ def test_repeated_forward_bit_exact(B, shape):
     """Repeated calls give identical bits (the second shape takes the split-K down GEMM)."""
     wl = wlm.custom("rep", *shape, seed=8)
     dw = DeviceWorkload(wl)
-    for path in (1, 2):
+    for path in (1, 2, 3):
         p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=path)
         bufs = forward(B, p, dw)
         first = bufs.out.clone()
@@ -75,7 +76,7 @@ def test_capacity_tail_poison_does_not_leak(B):
     dw = DeviceWorkload(wl)
     p0 = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
     clean = forward(B, p0, dw).out.clone()
-    for path in (1, 2):
+    for path in (1, 2, 3):
         p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, capacity=wl.R + 300, path=path)
         bufs = B.Buffers(p)
         bufs.ws.fill_(0xFF)                      # every bf16 in the sorted batches = NaN
