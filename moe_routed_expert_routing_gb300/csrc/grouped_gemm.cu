@@ -57,6 +57,8 @@ constexpr unsigned kFull = 0xffffffffu;
 
 struct GemmArgs {
     const int32_t *expert_offsets;
+    const int32_t *perm;    // gathered activations: sorted row -> routed slot (token = slot / k)
+    int k;
     void *out;          // gate-up: bf16 h[cap, n_out]; down: fp32 y[cap, n_out]
     int32_t *err;
     uint64_t wait_limit_ns;
@@ -222,12 +224,14 @@ __device__ __forceinline__ void tiled_epilogue(uint32_t t_row, const GemmArgs &a
     }
 }
 
-template <bool kSmallM, bool kGated, int kTileRows, int kStages, int kSplitK>
+template <bool kSmallM, bool kGated, int kTileRows, int kStages, int kSplitK, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
                         const GemmArgs args)
 {
     using C = Cfg<kSmallM, kGated, kTileRows, kStages, kSplitK>;
+    static_assert(!kGather || kGated, "row gather: gate-up GEMM only");
+    __shared__ __align__(16) int s_rows[kTileRows];   // gathered: token of each activation row of the unit
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
     __shared__ __align__(8) uint64_t bar_empty[kStages];
@@ -288,18 +292,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint64_t pol_w = kSmallM ? l2_policy_evict_first() : l2_policy_evict_normal();
-            const uint64_t pol_a = l2_policy_evict_last();
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load in flight, and its phase parity
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-                const Unit t = decode_unit<kSmallM, kTileRows, C::kOutCols>(u / kSplitK, s_off, s_tp, E, NT);
-                const int kb0 = (u % kSplitK) * k_blocks;
-                const int w_row0 = t.e * args.w_rows_per_expert + t.n0;
-                const int w_row1 = kGated ? t.e * args.w_rows_per_expert + args.up_row_offset + t.n0 : w_row0 + 128;
+        const uint64_t pol_w = kSmallM ? l2_policy_evict_first() : l2_policy_evict_normal();
+        const uint64_t pol_a = l2_policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load in flight, and its phase parity
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+            const Unit t = decode_unit<kSmallM, kTileRows, C::kOutCols>(u / kSplitK, s_off, s_tp, E, NT);
+            const int kb0 = (u % kSplitK) * k_blocks;
+            const int w_row0 = t.e * args.w_rows_per_expert + t.n0;
+            const int w_row1 = kGated ? t.e * args.w_rows_per_expert + args.up_row_offset + t.n0 : w_row0 + 128;
+            if (kGather) {
+                // token of every activation row of the tile; rows past the expert read token 0 and are never stored
+                for (int i = lane; i < kTileRows; i += 32)
+                    s_rows[i] = i < t.rows ? __ldg(args.perm + t.row0 + i) / args.k : 0;
+                __syncwarp();
+            }
+            if (lane == 0) {
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, abort_flag, args.wait_limit_ns)) {
                         ok = false;
@@ -313,7 +323,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(w_dst, &tm_w, full, kc, w_row0, pol_w);
                     if (C::kWRows == 256)
                         tma_load_2d(w_dst + 128 * 128, &tm_w, full, kc, w_row1, pol_w);
-                    tma_load_2d(a_dst, &tm_act, full, kc, t.row0, pol_a);
+                    if (kGather) {
+#pragma unroll
+                        for (int g = 0; g < kTileRows / 4; ++g)
+                            tma_gather4(a_dst + g * 512, &tm_act, full, kc, reinterpret_cast<const int4 *>(s_rows)[g],
+                                        pol_a);
+                    } else {
+                        tma_load_2d(a_dst, &tm_act, full, kc, t.row0, pol_a);
+                    }
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
@@ -322,16 +339,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!ok) {
-                // give-up path: let every load still in flight land before the CTA exits
-                for (int s = 0; s < kStages; ++s)
-                    if (issued_mask & (1u << s)) {
-                        const uint64_t t0 = global_timer_ns();
-                        while (!mbar_try_wait(smem_u32(&bar_full[s]), (issued_parity >> s) & 1u) &&
-                               global_timer_ns() - t0 < args.wait_limit_ns) {
-                        }
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;   // s_rows is rewritten only after lane 0 issued
+        }
+        if (!ok && lane == 0) {
+            // give-up path: let every load still in flight land before the CTA exits
+            for (int s = 0; s < kStages; ++s)
+                if (issued_mask & (1u << s)) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (!mbar_try_wait(smem_u32(&bar_full[s]), (issued_parity >> s) & 1u) &&
+                           global_timer_ns() - t0 < args.wait_limit_ns) {
                     }
-            }
+                }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -542,17 +560,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (both CTAs)
-        if (lane == 0) {
-            const uint64_t pol_w = l2_policy_evict_normal();
-            const uint64_t pol_a = l2_policy_evict_last();
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int u = cluster_id; ok && u < total_units; u += n_clusters) {
-                const Unit t = decode_unit<false, C::kPairRows, C::kOutCols>(u, s_off, s_tp, E, NT);
-                const int a_row = t.row0 + 128 * static_cast<int>(rank);
-                const int w_row = kGated ? t.e * args.w_rows_per_expert + (rank ? args.up_row_offset : 0) + t.n0
-                                         : t.e * args.w_rows_per_expert + t.n0 + 128 * static_cast<int>(rank);
+        const uint64_t pol_w = l2_policy_evict_normal();
+        const uint64_t pol_a = l2_policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int u = cluster_id; ok && u < total_units; u += n_clusters) {
+            const Unit t = decode_unit<false, C::kPairRows, C::kOutCols>(u, s_off, s_tp, E, NT);
+            const int a_row = t.row0 + 128 * static_cast<int>(rank);
+            const int w_row = kGated ? t.e * args.w_rows_per_expert + (rank ? args.up_row_offset : 0) + t.n0
+                                     : t.e * args.w_rows_per_expert + t.n0 + 128 * static_cast<int>(rank);
+            if (lane == 0) {
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, abort_flag, args.wait_limit_ns)) {
                         ok = false;
@@ -571,6 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -697,11 +716,11 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
     return r == CUDA_SUCCESS;
 }
 
-template <bool kSmallM, bool kGated, int kTileRows, int kStages, int kSplitK = 1>
+template <bool kSmallM, bool kGated, int kTileRows, int kStages, int kSplitK = 1, bool kGather = false>
 cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
 {
     using C = Cfg<kSmallM, kGated, kTileRows, kStages, kSplitK>;
-    auto kern = grouped_gemm_kernel<kSmallM, kGated, kTileRows, kStages, kSplitK>;
+    auto kern = grouped_gemm_kernel<kSmallM, kGated, kTileRows, kStages, kSplitK, kGather>;
     static int attr_done_for_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -714,11 +733,13 @@ cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
         attr_done_for_device = dev;
     }
     CUtensorMap tm_act, tm_w;
-    if (!make_map(&tm_act, p.act, static_cast<uint64_t>(p.cap), static_cast<uint64_t>(p.K), kTileRows) ||
+    if (!make_map(&tm_act, p.act, static_cast<uint64_t>(p.act_rows), static_cast<uint64_t>(p.K), kGather ? 1 : kTileRows) ||
         !make_map(&tm_w, p.w, static_cast<uint64_t>(p.E) * p.w_rows_per_expert, static_cast<uint64_t>(p.K), 128))
         return cudaErrorInvalidValue;
     GemmArgs a;
     a.expert_offsets = p.expert_offsets;
+    a.perm = p.perm;
+    a.k = p.k;
     a.out = p.out;
     a.err = p.err;
     a.wait_limit_ns = kWaitLimitNs;
@@ -771,11 +792,13 @@ cudaError_t run_pair(const GemmProblem &p, int num_sms, cudaStream_t stream)
         attr_done_for_device = dev;
     }
     CUtensorMap tm_act, tm_w;
-    if (!make_map(&tm_act, p.act, static_cast<uint64_t>(p.cap), static_cast<uint64_t>(p.K), 128) ||
+    if (!make_map(&tm_act, p.act, static_cast<uint64_t>(p.act_rows), static_cast<uint64_t>(p.K), 128) ||
         !make_map(&tm_w, p.w, static_cast<uint64_t>(p.E) * p.w_rows_per_expert, static_cast<uint64_t>(p.K), 128))
         return cudaErrorInvalidValue;
     GemmArgs a;
     a.expert_offsets = p.expert_offsets;
+    a.perm = p.perm;
+    a.k = p.k;
     a.out = p.out;
     a.err = p.err;
     a.wait_limit_ns = kWaitLimitNs;
@@ -799,8 +822,12 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t 
 {
     if (p.split_k != 1 && (p.split_k != 2 || !p.small_m || p.gated || p.tile_rows != 16 || (p.K / kBK) % 2 != 0))
         return cudaErrorInvalidValue;
+    if (p.gather && (!p.gated || !p.perm || p.k < 1))
+        return cudaErrorInvalidValue;
     if (!p.small_m) {
         if (p.tile_rows != 128)
+            return cudaErrorInvalidValue;
+        if (p.gather)   // tiled tiles would need 32 gather4 per stage: not built (see moe_forward)
             return cudaErrorInvalidValue;
         if (p.cta_pair)
             return p.gated ? run_pair<true, 6>(p, num_sms, stream) : run_pair<false, 6>(p, num_sms, stream);
@@ -810,11 +837,17 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t 
     case 16:
         if (!p.gated && p.split_k == 2)
             return run<true, false, 16, 10, 2>(p, num_sms, stream);
-        return p.gated ? run<true, true, 16, 6>(p, num_sms, stream) : run<true, false, 16, 10>(p, num_sms, stream);
+        if (p.gated)
+            return p.gather ? run<true, true, 16, 6, 1, true>(p, num_sms, stream) : run<true, true, 16, 6>(p, num_sms, stream);
+        return run<true, false, 16, 10>(p, num_sms, stream);
     case 32:
-        return p.gated ? run<true, true, 32, 5>(p, num_sms, stream) : run<true, false, 32, 9>(p, num_sms, stream);
+        if (p.gated)
+            return p.gather ? run<true, true, 32, 5, 1, true>(p, num_sms, stream) : run<true, true, 32, 5>(p, num_sms, stream);
+        return run<true, false, 32, 9>(p, num_sms, stream);
     case 64:
-        return p.gated ? run<true, true, 64, 5>(p, num_sms, stream) : run<true, false, 64, 8>(p, num_sms, stream);
+        if (p.gated)
+            return p.gather ? run<true, true, 64, 5, 1, true>(p, num_sms, stream) : run<true, true, 64, 5>(p, num_sms, stream);
+        return run<true, false, 64, 8>(p, num_sms, stream);
     default:
         return cudaErrorInvalidValue;
     }

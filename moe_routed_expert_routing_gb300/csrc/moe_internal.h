@@ -69,7 +69,11 @@ cudaError_t launch_combine(const float *y_sorted, const int32_t *inv, const floa
 
 // ---- expert GEMMs (grouped_gemm.cu) ----
 struct GemmProblem {
-    const void *act;          // [cap, K] bf16, rows grouped by expert
+    const void *act;          // [act_rows, K] bf16: sorted rows, or x itself when gather is set
+    int act_rows;             // rows of `act` (cap, or T_max for x)
+    bool gather;              // A rows fetched from x through perm (tile::gather4), gate-up only
+    const int32_t *perm;      // gather: sorted row -> routed slot
+    int k;                    // gather: token = slot / k
     const void *w;            // [E, w_rows_per_expert, K] bf16
     void *out;                // [cap, n_out]: bf16 h (gated) or fp32 y (down)
     const int32_t *expert_offsets;

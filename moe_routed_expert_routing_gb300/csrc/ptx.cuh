@@ -167,6 +167,18 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
                  : "memory");
 }
 
+// Four rows of a 2-D tensor (box of 64 columns x 1 row) gathered into four
+// consecutive 128-byte rows of shared memory, swizzled like a 4-row box.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t c0,
+                                            int4 rows, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+                 ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w),
+                 "r"(bar), "l"(policy)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
