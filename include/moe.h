@@ -66,13 +66,14 @@ typedef enum moe_status {
 #define MOE_DEVERR_BAD_EXPERT_ID 0x1 /* an id outside [0, E) and not -1: slot dropped */
 #define MOE_DEVERR_WAIT_TIMEOUT 0x2  /* a pipeline wait gave up: results of that call are invalid */
 
-/* Expert-GEMM path. AUTO picks from the static shape: M-small when
- * T_max*k/E <= 16 rows per expert on average, large-tile otherwise. */
+/* Expert-GEMM path. AUTO picks from the static shape, a = T_max*k/E routed
+ * rows per expert on average: M-small for a <= 16, single-CTA tiles for
+ * 16 < a < 256, CTA-pair tiles for a >= 256. */
 typedef enum moe_path {
     MOE_PATH_AUTO = 0,
     MOE_PATH_TILED = 1,       /* 256-row activation tiles x 256-row weight tiles on CTA pairs (cta_group::2) */
     MOE_PATH_SMALL_M = 2,     /* weights on the MMA M side, token tiles of 16..64 rows */
-    MOE_PATH_TILED_1CTA = 3   /* 128 x 256 tiles on single CTAs; never chosen by AUTO (for comparison) */
+    MOE_PATH_TILED_1CTA = 3   /* 128 x 256 tiles on single CTAs */
 } moe_path_t;
 
 typedef struct moe_problem {

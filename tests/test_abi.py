@@ -57,7 +57,7 @@ def test_workspace_size_and_path(lib):
     assert lib.moe_resolve_path(P(1, 384, 6, 7168, 3072)) == (lib.MOE_PATH_SMALL_M, 16)
     assert lib.moe_resolve_path(P(8, 384, 6, 7168, 3072)) == (lib.MOE_PATH_SMALL_M, 16)
     assert lib.moe_resolve_path(P(128, 256, 8, 7168, 2048)) == (lib.MOE_PATH_SMALL_M, 32)
-    assert lib.moe_resolve_path(P(2048, 384, 6, 7168, 3072)) == (lib.MOE_PATH_TILED, 128)
+    assert lib.moe_resolve_path(P(2048, 384, 6, 7168, 3072)) == (lib.MOE_PATH_TILED_1CTA, 128)
     assert lib.moe_resolve_path(P(8192, 128, 8, 4096, 1536)) == (lib.MOE_PATH_TILED, 128)
     assert lib.moe_resolve_path(P(8192, 128, 8, 4096, 1536, path=lib.MOE_PATH_SMALL_M)) == (lib.MOE_PATH_SMALL_M, 64)
     assert lib.moe_resolve_path(P(1, 384, 6, 7168, 3072, path=lib.MOE_PATH_TILED)) == (lib.MOE_PATH_TILED, 128)
