@@ -54,10 +54,16 @@ STAGES = ["dispatch", "gather", "gemm_gate_up", "gemm_down", "combine"]
 LAUNCHES_PER_FORWARD = 7   # count, scan, scatter, gather, gate-up GEMM, down GEMM, combine
 GRAPH_STEPS = 10
 
-# DRAM bytes per launch of the dominant kernel (gate-up GEMM) from an ncu capture:
-# (sha256 of grouped_gemm.cu when captured, {workload: bytes per launch}).
-# A mismatching hash reports traffic as null (kernel changed since the capture).
-NCU_TRAFFIC = {"kernel_sha256": None, "bytes_per_launch": {}}
+# DRAM traffic of the dominant kernel (gate-up GEMM) from an ncu capture
+# (profiles/gemm_small_m_decode8_E24.md: dram__bytes_read.sum +
+# dram__bytes_write.sum = 1.7648 GB for one launch with 20 touched experts).
+# The M-small gate-up GEMM reads each touched expert's weights exactly once, so
+# the capture is scaled to a launch by its touched experts. Keyed to the sha256
+# of the GEMM sources at capture time: after any change, traffic reports null.
+NCU_TRAFFIC = {
+    "kernel_sha256": "8f9a138d87d9c6a20dc615df94624dcde032d2c4f843ccf12fc4ff251b759b30",
+    "small_m_gate_up_bytes_per_touched_expert": 1.7648e9 / 20,
+}
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -90,9 +96,11 @@ def load_peaks() -> dict:
 
 
 def kernel_sha() -> str:
-    p = os.path.join(ROOT, "moe_routed_expert_routing_gb300", "csrc", "grouped_gemm.cu")
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    h = hashlib.sha256()
+    for name in ("grouped_gemm.cu", "ptx.cuh", "moe_internal.h"):
+        with open(os.path.join(ROOT, "moe_routed_expert_routing_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -390,11 +398,14 @@ def run_ours(args, world, rank, local):
     roof["kernel"] = "grouped_gemm_kernel (gate-up, SiLU*up epilogue)"
     roof["algorithmic_per_step"] = g1_flops if roof["bound"] == "tensor" else g1_bytes
     traffic = None
-    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha():
-        per = [NCU_TRAFFIC["bytes_per_launch"].get(d["wl"].name) for d in inputs]
-        if all(v is not None for v in per):
-            traffic = float(sum(per)) / len(per)
+    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and all(d["path"][0] == 2 for d in inputs):
+        per = [d["acct"]["touched_experts"] * NCU_TRAFFIC["small_m_gate_up_bytes_per_touched_expert"]
+               for d in inputs]
+        traffic = float(sum(per)) / len(per)
     roof["traffic"] = traffic
+    roof["traffic_note"] = ("ncu dram read+write bytes per launch, scaled from a 20-expert capture by touched experts"
+                            if traffic is not None else "no capture for this kernel version/workload")
+    roof["algorithmic_per_launch"] = roof["algorithmic_per_step"] / len(inputs)
     # whole-call roofline: slower of FLOPs at tensor peak and touched bytes at HBM bandwidth
     t_roof = sum(max(d["acct"]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12),
                      d["acct"]["bytes"] / (peaks["hbm_gbs"] * 1e9)) for d in inputs)

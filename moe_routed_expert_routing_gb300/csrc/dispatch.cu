@@ -261,11 +261,11 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_scatter_kernel(
     scatter_slots(ids, s0, s1, E, cursor, wcnt, perm, inv);
 }
 
-// x_sorted[row] = x[perm[row] / k] for row < expert_offsets[E]. Work item =
-// (row, 2048-column slice): a thread moves 16 bytes of each of the item's
-// columns groups, four loads in flight before the stores.
+// x_sorted[row] = x[perm[row] / k] for row < expert_offsets[E]. One warp per
+// row (grid-stride over rows); each lane moves 16-byte vectors lane, lane+32,
+// ..., with eight loads in flight before their stores.
 constexpr int kGatherThreads = 256;
-constexpr int kGatherVecPerItem = kGatherThreads * 4;   // 16-byte vectors per work item
+constexpr int kGatherUnroll = 8;
 
 __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const uint4 *__restrict__ x,
                                                                      const int32_t *__restrict__ perm,
@@ -276,26 +276,26 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const uint4
     pdl_wait();
     pdl_trigger();
     const int n_rows = min(expert_offsets[E], cap);
-    const int slices = (vec_per_row + kGatherVecPerItem - 1) / kGatherVecPerItem;
-    const long long items = static_cast<long long>(n_rows) * slices;
-    for (long long item = blockIdx.x; item < items; item += gridDim.x) {
-        const int r = static_cast<int>(item / slices);
-        const int c0 = static_cast<int>(item % slices) * kGatherVecPerItem + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int warps = kGatherThreads / 32;
+    for (int r = blockIdx.x * warps + (threadIdx.x >> 5); r < n_rows; r += gridDim.x * warps) {
         const int t = perm[r] / k;
         const uint4 *src = x + static_cast<size_t>(t) * vec_per_row;
         uint4 *dst = x_sorted + static_cast<size_t>(r) * vec_per_row;
-        uint4 v[4];
+        for (int c0 = lane; c0 < vec_per_row; c0 += 32 * kGatherUnroll) {
+            uint4 v[kGatherUnroll];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int c = c0 + q * kGatherThreads;
-            if (c < vec_per_row)
-                v[q] = __ldg(src + c);
-        }
+            for (int q = 0; q < kGatherUnroll; ++q) {
+                const int c = c0 + 32 * q;
+                if (c < vec_per_row)
+                    v[q] = __ldg(src + c);
+            }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int c = c0 + q * kGatherThreads;
-            if (c < vec_per_row)
-                dst[c] = v[q];
+            for (int q = 0; q < kGatherUnroll; ++q) {
+                const int c = c0 + 32 * q;
+                if (c < vec_per_row)
+                    dst[c] = v[q];
+            }
         }
     }
 }
@@ -328,9 +328,9 @@ cudaError_t launch_dispatch(const int32_t *topk_ids, const int32_t *d_num_tokens
 cudaError_t launch_gather_rows(const void *x, const int32_t *perm, const int32_t *expert_offsets, int E, int k, int H,
                                int cap, void *x_sorted, int num_sms, cudaStream_t stream, bool pdl)
 {
-    const long long slices = (H / 8 + kGatherVecPerItem - 1) / kGatherVecPerItem;
-    const long long items = static_cast<long long>(cap) * slices;
-    int blocks = static_cast<int>(items < num_sms * 8LL ? items : num_sms * 8LL);
+    const int warps = kGatherThreads / 32;
+    int blocks = (cap + warps - 1) / warps;
+    blocks = blocks < num_sms * 8 ? blocks : num_sms * 8;
     if (blocks < 1)
         blocks = 1;
     return launch_k(gather_rows_kernel, dim3(blocks), dim3(kGatherThreads), 0, stream, pdl,
