@@ -499,6 +499,76 @@ def run_e2e(B, inputs, stream, device, args, world):
             "ms_per_step": ms / steps, "api": "moe_forward (eager, C ABI) with pinned host copies each step"}
 
 
+# ----------------------------------------------------------------------------- token sweep
+
+SWEEP_TOKENS = [1, 8, 32, 128, 512, 2048, 8192]
+
+
+def run_sweep(args, world, rank, local):
+    """us/call vs roofline across token counts at one layer shape (E=384, k=6,
+    H=7168, I=3072 by default): every batch shares the same weights, each gets
+    its own routing; the launch profile follows from T alone."""
+    from moe_routed_expert_routing_gb300.build import build
+    build()
+    from moe_routed_expert_routing_gb300 import binding as B
+    import dataclasses
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    base = dataclasses.replace(wlm.WORKLOADS["prefill"], name="sweep")
+    if args.experts > 0:
+        base = dataclasses.replace(base, E=args.experts)
+    W13, W2 = wlm.make_weights(base, device)
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(device)
+    rows = []
+    for T in SWEEP_TOKENS:
+        wl = dataclasses.replace(base, T=T, name=f"T{T}", seed=1000 + T)
+        ids_np, w_np = wlm.make_routing(wl)
+        x = wlm.make_x(wl, device)
+        ids = torch.from_numpy(ids_np).to(device)
+        w = torch.from_numpy(w_np).to(device)
+        p = B.Problem.make(T, wl.E, wl.k, wl.H, wl.I, path=args.path)
+        bufs = B.Buffers(p, device)
+        acct = call_accounting(wl, ids_np)
+
+        def fwd():
+            B.moe_forward(p, x, ids, w, W13, W2, bufs.expert_offsets, bufs.perm, bufs.out, bufs.ws, stream=stream)
+
+        with torch.cuda.stream(stream):
+            fwd()
+        stream.synchronize()
+        if B.moe_last_device_error(bufs.ws, stream):
+            raise RuntimeError(f"device error at T={T}")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(GRAPH_STEPS):
+                    fwd()
+        reps = max(1, args.steps // GRAPH_STEPS)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(device)
+        us = e0.elapsed_time(e1) * 1e3 / (reps * GRAPH_STEPS)
+        t_roof = max(acct["flops"] / (peaks["bf16_tflops_sustained"] * 1e12), acct["bytes"] / (peaks["hbm_gbs"] * 1e9))
+        rows.append({"T": T, "us_per_call": us, "tflops": acct["flops"] / (us * 1e-6) / 1e12,
+                     "touched_experts": acct["touched_experts"], "roof_us": t_roof * 1e6,
+                     "roof_bound": "tensor" if acct["flops"] / (peaks["bf16_tflops_sustained"] * 1e12) >
+                     acct["bytes"] / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                     "frac": t_roof * 1e6 / us, "profile": B.moe_resolve_profile(p)})
+        del bufs, g
+        torch.cuda.empty_cache()
+    return {"sweep": "token count", "shape": f"E={base.E} k={base.k} H={base.H} I={base.I}, bf16, uniform routing",
+            "steps_per_point": max(1, args.steps // GRAPH_STEPS) * GRAPH_STEPS, "rows": rows,
+            "peaks": peaks}
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args, world, rank, local):
@@ -552,6 +622,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--experts", type=int, default=0, help="override E (small profiler cases)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (small profiler cases)")
+    ap.add_argument("--sweep", action="store_true", help="token-count sweep at the 384-expert shape (not the bench line)")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3],
                     help="expert-GEMM path: 0 auto, 1 tiled CTA pairs, 2 M-small, 3 tiled single CTA")
     return ap.parse_args(argv)
@@ -569,6 +640,10 @@ def main(argv=None):
             args.cpu_tokens = 1
         line = run_reference(args, world, rank, local)
         print(json.dumps(line), flush=True)
+        return 0
+    if args.sweep:
+        if rank == 0:
+            print(json.dumps(run_sweep(args, world, rank, local)), flush=True)
         return 0
     if args.cpu_tokens == 0:
         wl_T = max(wlm.WORKLOADS[n].T for n in WORKLOAD_SETS[args.workload])

@@ -98,6 +98,22 @@ moe_status_t moe_workspace_size(const moe_problem_t *problem, size_t *bytes);
  * per CTA. Pure host. */
 moe_status_t moe_resolve_path(const moe_problem_t *problem, int32_t *path, int32_t *tile_rows);
 
+/* The full static launch profile of `problem` on the current device: every
+ * choice the library makes from shapes alone (FlashInfer moe_ep page: tile,
+ * schedule and token-back knobs keyed on the compile-time maximum token
+ * count). Queries the current device's SM count; enqueues nothing. */
+typedef struct moe_profile {
+    int32_t path;          /* moe_path_t that runs (never AUTO) */
+    int32_t tile_rows;     /* activation rows of one CTA's tile */
+    int32_t down_split_k;  /* 1, or 2: the down GEMM's K halves added into a zeroed fp32 y */
+    int32_t pdl;           /* 1: kernels of a call use programmatic dependent launch */
+    int32_t fused_gather;  /* 1: moe_forward's gate-up GEMM gathers rows from x (no x_sorted) */
+    int32_t cta_pair;      /* 1: tiled GEMMs run on 2-CTA clusters */
+    int32_t reserved[2];
+} moe_profile_t;
+
+moe_status_t moe_resolve_profile(const moe_problem_t *problem, moe_profile_t *profile);
+
 /*
  * Local dispatch: routing -> tight expert-major batch (TileOps page,
  * Summary: local dispatch; Scope: tight/no-pad batch, valid rows read from

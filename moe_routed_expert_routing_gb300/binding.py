@@ -27,6 +27,7 @@ MOE_DEVERR_WAIT_TIMEOUT = 0x2
 EXPORTED_SYMBOLS = (
     "moe_workspace_size",
     "moe_resolve_path",
+    "moe_resolve_profile",
     "moe_dispatch",
     "moe_expert_compute",
     "moe_combine",
@@ -72,6 +73,17 @@ class Problem(ctypes.Structure):
                 f"capacity={self.capacity}, path={self.path})")
 
 
+class Profile(ctypes.Structure):
+    """``moe_profile_t``: the static launch profile of a problem."""
+
+    _fields_ = [("path", ctypes.c_int32), ("tile_rows", ctypes.c_int32), ("down_split_k", ctypes.c_int32),
+                ("pdl", ctypes.c_int32), ("fused_gather", ctypes.c_int32), ("cta_pair", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
+
+
 _lib = None
 _vp = ctypes.c_void_p
 _P = ctypes.POINTER(Problem)
@@ -92,6 +104,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.moe_workspace_size.restype = st
     lib.moe_resolve_path.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     lib.moe_resolve_path.restype = st
+    lib.moe_resolve_profile.argtypes = [_P, ctypes.POINTER(Profile)]
+    lib.moe_resolve_profile.restype = st
     lib.moe_dispatch.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.moe_dispatch.restype = st
     lib.moe_expert_compute.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
@@ -158,6 +172,12 @@ def moe_resolve_path(problem: Problem):
     _check(load_library().moe_resolve_path(ctypes.byref(problem), ctypes.byref(path), ctypes.byref(rows)),
            "moe_resolve_path")
     return path.value, rows.value
+
+
+def moe_resolve_profile(problem: Problem) -> dict:
+    prof = Profile()
+    _check(load_library().moe_resolve_profile(ctypes.byref(problem), ctypes.byref(prof)), "moe_resolve_profile")
+    return prof.as_dict()
 
 
 def moe_dispatch(problem, topk_ids, expert_offsets, perm, inv, ws, x=None, x_sorted=None, d_num_tokens=None,

@@ -273,6 +273,28 @@ moe_status_t moe_resolve_path(const moe_problem_t *problem, int32_t *path, int32
     return MOE_OK;
 }
 
+moe_status_t moe_resolve_profile(const moe_problem_t *problem, moe_profile_t *profile)
+{
+    if (!profile)
+        return MOE_ERR_NULL;
+    const moe_status_t st = check_problem(problem);
+    if (st != MOE_OK)
+        return st;
+    const int sms = device_sm_count();
+    if (sms <= 0)
+        return MOE_ERR_CUDA;
+    int path = 0, tile_rows = 0;
+    resolve(*problem, &path, &tile_rows);
+    std::memset(profile, 0, sizeof *profile);
+    profile->path = path;
+    profile->tile_rows = tile_rows;
+    profile->down_split_k = down_split_k(*problem, path, tile_rows, sms) ? 2 : 1;
+    profile->pdl = use_pdl(*problem) ? 1 : 0;
+    profile->fused_gather = path == MOE_PATH_SMALL_M ? 1 : 0;
+    profile->cta_pair = path == MOE_PATH_TILED ? 1 : 0;
+    return MOE_OK;
+}
+
 moe_status_t moe_dispatch(const moe_problem_t *problem, const int32_t *topk_ids, const int32_t *d_num_tokens,
                           int32_t *expert_offsets, int32_t *perm, int32_t *inv, const void *x, void *x_sorted,
                           void *ws, size_t ws_bytes, void *stream)

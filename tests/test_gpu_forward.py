@@ -143,3 +143,18 @@ def test_prefill_dynamic_capacity_sampled(B):
         ref_acc, _ = dw.oracle_out(tokens, ids_np=ids_np, w_np=dw.w_np[:T_dev])
         m = error_metrics(wlm.bf16_bits(bufs.out)[tokens], ref_acc)
         assert m["max_err_beyond_output_rounding"] <= m["bound"] and m["mean_rel_err"] <= 5e-3, m
+
+
+def test_launch_profile_table(B):
+    """The static profile follows from the shape alone (a = T_max*k/E rows per expert)."""
+    P = B.Problem.make
+    dec1 = B.moe_resolve_profile(P(1, 384, 6, 7168, 3072))
+    assert dec1 == dict(path=2, tile_rows=16, down_split_k=2, pdl=1, fused_gather=1, cta_pair=0)
+    dec8 = B.moe_resolve_profile(P(8, 384, 6, 7168, 3072))
+    assert dec8 == dict(path=2, tile_rows=16, down_split_k=1, pdl=1, fused_gather=1, cta_pair=0)
+    small = B.moe_resolve_profile(P(128, 256, 8, 7168, 2048))
+    assert small["path"] == 2 and small["tile_rows"] == 32 and small["down_split_k"] == 1
+    prefill = B.moe_resolve_profile(P(2048, 384, 6, 7168, 3072))
+    assert prefill == dict(path=3, tile_rows=128, down_split_k=1, pdl=0, fused_gather=0, cta_pair=0)
+    large = B.moe_resolve_profile(P(8192, 128, 8, 4096, 1536))
+    assert large == dict(path=1, tile_rows=128, down_split_k=1, pdl=0, fused_gather=0, cta_pair=1)
