@@ -275,9 +275,14 @@ def run_ours(args, world, rank, local):
     init_dist(world, local)
     names = WORKLOAD_SETS[args.workload]
     inputs = make_inputs(names, device, args.experts, args.tokens)
+    layout = B.MOE_WEIGHTS_PACKED if args.packed else B.MOE_WEIGHTS_ROW_MAJOR
     for d in inputs:
         wl = d["wl"]
-        d["problem"] = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path)
+        d["problem"] = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path, weight_layout=layout)
+        if args.packed:   # model-load transform; the row-major copy is released
+            d["W13"], d["W2"] = B.moe_pack_weights(d["problem"], d["W13"], d["W2"])
+            torch.cuda.synchronize(device)
+            torch.cuda.empty_cache()
         d["bufs"] = B.Buffers(d["problem"], device)
         d["path"] = B.moe_resolve_path(d["problem"])
     stream = torch.cuda.Stream(device)
@@ -434,6 +439,7 @@ def run_ours(args, world, rank, local):
             "timing": (f"CUDA graph of {G} step(s) replayed {n_replays}x between CUDA events; kernel and stage "
                        f"times from a second graph of the same steps with stage events, replayed {prof_replays}x"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "weights": "packed (access-ordered)" if args.packed else "row-major",
         },
         "us_per_call": {d["wl"].name: float(sum(s)) for d, s in zip(inputs, stage_us)},
         "profiled_ms_per_step": prof_ms_per_step,
@@ -449,7 +455,10 @@ def run_ours(args, world, rank, local):
         "gpu_launches": LAUNCHES_PER_FORWARD * len(inputs) * K,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and args.packed:
+        result["cpu_baseline"] = None
+        result["cpu_baseline_note"] = "not run with --packed (the oracle reads row-major weights)"
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = time_oracle(inputs, args.cpu_seconds,
                                              tokens_cap=args.cpu_tokens if args.cpu_tokens > 0 else None)
         result["cpu_baseline"]["value_note"] = "oracle FLOP rate on the sample; a baseline, not the target"
@@ -622,6 +631,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--experts", type=int, default=0, help="override E (small profiler cases)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (small profiler cases)")
+    ap.add_argument("--packed", action="store_true", help="weights in the access-ordered PACKED layout")
     ap.add_argument("--sweep", action="store_true", help="token-count sweep at the 384-expert shape (not the bench line)")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3],
                     help="expert-GEMM path: 0 auto, 1 tiled CTA pairs, 2 M-small, 3 tiled single CTA")

@@ -84,8 +84,23 @@ typedef struct moe_problem {
     int32_t I;        /* intermediate size, multiple of 128 */
     int32_t capacity; /* rows of the sorted batch; 0 means T_max*k; else >= T_max*k */
     int32_t path;     /* moe_path_t */
-    int32_t reserved; /* must be 0 */
+    int32_t weight_layout; /* moe_weight_layout_t of W13 and W2 */
 } moe_problem_t;
+
+/* Layout of W13 / W2 in memory.
+ *  ROW_MAJOR: W13[E, 2I, H], W2[E, H, I] bf16, row-major.
+ *  PACKED: the output of moe_pack_weights. Same bytes, reordered in the order
+ *  the GEMMs read them (DeepGEMM page "MegaMoE: add cluster-paired FP4 weight
+ *  packets", Summary and Motivation: a weight layout that follows the kernel's
+ *  access order, loaded through TMA descriptors): expert -> 128-row weight
+ *  tile -> 64-wide K block, each block stored as the 128-byte-swizzled
+ *  shared-memory image of its 128 rows x 64 columns (16 KB), the gate and up
+ *  tiles of one W13 block side by side (32 KB). Every path reads it; results
+ *  are bitwise identical to ROW_MAJOR. */
+typedef enum moe_weight_layout {
+    MOE_WEIGHTS_ROW_MAJOR = 0,
+    MOE_WEIGHTS_PACKED = 1
+} moe_weight_layout_t;
 
 /* Bytes of workspace every entry point below needs for `problem` (pure host
  * arithmetic, no CUDA call). The same workspace serves all entry points; it
@@ -219,6 +234,14 @@ moe_status_t moe_dispatch_noalloc(const moe_problem_t *problem, const int32_t *t
                                   const int32_t *d_num_tokens, int32_t *expert_offsets,
                                   int32_t *perm, int32_t *inv, const void *x, void *x_sorted,
                                   void *stream);
+
+/*
+ * Reorder W13 and W2 (row-major) into the PACKED layout, once, at model load.
+ * W13_packed and W2_packed have the sizes of W13 and W2 and must not overlap
+ * them. Only problem->E, H and I matter. Enqueued on `stream`.
+ */
+moe_status_t moe_pack_weights(const moe_problem_t *problem, const void *W13, const void *W2, void *W13_packed,
+                              void *W2_packed, void *stream);
 
 /* Read the sticky device error word of `ws` into *host_code (0 = none).
  * Synchronises `stream` (the only entry point that does). */

@@ -20,6 +20,8 @@ MOE_PATH_AUTO = 0
 MOE_PATH_TILED = 1
 MOE_PATH_SMALL_M = 2
 MOE_PATH_TILED_1CTA = 3
+MOE_WEIGHTS_ROW_MAJOR = 0
+MOE_WEIGHTS_PACKED = 1
 MOE_DEVERR_BAD_EXPERT_ID = 0x1
 MOE_DEVERR_WAIT_TIMEOUT = 0x2
 
@@ -34,6 +36,7 @@ EXPORTED_SYMBOLS = (
     "moe_forward",
     "moe_forward_profiled",
     "moe_dispatch_noalloc",
+    "moe_pack_weights",
     "moe_last_device_error",
     "moe_clear_device_error",
     "moe_status_string",
@@ -57,12 +60,12 @@ class Problem(ctypes.Structure):
         ("I", ctypes.c_int32),
         ("capacity", ctypes.c_int32),
         ("path", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("weight_layout", ctypes.c_int32),
     ]
 
     @classmethod
-    def make(cls, T_max, E, k, H, I, capacity=0, path=MOE_PATH_AUTO):
-        return cls(int(T_max), int(E), int(k), int(H), int(I), int(capacity), int(path), 0)
+    def make(cls, T_max, E, k, H, I, capacity=0, path=MOE_PATH_AUTO, weight_layout=MOE_WEIGHTS_ROW_MAJOR):
+        return cls(int(T_max), int(E), int(k), int(H), int(I), int(capacity), int(path), int(weight_layout))
 
     @property
     def cap(self) -> int:
@@ -70,7 +73,7 @@ class Problem(ctypes.Structure):
 
     def __repr__(self):
         return (f"Problem(T_max={self.T_max}, E={self.E}, k={self.k}, H={self.H}, I={self.I}, "
-                f"capacity={self.capacity}, path={self.path})")
+                f"capacity={self.capacity}, path={self.path}, weight_layout={self.weight_layout})")
 
 
 class Profile(ctypes.Structure):
@@ -119,6 +122,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.moe_forward_profiled.restype = st
     lib.moe_dispatch_noalloc.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.moe_dispatch_noalloc.restype = st
+    lib.moe_pack_weights.argtypes = [_P, _vp, _vp, _vp, _vp, _vp]
+    lib.moe_pack_weights.restype = st
     lib.moe_last_device_error.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
     lib.moe_last_device_error.restype = st
     lib.moe_clear_device_error.argtypes = [_vp, _vp]
@@ -222,6 +227,17 @@ def moe_forward_profiled(problem, x, topk_ids, topk_weights, W13, W2, expert_off
                                                _ptr(d_num_tokens), _ptr(W13), _ptr(W2), _ptr(expert_offsets),
                                                _ptr(perm), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
                                                _stream(stream), arr), "moe_forward_profiled")
+
+
+def moe_pack_weights(problem, W13, W2, W13_packed=None, W2_packed=None, stream=None):
+    """Reorder W13/W2 into the PACKED layout; returns (W13_packed, W2_packed)."""
+    if W13_packed is None:
+        W13_packed = torch.empty_like(W13)
+    if W2_packed is None:
+        W2_packed = torch.empty_like(W2)
+    _check(load_library().moe_pack_weights(ctypes.byref(problem), _ptr(W13), _ptr(W2), _ptr(W13_packed),
+                                           _ptr(W2_packed), _stream(stream)), "moe_pack_weights")
+    return W13_packed, W2_packed
 
 
 def moe_last_device_error(ws, stream=None) -> int:

@@ -65,7 +65,28 @@ struct GemmArgs {
     int E, cap, K, n_out;
     int w_rows_per_expert;
     int up_row_offset;
+    int w_packed;       // weights in the PACKED layout (see include/moe.h)
 };
+
+// TMA coordinates {column, row} of the 128-row weight tile starting at
+// row-major weight row `wr` (a multiple of 128) for K block `kb`. Row-major:
+// the tile itself. PACKED: the pre-swizzled 16 KB image of that tile and block
+// (gate-up: packets of 256 lines, gate then up; down: 128 lines).
+__device__ __forceinline__ int2 weight_coords(const GemmArgs &a, bool gated, int wr, int kb)
+{
+    if (!a.w_packed)
+        return make_int2(kb * 64, wr);
+    const int KB = a.K / 64;
+    if (gated) {
+        const int two_i = a.w_rows_per_expert, i = a.up_row_offset;
+        const int e = wr / two_i, rem = wr - e * two_i;
+        const int half = rem >= i ? 1 : 0;
+        const int nt = (rem - half * i) >> 7;
+        const long long packet = (static_cast<long long>(e) * (i >> 7) + nt) * KB + kb;
+        return make_int2(0, static_cast<int>(packet * 256 + half * 128));
+    }
+    return make_int2(0, static_cast<int>((static_cast<long long>(wr >> 7) * KB + kb) * 128));
+}
 
 __host__ __device__ constexpr int pow2_at_least(int v)
 {
@@ -320,9 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_dst = w_dst + C::kWBytes;
                     mbar_arrive_expect_tx(full, C::kStageBytes);
                     const int kc = (kb0 + kb) * kBK;
-                    tma_load_2d(w_dst, &tm_w, full, kc, w_row0, pol_w);
-                    if (C::kWRows == 256)
-                        tma_load_2d(w_dst + 128 * 128, &tm_w, full, kc, w_row1, pol_w);
+                    const int2 w0 = weight_coords(args, kGated, w_row0, kb0 + kb);
+                    tma_load_2d(w_dst, &tm_w, full, w0.x, w0.y, pol_w);
+                    if (C::kWRows == 256) {
+                        const int2 w1 = weight_coords(args, kGated, w_row1, kb0 + kb);
+                        tma_load_2d(w_dst + 128 * 128, &tm_w, full, w1.x, w1.y, pol_w);
+                    }
                     if (kGather) {
 #pragma unroll
                         for (int g = 0; g < kTileRows / 4; ++g)
@@ -582,7 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int kc = kb * kBK;
                     mbar_arrive_expect_tx_cluster(full0, C::kStageBytes);
                     tma_load_2d_pair(a_dst, &tm_act, full0, kc, a_row, pol_a);
-                    tma_load_2d_pair(b_dst, &tm_w, full0, kc, w_row, pol_w);
+                    const int2 wc = weight_coords(args, kGated, w_row, kb);
+                    tma_load_2d_pair(b_dst, &tm_w, full0, wc.x, wc.y, pol_w);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -700,8 +725,9 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D bf16 tensor [rows, cols] (cols contiguous), box of 64 columns x box_rows rows, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows)
+// 2-D bf16 tensor [rows, cols] (cols contiguous), box of 64 columns x box_rows rows, 128-byte swizzle
+// (none for data that is already stored as swizzled shared-memory images).
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows, bool swizzle = true)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -711,9 +737,20 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Weight tensor map: row-major [E * rows_per_expert, K] with swizzle, or the
+// packed buffer as [bytes / 128, 64] lines of pre-swizzled images, no swizzle.
+bool make_weight_map(CUtensorMap *m, const GemmProblem &p)
+{
+    const uint64_t rows = static_cast<uint64_t>(p.E) * p.w_rows_per_expert;
+    if (!p.w_packed)
+        return make_map(m, p.w, rows, static_cast<uint64_t>(p.K), 128);
+    return make_map(m, p.w, rows * static_cast<uint64_t>(p.K) / 64, 64, 128, false);
 }
 
 template <bool kSmallM, bool kGated, int kTileRows, int kStages, int kSplitK = 1, bool kGather = false>
@@ -734,7 +771,7 @@ cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
     }
     CUtensorMap tm_act, tm_w;
     if (!make_map(&tm_act, p.act, static_cast<uint64_t>(p.act_rows), static_cast<uint64_t>(p.K), kGather ? 1 : kTileRows) ||
-        !make_map(&tm_w, p.w, static_cast<uint64_t>(p.E) * p.w_rows_per_expert, static_cast<uint64_t>(p.K), 128))
+        !make_weight_map(&tm_w, p))
         return cudaErrorInvalidValue;
     GemmArgs a;
     a.expert_offsets = p.expert_offsets;
@@ -749,6 +786,7 @@ cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
     a.n_out = p.n_out;
     a.w_rows_per_expert = p.w_rows_per_expert;
     a.up_row_offset = p.up_row_offset;
+    a.w_packed = p.w_packed ? 1 : 0;
     // Upper bound of the units any routing can produce; no more CTAs than that.
     const long long max_row_tiles = (static_cast<long long>(p.cap) + kTileRows - 1) / kTileRows + p.E;
     const long long max_units = max_row_tiles * (p.n_out / C::kOutCols) * kSplitK;
@@ -793,7 +831,7 @@ cudaError_t run_pair(const GemmProblem &p, int num_sms, cudaStream_t stream)
     }
     CUtensorMap tm_act, tm_w;
     if (!make_map(&tm_act, p.act, static_cast<uint64_t>(p.act_rows), static_cast<uint64_t>(p.K), 128) ||
-        !make_map(&tm_w, p.w, static_cast<uint64_t>(p.E) * p.w_rows_per_expert, static_cast<uint64_t>(p.K), 128))
+        !make_weight_map(&tm_w, p))
         return cudaErrorInvalidValue;
     GemmArgs a;
     a.expert_offsets = p.expert_offsets;
@@ -808,6 +846,7 @@ cudaError_t run_pair(const GemmProblem &p, int num_sms, cudaStream_t stream)
     a.n_out = p.n_out;
     a.w_rows_per_expert = p.w_rows_per_expert;
     a.up_row_offset = p.up_row_offset;
+    a.w_packed = p.w_packed ? 1 : 0;
     const long long max_units = ((static_cast<long long>(p.cap) + 255) / 256 + p.E) * (p.n_out / C::kOutCols);
     long long clusters = max_units < max_clusters ? max_units : max_clusters;
     if (clusters < 1)

@@ -53,9 +53,11 @@ moe_status_t check_problem(const moe_problem_t *p)
     if (!p)
         return MOE_ERR_NULL;
     if (p->T_max < 1 || p->E < 1 || p->E > kMaxExperts || p->k < 1 || p->k > p->E || p->k > kMaxTopK ||
-        p->H < 1 || p->I < 1 || p->reserved != 0)
+        p->H < 1 || p->I < 1)
         return MOE_ERR_SHAPE;
     if (p->path < MOE_PATH_AUTO || p->path > MOE_PATH_TILED_1CTA)
+        return MOE_ERR_SHAPE;
+    if (p->weight_layout != MOE_WEIGHTS_ROW_MAJOR && p->weight_layout != MOE_WEIGHTS_PACKED)
         return MOE_ERR_SHAPE;
     const long long R = static_cast<long long>(p->T_max) * p->k;
     if (R > (1LL << 28))
@@ -175,6 +177,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
     g.cap = capacity_of(p);
     g.small_m = path == MOE_PATH_SMALL_M;
     g.cta_pair = path == MOE_PATH_TILED;
+    g.w_packed = p.weight_layout == MOE_WEIGHTS_PACKED;
     g.tile_rows = tile_rows;
     g.split_k = 1;
     g.pdl = path == MOE_PATH_SMALL_M;
@@ -439,6 +442,23 @@ moe_status_t moe_forward_profiled(const moe_problem_t *problem, const void *x, c
             return MOE_ERR_NULL;
     return forward_impl(problem, x, topk_ids, topk_weights, d_num_tokens, W13, W2, expert_offsets, perm, out, ws,
                         ws_bytes, stream, stage_events);
+}
+
+moe_status_t moe_pack_weights(const moe_problem_t *problem, const void *W13, const void *W2, void *W13_packed,
+                              void *W2_packed, void *stream)
+{
+    moe_status_t st = check_problem(problem);
+    if (st != MOE_OK)
+        return st;
+    const moe_problem_t &p = *problem;
+    if (!W13 || !W2 || !W13_packed || !W2_packed)
+        return MOE_ERR_NULL;
+    if (!aligned16(W13) || !aligned16(W2) || !aligned16(W13_packed) || !aligned16(W2_packed))
+        return MOE_ERR_ALIGN;
+    if ((st = check_device()) != MOE_OK)
+        return st;
+    return cuda_status(launch_pack_weights(W13, W2, W13_packed, W2_packed, p.E, p.H, p.I, device_sm_count(),
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_last_device_error(const void *ws, void *stream, int32_t *host_code)

@@ -67,6 +67,10 @@ cudaError_t launch_combine(const float *y_sorted, const int32_t *inv, const floa
                            const int32_t *d_num_tokens, int T_max, int k, int H, void *out, int num_sms,
                            cudaStream_t stream, bool pdl);
 
+// ---- packed weights (weights_pack.cu) ----
+cudaError_t launch_pack_weights(const void *W13, const void *W2, void *W13_packed, void *W2_packed, int E, int H,
+                                int I, int num_sms, cudaStream_t stream);
+
 // ---- expert GEMMs (grouped_gemm.cu) ----
 struct GemmProblem {
     const void *act;          // [act_rows, K] bf16: sorted rows, or x itself when gather is set
@@ -87,6 +91,7 @@ struct GemmProblem {
     int split_k;              // 1, or 2 (M-small down GEMM only: two K halves added into a zeroed fp32 out)
     bool pdl;                 // programmatic dependent launch
     bool cta_pair;            // tiled path on 2-CTA clusters (tcgen05 cta_group::2)
+    bool w_packed;            // `w` is in the access-ordered PACKED layout
 };
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);

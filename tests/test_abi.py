@@ -67,9 +67,10 @@ def test_workspace_size_and_path(lib):
 @pytest.mark.parametrize("bad,status", [
     (dict(T_max=0), 2), (dict(E=0), 2), (dict(E=1025), 2), (dict(k=0), 2), (dict(k=9, E=8), 2),
     (dict(H=300), 3), (dict(I=100), 3), (dict(capacity=5), 2), (dict(path=7), 2), (dict(path=-1), 2),
+    (dict(weight_layout=2), 2),
 ])
 def test_problem_validation(lib, bad, status):
-    args = dict(T_max=64, E=8, k=2, H=256, I=512, capacity=0, path=0)
+    args = dict(T_max=64, E=8, k=2, H=256, I=512, capacity=0, path=0, weight_layout=0)
     args.update(bad)
     p = lib.Problem.make(**args)
     with pytest.raises(lib.MoeError) as ei:
@@ -101,3 +102,5 @@ def test_entry_points_fail_closed_without_touching_the_device(lib):
     assert so.moe_forward(None, fake, fake, fake, None, fake, fake, fake, fake, fake, fake, need, None) == 1
     code = ctypes.c_int32(0)
     assert so.moe_last_device_error(None, None, ctypes.byref(code)) == 1
+    assert so.moe_pack_weights(P, fake, fake, None, fake, None) == 1
+    assert so.moe_pack_weights(P, fake, fake, fake + 8, fake, None) == 3
