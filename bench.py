@@ -55,14 +55,15 @@ LAUNCHES_PER_FORWARD = 7   # count, scan, scatter, gather, gate-up GEMM, down GE
 GRAPH_STEPS = 10
 
 # DRAM traffic of the dominant kernel (gate-up GEMM) from an ncu capture
-# (profiles/gemm_small_m_decode8_E24.md: dram__bytes_read.sum +
-# dram__bytes_write.sum = 1.7648 GB for one launch with 20 touched experts).
+# (profiles/packed_weights_decode.md: dram__bytes_read.sum +
+# dram__bytes_write.sum = 1.7647 GB for one launch with 20 touched experts,
+# the same for row-major and packed weights).
 # The M-small gate-up GEMM reads each touched expert's weights exactly once, so
 # the capture is scaled to a launch by its touched experts. Keyed to the sha256
 # of the GEMM sources at capture time: after any change, traffic reports null.
 NCU_TRAFFIC = {
-    "kernel_sha256": "8f9a138d87d9c6a20dc615df94624dcde032d2c4f843ccf12fc4ff251b759b30",
-    "small_m_gate_up_bytes_per_touched_expert": 1.7648e9 / 20,
+    "kernel_sha256": "638c40b11fd1b273b1f2f95920a755762f8896bd59e78fe1231a72258b25f46c",
+    "small_m_gate_up_bytes_per_touched_expert": 1.7647e9 / 20,
 }
 
 
