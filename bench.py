@@ -54,16 +54,18 @@ STAGES = ["dispatch", "gather", "gemm_gate_up", "gemm_down", "combine"]
 LAUNCHES_PER_FORWARD = 7   # count, scan, scatter, gather, gate-up GEMM, down GEMM, combine
 GRAPH_STEPS = 10
 
-# DRAM traffic of the dominant kernel (gate-up GEMM) from an ncu capture
-# (profiles/packed_weights_decode.md: dram__bytes_read.sum +
-# dram__bytes_write.sum = 1.7647 GB for one launch with 20 touched experts,
-# the same for row-major and packed weights).
-# The M-small gate-up GEMM reads each touched expert's weights exactly once, so
-# the capture is scaled to a launch by its touched experts. Keyed to the sha256
-# of the GEMM sources at capture time: after any change, traffic reports null.
+# DRAM traffic of the dominant kernel from ncu captures of the decode T=8 shape
+# with E=24 (20 touched experts; dram__bytes_read.sum + dram__bytes_write.sum per
+# launch): the fused M-small kernel (both GEMMs) 2.6446 GB
+# (profiles/fused_small_decode8_E24.md), the gate-up GEMM alone 1.7647 GB
+# (profiles/packed_weights_decode.md). Both read each touched expert's weights
+# exactly once, so a capture is scaled to a launch by its touched experts.
+# Keyed to the sha256 of the GEMM sources at capture time: after any change,
+# traffic reports null.
 NCU_TRAFFIC = {
-    "kernel_sha256": "638c40b11fd1b273b1f2f95920a755762f8896bd59e78fe1231a72258b25f46c",
+    "kernel_sha256": "2e49da369cb146b4b921246d2aae6c74bc6a4d58236508d7e644c0e869035756",
     "small_m_gate_up_bytes_per_touched_expert": 1.7647e9 / 20,
+    "small_m_fused_bytes_per_touched_expert": 2.6446e9 / 20,
 }
 
 
@@ -286,6 +288,7 @@ def run_ours(args, world, rank, local):
             torch.cuda.empty_cache()
         d["bufs"] = B.Buffers(d["problem"], device)
         d["path"] = B.moe_resolve_path(d["problem"])
+        d["profile"] = B.moe_resolve_profile(d["problem"])
     stream = torch.cuda.Stream(device)
 
     def new_events():
@@ -386,10 +389,12 @@ def run_ours(args, world, rank, local):
     value = world * flops_step * K / (max_ms * 1e-3) / 1e12
     peaks = load_peaks()
 
-    # dominant kernel: the gate-up GEMM (2/3 of the FLOPs and weight bytes)
-    g1_us = sum(float(s[2]) for s in stage_us)
-    g1_flops = sum(d["acct"]["gemm1_flops"] for d in inputs)
-    g1_bytes = sum(d["acct"]["gemm1_bytes"] for d in inputs)
+    # dominant kernel: the gate-up GEMM (2/3 of the FLOPs and weight bytes); on
+    # the M-small path both GEMMs run as one persistent kernel, timed as one
+    fused = all(d["profile"]["fused_mlp"] for d in inputs)
+    g1_us = sum(float(s[2]) + (float(s[3]) if fused else 0.0) for s in stage_us)
+    g1_flops = sum(d["acct"]["gemm1_flops"] * (1.5 if fused else 1.0) for d in inputs)
+    g1_bytes = sum(d["acct"]["gemm1_bytes"] + (d["acct"]["gemm2_bytes"] if fused else 0.0) for d in inputs)
     t_tensor = g1_flops / (peaks["bf16_tflops_sustained"] * 1e12)
     t_hbm = g1_bytes / (peaks["hbm_gbs"] * 1e9)
     if t_tensor > t_hbm:
@@ -401,12 +406,13 @@ def run_ours(args, world, rank, local):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "peak_kind": f"HBM copy, {peaks['source']}"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = "grouped_gemm_kernel (gate-up, SiLU*up epilogue)"
+    roof["kernel"] = ("fused_small_kernel (gate-up + down, one persistent launch)" if fused
+                      else "grouped_gemm_kernel (gate-up, SiLU*up epilogue)")
     roof["algorithmic_per_step"] = g1_flops if roof["bound"] == "tensor" else g1_bytes
     traffic = None
-    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and all(d["path"][0] == 2 for d in inputs):
-        per = [d["acct"]["touched_experts"] * NCU_TRAFFIC["small_m_gate_up_bytes_per_touched_expert"]
-               for d in inputs]
+    key = "small_m_fused_bytes_per_touched_expert" if fused else "small_m_gate_up_bytes_per_touched_expert"
+    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and key in NCU_TRAFFIC and all(d["path"][0] == 2 for d in inputs):
+        per = [d["acct"]["touched_experts"] * NCU_TRAFFIC[key] for d in inputs]
         traffic = float(sum(per)) / len(per)
     roof["traffic"] = traffic
     roof["traffic_note"] = ("ncu dram read+write bytes per launch, scaled from a 20-expert capture by touched experts"

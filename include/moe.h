@@ -124,7 +124,8 @@ typedef struct moe_profile {
     int32_t pdl;           /* 1: kernels of a call use programmatic dependent launch */
     int32_t fused_gather;  /* 1: moe_forward's gate-up GEMM gathers rows from x (no x_sorted) */
     int32_t cta_pair;      /* 1: tiled GEMMs run on 2-CTA clusters */
-    int32_t reserved[2];
+    int32_t fused_mlp;     /* 1: moe_forward runs both GEMMs as one persistent kernel */
+    int32_t reserved;
 } moe_profile_t;
 
 moe_status_t moe_resolve_profile(const moe_problem_t *problem, moe_profile_t *profile);

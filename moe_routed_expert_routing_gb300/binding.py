@@ -81,7 +81,7 @@ class Profile(ctypes.Structure):
 
     _fields_ = [("path", ctypes.c_int32), ("tile_rows", ctypes.c_int32), ("down_split_k", ctypes.c_int32),
                 ("pdl", ctypes.c_int32), ("fused_gather", ctypes.c_int32), ("cta_pair", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("fused_mlp", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}

@@ -18,7 +18,7 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-    size_t err, block_counts, block_base, h, x_sorted, y_sorted, inv, total;
+    size_t err, block_counts, block_base, h, x_sorted, y_sorted, inv, ready, total;
 };
 
 int capacity_of(const moe_problem_t &p) { return p.capacity ? p.capacity : p.T_max * p.k; }
@@ -44,6 +44,8 @@ Layout layout_of(const moe_problem_t &p)
     o = align_up(o + 4 * cap * p.H);
     L.inv = o;
     o = align_up(o + sizeof(int32_t) * R);
+    L.ready = o;   // per-expert count of finished gate-up units (fused M-small kernel)
+    o = align_up(o + sizeof(int32_t) * p.E);
     L.total = o;
     return L;
 }
@@ -158,7 +160,7 @@ bool down_split_k(const moe_problem_t &p, int path, int tile_rows, int sms)
 moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, const int32_t *expert_offsets,
                                     const void *W13, const void *W2, float *y_sorted, void *ws, cudaStream_t s,
                                     void *const *stage_events = nullptr, bool y_zeroed = false,
-                                    const int32_t *gather_perm = nullptr)
+                                    const int32_t *gather_perm = nullptr, bool fused = false)
 {
     const Layout L = layout_of(p);
     int path = 0, tile_rows = 0;
@@ -194,11 +196,15 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
     g.w_rows_per_expert = 2 * p.I;
     g.up_row_offset = p.I;
     g.gated = true;
-    moe_status_t st = cuda_status(launch_grouped_gemm(g, sms, s));
-    if (st != MOE_OK)
-        return st;
-    if ((st = record_stage(stage_events, 3, s)) != MOE_OK)
-        return st;
+    GemmProblem up = g;
+    moe_status_t st = MOE_OK;
+    if (!fused) {
+        st = cuda_status(launch_grouped_gemm(g, sms, s));
+        if (st != MOE_OK)
+            return st;
+        if ((st = record_stage(stage_events, 3, s)) != MOE_OK)
+            return st;
+    }
     // down: h[cap, I] x W2[E, H, I] -> y_sorted[cap, H] (fp32)
     g.act = at<void>(ws, L.h);
     g.gather = false;
@@ -212,7 +218,13 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
     g.up_row_offset = 0;
     g.gated = false;
     g.split_k = split ? 2 : 1;
-    return cuda_status(launch_grouped_gemm(g, sms, s));
+    if (!fused)
+        return cuda_status(launch_grouped_gemm(g, sms, s));
+    // both GEMMs in one persistent launch; its stage marks share one instant
+    st = cuda_status(launch_fused_small(up, g, at<int32_t>(ws, L.ready), sms, s));
+    if (st != MOE_OK)
+        return st;
+    return record_stage(stage_events, 3, s);
 }
 
 }  // namespace
@@ -295,6 +307,7 @@ moe_status_t moe_resolve_profile(const moe_problem_t *problem, moe_profile_t *pr
     profile->pdl = use_pdl(*problem) ? 1 : 0;
     profile->fused_gather = path == MOE_PATH_SMALL_M ? 1 : 0;
     profile->cta_pair = path == MOE_PATH_TILED ? 1 : 0;
+    profile->fused_mlp = (path == MOE_PATH_SMALL_M && tile_rows == 16) ? 1 : 0;
     return MOE_OK;
 }
 
@@ -394,6 +407,13 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
     if (split && cudaMemsetAsync(y_sorted, 0, sizeof(float) * static_cast<size_t>(capacity_of(p)) * p.H, s) !=
                      cudaSuccess)
         return MOE_ERR_CUDA;
+    // decode-size batches (M-small, 16-row token tiles): both GEMMs run as one
+    // persistent kernel whose down units wait on per-expert counts; those start
+    // from zero every call. Measured in one process against two launches:
+    // -1.3% per decode step; +2% on 32-row tiles, which keep two launches.
+    const bool fused_mlp = path == MOE_PATH_SMALL_M && tile_rows == 16;
+    if (fused_mlp && cudaMemsetAsync(at<int32_t>(ws, L.ready), 0, sizeof(int32_t) * p.E, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
     if ((st = mark(0)) != MOE_OK)
         return st;
     st = cuda_status(launch_dispatch(topk_ids, d_num_tokens, p.T_max, p.k, p.E, at<int32_t>(ws, L.block_counts),
@@ -412,7 +432,7 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
     if (st != MOE_OK || (st = mark(2)) != MOE_OK)
         return st;
     st = enqueue_expert_compute(p, fused_gather ? x : x_sorted, expert_offsets, W13, W2, y_sorted, ws, s,
-                                stage_events, true, fused_gather ? perm : nullptr);
+                                stage_events, true, fused_gather ? perm : nullptr, fused_mlp);
     if (st != MOE_OK || (st = mark(4)) != MOE_OK)
         return st;
     st = cuda_status(

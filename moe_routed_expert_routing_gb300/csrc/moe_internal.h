@@ -96,6 +96,11 @@ struct GemmProblem {
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);
 
+// Both M-small GEMMs in one persistent launch (gate-up with gathered rows, then
+// down); ready[E] must be zero when the kernel starts.
+cudaError_t launch_fused_small(const GemmProblem &up, const GemmProblem &down, int32_t *ready, int num_sms,
+                               cudaStream_t stream);
+
 // number of SMs of the current device (cached)
 int device_sm_count();
 

@@ -117,6 +117,27 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_b
                  : "memory");
 }
 
+// ---------------------------------------------------------------- inter-CTA flags
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int32_t *p, int v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Order this thread's earlier generic-proxy accesses (e.g. the acquire that
+// saw another CTA's stores) before its later async-proxy (TMA) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first()

@@ -149,12 +149,47 @@ def test_launch_profile_table(B):
     """The static profile follows from the shape alone (a = T_max*k/E rows per expert)."""
     P = B.Problem.make
     dec1 = B.moe_resolve_profile(P(1, 384, 6, 7168, 3072))
-    assert dec1 == dict(path=2, tile_rows=16, down_split_k=2, pdl=1, fused_gather=1, cta_pair=0)
+    assert dec1 == dict(path=2, tile_rows=16, down_split_k=2, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1)
     dec8 = B.moe_resolve_profile(P(8, 384, 6, 7168, 3072))
-    assert dec8 == dict(path=2, tile_rows=16, down_split_k=1, pdl=1, fused_gather=1, cta_pair=0)
+    assert dec8 == dict(path=2, tile_rows=16, down_split_k=1, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1)
     small = B.moe_resolve_profile(P(128, 256, 8, 7168, 2048))
-    assert small["path"] == 2 and small["tile_rows"] == 32 and small["down_split_k"] == 1
+    assert small["path"] == 2 and small["tile_rows"] == 32 and small["down_split_k"] == 1 and small["fused_mlp"] == 0
     prefill = B.moe_resolve_profile(P(2048, 384, 6, 7168, 3072))
-    assert prefill == dict(path=3, tile_rows=128, down_split_k=1, pdl=0, fused_gather=0, cta_pair=0)
+    assert prefill == dict(path=3, tile_rows=128, down_split_k=1, pdl=0, fused_gather=0, cta_pair=0, fused_mlp=0)
     large = B.moe_resolve_profile(P(8192, 128, 8, 4096, 1536))
-    assert large == dict(path=1, tile_rows=128, down_split_k=1, pdl=0, fused_gather=0, cta_pair=1)
+    assert large == dict(path=1, tile_rows=128, down_split_k=1, pdl=0, fused_gather=0, cta_pair=1, fused_mlp=0)
+
+
+def test_fused_decode_kernel_graph_replay_token_counts(B):
+    """Decode-size batches run both GEMMs as one persistent kernel with per-expert
+    readiness counts: captured once, replayed with T in {8, 3, 1, 0}, every
+    replay equals an eager call bit for bit and the oracle within tolerance."""
+    wl = wlm.custom("fusedgraph", 8, 64, 4, 512, 256, seed=44)
+    dw = DeviceWorkload(wl)
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
+    assert B.moe_resolve_profile(p)["fused_mlp"] == 1
+    bufs = B.Buffers(p)
+    d_T = torch.tensor([wl.T], dtype=torch.int32, device="cuda")
+    forward(B, p, dw, bufs, d_T=d_T)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            B.moe_forward(p, dw.x, dw.ids, dw.w, dw.W13, dw.W2, bufs.expert_offsets, bufs.perm, bufs.out, bufs.ws,
+                          d_num_tokens=d_T, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for T_dev in (8, 3, 1, 0):
+        d_T.fill_(T_dev)
+        bufs.out.fill_(5.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert B.moe_last_device_error(bufs.ws) == 0
+        assert torch.all(bufs.out[T_dev:] == 5.0)
+        if T_dev == 0:
+            continue
+        eager = B.Buffers(p)
+        forward(B, p, dw, eager, d_T=d_T)
+        assert torch.equal(bufs.out[:T_dev].view(torch.int16), eager.out[:T_dev].view(torch.int16))
+        ref_acc, _ = dw.oracle_out(np.arange(T_dev, dtype=np.int32))
+        assert_within_tolerance(wlm.bf16_bits(bufs.out[:T_dev]), ref_acc, f"fused T={T_dev}")
