@@ -51,21 +51,20 @@ WORKLOAD_SETS = {
     "large": ["large"],
 }
 STAGES = ["dispatch", "gather", "gemm_gate_up", "gemm_down", "combine"]
-LAUNCHES_PER_FORWARD = 7   # count, scan, scatter, gather, gate-up GEMM, down GEMM, combine
 GRAPH_STEPS = 10
 
 # DRAM traffic of the dominant kernel from ncu captures of the decode T=8 shape
 # with E=24 (20 touched experts; dram__bytes_read.sum + dram__bytes_write.sum per
-# launch): the fused M-small kernel (both GEMMs) 2.6446 GB
-# (profiles/fused_small_decode8_E24.md), the gate-up GEMM alone 1.7647 GB
-# (profiles/packed_weights_decode.md). Both read each touched expert's weights
-# exactly once, so a capture is scaled to a launch by its touched experts.
-# Keyed to the sha256 of the GEMM sources at capture time: after any change,
-# traffic reports null.
+# launch): the fused M-small kernel (both GEMMs; separate and one-kernel forms
+# alike) 2.6439 GB (profiles/fused_small_decode8_E24.md), the gate-up GEMM alone
+# 1.7647 GB (profiles/packed_weights_decode.md). Both read each touched
+# expert's weights exactly once, so a capture is scaled to a launch by its
+# touched experts. Keyed to the sha256 of the GEMM sources at capture time:
+# after any change, traffic reports null.
 NCU_TRAFFIC = {
-    "kernel_sha256": "2e49da369cb146b4b921246d2aae6c74bc6a4d58236508d7e644c0e869035756",
+    "kernel_sha256": "ffe54f89261158667c5696bbaf227efb8ff9f85cc001733a966de17dbafba6b9",
     "small_m_gate_up_bytes_per_touched_expert": 1.7647e9 / 20,
-    "small_m_fused_bytes_per_touched_expert": 2.6446e9 / 20,
+    "small_m_fused_bytes_per_touched_expert": 2.6439e9 / 20,
 }
 
 
@@ -281,7 +280,8 @@ def run_ours(args, world, rank, local):
     layout = B.MOE_WEIGHTS_PACKED if args.packed else B.MOE_WEIGHTS_ROW_MAJOR
     for d in inputs:
         wl = d["wl"]
-        d["problem"] = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path, weight_layout=layout)
+        d["problem"] = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path, weight_layout=layout,
+                                      forward_form=args.form)
         if args.packed:   # model-load transform; the row-major copy is released
             d["W13"], d["W2"] = B.moe_pack_weights(d["problem"], d["W13"], d["W2"])
             torch.cuda.synchronize(device)
@@ -390,9 +390,17 @@ def run_ours(args, world, rank, local):
     peaks = load_peaks()
 
     # dominant kernel: the gate-up GEMM (2/3 of the FLOPs and weight bytes); on
-    # the M-small path both GEMMs run as one persistent kernel, timed as one
+    # the M-small path both GEMMs run as one persistent kernel, timed as one;
+    # for decode batches that kernel is the whole call (all stage marks after it)
     fused = all(d["profile"]["fused_mlp"] for d in inputs)
-    g1_us = sum(float(s[2]) + (float(s[3]) if fused else 0.0) for s in stage_us)
+    mega = [d["profile"]["megakernel"] for d in inputs]
+
+    def kernel_us(d, s):
+        if d["profile"]["megakernel"]:
+            return float(sum(s))
+        return float(s[2]) + (float(s[3]) if fused else 0.0)
+
+    g1_us = sum(kernel_us(d, s) for d, s in zip(inputs, stage_us))
     g1_flops = sum(d["acct"]["gemm1_flops"] * (1.5 if fused else 1.0) for d in inputs)
     g1_bytes = sum(d["acct"]["gemm1_bytes"] + (d["acct"]["gemm2_bytes"] if fused else 0.0) for d in inputs)
     t_tensor = g1_flops / (peaks["bf16_tflops_sustained"] * 1e12)
@@ -406,8 +414,10 @@ def run_ours(args, world, rank, local):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "peak_kind": f"HBM copy, {peaks['source']}"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = ("fused_small_kernel (gate-up + down, one persistent launch)" if fused
-                      else "grouped_gemm_kernel (gate-up, SiLU*up epilogue)")
+    roof["kernel"] = ("fused_small_kernel (gate-up + down in one persistent launch"
+                      + ("; the whole forward for " + ", ".join(d["wl"].name for d, m in zip(inputs, mega) if m)
+                         if any(mega) else "") + ")"
+                      if fused else "grouped_gemm_kernel (gate-up, SiLU*up epilogue)")
     roof["algorithmic_per_step"] = g1_flops if roof["bound"] == "tensor" else g1_bytes
     traffic = None
     key = "small_m_fused_bytes_per_touched_expert" if fused else "small_m_gate_up_bytes_per_touched_expert"
@@ -450,7 +460,9 @@ def run_ours(args, world, rank, local):
         },
         "us_per_call": {d["wl"].name: float(sum(s)) for d, s in zip(inputs, stage_us)},
         "profiled_ms_per_step": prof_ms_per_step,
-        "stages_us": {d["wl"].name: {k: float(v) for k, v in zip(STAGES, s)} for d, s in zip(inputs, stage_us)},
+        "stages_us": {d["wl"].name: ({"forward_one_kernel": float(sum(s))} if d["profile"]["megakernel"]
+                                     else {k: float(v) for k, v in zip(STAGES, s)})
+                      for d, s in zip(inputs, stage_us)},
         "tflops_per_call": {d["wl"].name: d["acct"]["flops"] / (float(sum(s)) * 1e-6) / 1e12
                             for d, s in zip(inputs, stage_us)},
         "call_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": ms_per_step * 1e3,
@@ -459,7 +471,7 @@ def run_ours(args, world, rank, local):
                                                         * d["wl"].I / 1e9 for d in inputs}},
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": LAUNCHES_PER_FORWARD * len(inputs) * K,
+        "gpu_launches": sum(d["profile"]["kernel_launches"] for d in inputs) * K,
         "clocks": clk,
     }
     if rank == 0 and args.packed:
@@ -544,7 +556,7 @@ def run_sweep(args, world, rank, local):
         x = wlm.make_x(wl, device)
         ids = torch.from_numpy(ids_np).to(device)
         w = torch.from_numpy(w_np).to(device)
-        p = B.Problem.make(T, wl.E, wl.k, wl.H, wl.I, path=args.path)
+        p = B.Problem.make(T, wl.E, wl.k, wl.H, wl.I, path=args.path, forward_form=args.form)
         bufs = B.Buffers(p, device)
         acct = call_accounting(wl, ids_np)
 
@@ -583,6 +595,69 @@ def run_sweep(args, world, rank, local):
     return {"sweep": "token count", "shape": f"E={base.E} k={base.k} H={base.H} I={base.I}, bf16, uniform routing",
             "steps_per_point": max(1, args.steps // GRAPH_STEPS) * GRAPH_STEPS, "rows": rows,
             "peaks": peaks}
+
+
+def run_compare_forms(args, world, rank, local):
+    """Decode-size forward as three kernels (MOE_FORWARD_SEPARATE) against one
+    (MOE_FORWARD_ONE_KERNEL), per batch of the workload set: both captured as
+    graphs of GRAPH_STEPS calls and replayed alternately in one process (an
+    A/B in one process, as the DeepGEMM page measures its variants), median
+    of 7 rounds of 20 replays. Not the bench line."""
+    from moe_routed_expert_routing_gb300.build import build
+    build()
+    from moe_routed_expert_routing_gb300 import binding as B
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    forms = {"separate": B.MOE_FORWARD_SEPARATE, "one_kernel": B.MOE_FORWARD_ONE_KERNEL}
+    rows = []
+    for name in WORKLOAD_SETS[args.workload]:
+        d = make_inputs([name], device, args.experts, args.tokens)[0]
+        wl = d["wl"]
+        graphs, bufs = {}, {}
+        for f, code in forms.items():
+            p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path, forward_form=code)
+            bufs[f] = B.Buffers(p, device)
+
+            def fwd(p=p, b=bufs[f]):
+                B.moe_forward(p, d["x"], d["ids"], d["w"], d["W13"], d["W2"], b.expert_offsets, b.perm, b.out,
+                              b.ws, stream=stream)
+
+            with torch.cuda.stream(stream):
+                fwd()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(g, stream=stream):
+                    for _ in range(GRAPH_STEPS):
+                        fwd()
+            graphs[f] = g
+        us = {f: [] for f in forms}
+        for _ in range(7):
+            for f, g in graphs.items():
+                with torch.cuda.stream(stream):
+                    for _ in range(2):
+                        g.replay()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(20):
+                        g.replay()
+                    e1.record(stream)
+                torch.cuda.synchronize(device)
+                us[f].append(e0.elapsed_time(e1) * 1e3 / (20 * GRAPH_STEPS))
+        for f in forms:
+            if B.moe_last_device_error(bufs[f].ws, stream):
+                raise RuntimeError(f"device error ({f}) on {name}")
+        same = torch.equal(bufs["separate"].out.view(torch.int16), bufs["one_kernel"].out.view(torch.int16))
+        rows.append({"workload": wl.describe(), "us_per_call": {f: float(np.median(v)) for f, v in us.items()},
+                     "rounds_us": {f: [round(x, 2) for x in v] for f, v in us.items()},
+                     "bit_identical": bool(same), "auto_picks": "one_kernel" if B.moe_resolve_profile(
+                         B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path))["megakernel"] else "separate"})
+        del graphs, bufs, d
+        torch.cuda.empty_cache()
+    return {"compare": "moe_forward forms (separate kernels vs one kernel)", "rows": rows}
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -642,6 +717,10 @@ def parse_args(argv=None):
     ap.add_argument("--sweep", action="store_true", help="token-count sweep at the 384-expert shape (not the bench line)")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3],
                     help="expert-GEMM path: 0 auto, 1 tiled CTA pairs, 2 M-small, 3 tiled single CTA")
+    ap.add_argument("--form", type=int, default=0, choices=[0, 1, 2],
+                    help="decode-size forward: 0 auto, 1 separate kernels, 2 one kernel")
+    ap.add_argument("--compare-forms", action="store_true",
+                    help="decode-size forward: separate kernels vs one kernel, alternating (not the bench line)")
     return ap.parse_args(argv)
 
 
@@ -661,6 +740,10 @@ def main(argv=None):
     if args.sweep:
         if rank == 0:
             print(json.dumps(run_sweep(args, world, rank, local)), flush=True)
+        return 0
+    if args.compare_forms:
+        if rank == 0:
+            print(json.dumps(run_compare_forms(args, world, rank, local)), flush=True)
         return 0
     if args.cpu_tokens == 0:
         wl_T = max(wlm.WORKLOADS[n].T for n in WORKLOAD_SETS[args.workload])

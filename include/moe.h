@@ -85,7 +85,24 @@ typedef struct moe_problem {
     int32_t capacity; /* rows of the sorted batch; 0 means T_max*k; else >= T_max*k */
     int32_t path;     /* moe_path_t */
     int32_t weight_layout; /* moe_weight_layout_t of W13 and W2 */
+    int32_t forward_form;  /* moe_forward_form_t */
 } moe_problem_t;
+
+/* How moe_forward launches decode-size batches (M-small path, 16-row token
+ * tiles). ONE_KERNEL: dispatch, both GEMMs and the combine as one persistent
+ * kernel (results bit-identical to SEPARATE); moe_forward and
+ * moe_resolve_profile return MOE_ERR_UNSUPPORTED for a problem that is not
+ * decode-size or whose tables do not fit that kernel's shared memory.
+ * SEPARATE: dispatch, the two fused GEMMs and the combine as three kernels
+ * chained by programmatic dependent launch. AUTO: ONE_KERNEL where the down
+ * GEMM splits K (the smallest batches: measured 132.4 vs 133.4 us for one
+ * token at E=384, H=7168, I=3072), SEPARATE otherwise (873.6 vs 875.8 us for
+ * eight tokens). Other problems ignore the field. */
+typedef enum moe_forward_form {
+    MOE_FORWARD_AUTO = 0,
+    MOE_FORWARD_SEPARATE = 1,
+    MOE_FORWARD_ONE_KERNEL = 2
+} moe_forward_form_t;
 
 /* Layout of W13 / W2 in memory.
  *  ROW_MAJOR: W13[E, 2I, H], W2[E, H, I] bf16, row-major.
@@ -104,8 +121,13 @@ typedef enum moe_weight_layout {
 
 /* Bytes of workspace every entry point below needs for `problem` (pure host
  * arithmetic, no CUDA call). The same workspace serves all entry points; it
- * holds the device error word, dispatch scratch, the activation h[cap, I]
- * and, for moe_forward, the sorted batches. */
+ * holds the device error word, the decode kernel's counters, dispatch
+ * scratch, the activation h[cap, I] and, for moe_forward, the sorted batches.
+ * A new workspace must be zero-filled (cudaMemset, or moe_clear_device_error)
+ * before its first moe_forward call; every call leaves its counters at zero
+ * again (FlashInfer moe_ep page, launch-path notes: workspaces allocated
+ * zeroed, counters cleaned by the kernel's tail), so no per-call clearing is
+ * needed. */
 moe_status_t moe_workspace_size(const moe_problem_t *problem, size_t *bytes);
 
 /* Which expert-GEMM path `problem` resolves to (MOE_PATH_TILED,
@@ -125,7 +147,8 @@ typedef struct moe_profile {
     int32_t fused_gather;  /* 1: moe_forward's gate-up GEMM gathers rows from x (no x_sorted) */
     int32_t cta_pair;      /* 1: tiled GEMMs run on 2-CTA clusters */
     int32_t fused_mlp;     /* 1: moe_forward runs both GEMMs as one persistent kernel */
-    int32_t reserved;
+    int32_t megakernel;    /* 1: moe_forward is that one kernel, dispatch and combine included */
+    int32_t kernel_launches; /* kernels one moe_forward call launches (memsets not counted) */
 } moe_profile_t;
 
 moe_status_t moe_resolve_profile(const moe_problem_t *problem, moe_profile_t *profile);
@@ -186,7 +209,12 @@ moe_status_t moe_combine(const moe_problem_t *problem, const float *y_sorted, co
  * The whole routed expert execution in one call: dispatch (with the row
  * gather) -> expert compute -> combine, all on `stream`, with the sorted
  * batches and inv held in the workspace. Arguments as above; perm and
- * expert_offsets are still returned to the caller.
+ * expert_offsets are still returned to the caller. For decode-size batches
+ * (moe_profile_t.megakernel) the call is a single persistent kernel: every
+ * CTA dispatches the call's slots itself, then runs its share of both GEMMs
+ * and of the combine; its CTAs wait on one another (bounded), so it expects
+ * the GPU's SMs free for its CTAs, one per SM, when it starts. Results equal
+ * those of the separate entry points bit for bit.
  */
 moe_status_t moe_forward(const moe_problem_t *problem, const void *x, const int32_t *topk_ids,
                          const float *topk_weights, const int32_t *d_num_tokens, const void *W13,
@@ -248,7 +276,8 @@ moe_status_t moe_pack_weights(const moe_problem_t *problem, const void *W13, con
  * Synchronises `stream` (the only entry point that does). */
 moe_status_t moe_last_device_error(const void *ws, void *stream, int32_t *host_code);
 
-/* Clear the device error word (enqueued on `stream`). */
+/* Clear the device error word and the decode kernel's counters (enqueued on
+ * `stream`); also readies a workspace of unknown contents for moe_forward. */
 moe_status_t moe_clear_device_error(void *ws, void *stream);
 
 /* Human-readable name of a status. Never NULL. */

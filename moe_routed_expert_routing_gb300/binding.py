@@ -22,6 +22,9 @@ MOE_PATH_SMALL_M = 2
 MOE_PATH_TILED_1CTA = 3
 MOE_WEIGHTS_ROW_MAJOR = 0
 MOE_WEIGHTS_PACKED = 1
+MOE_FORWARD_AUTO = 0
+MOE_FORWARD_SEPARATE = 1
+MOE_FORWARD_ONE_KERNEL = 2
 MOE_DEVERR_BAD_EXPERT_ID = 0x1
 MOE_DEVERR_WAIT_TIMEOUT = 0x2
 
@@ -61,11 +64,14 @@ class Problem(ctypes.Structure):
         ("capacity", ctypes.c_int32),
         ("path", ctypes.c_int32),
         ("weight_layout", ctypes.c_int32),
+        ("forward_form", ctypes.c_int32),
     ]
 
     @classmethod
-    def make(cls, T_max, E, k, H, I, capacity=0, path=MOE_PATH_AUTO, weight_layout=MOE_WEIGHTS_ROW_MAJOR):
-        return cls(int(T_max), int(E), int(k), int(H), int(I), int(capacity), int(path), int(weight_layout))
+    def make(cls, T_max, E, k, H, I, capacity=0, path=MOE_PATH_AUTO, weight_layout=MOE_WEIGHTS_ROW_MAJOR,
+             forward_form=MOE_FORWARD_AUTO):
+        return cls(int(T_max), int(E), int(k), int(H), int(I), int(capacity), int(path), int(weight_layout),
+                   int(forward_form))
 
     @property
     def cap(self) -> int:
@@ -73,7 +79,8 @@ class Problem(ctypes.Structure):
 
     def __repr__(self):
         return (f"Problem(T_max={self.T_max}, E={self.E}, k={self.k}, H={self.H}, I={self.I}, "
-                f"capacity={self.capacity}, path={self.path}, weight_layout={self.weight_layout})")
+                f"capacity={self.capacity}, path={self.path}, weight_layout={self.weight_layout}, "
+                f"forward_form={self.forward_form})")
 
 
 class Profile(ctypes.Structure):
@@ -81,10 +88,11 @@ class Profile(ctypes.Structure):
 
     _fields_ = [("path", ctypes.c_int32), ("tile_rows", ctypes.c_int32), ("down_split_k", ctypes.c_int32),
                 ("pdl", ctypes.c_int32), ("fused_gather", ctypes.c_int32), ("cta_pair", ctypes.c_int32),
-                ("fused_mlp", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("fused_mlp", ctypes.c_int32), ("megakernel", ctypes.c_int32),
+                ("kernel_launches", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
-        return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 _lib = None

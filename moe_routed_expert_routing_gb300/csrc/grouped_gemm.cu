@@ -509,10 +509,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 // their own pipeline, and the grid is one CTA per SM, all resident once the
 // (independent) previous kernel leaves. The GPU-wide tail between the two
 // GEMMs disappears: an SM moves on to down units of finished experts while
-// others still stream gate-up weights. ready[] is zeroed before the launch.
+// others still stream gate-up weights. ready[] is zero when the kernel starts
+// and again when it ends: the last CTA to leave clears it.
 // A stage holds 32 KB of weights either way: the gate and up tiles of one K
 // block, or two K blocks of a down tile (with two token-tile slots), so the
 // down units keep as many weight bytes in flight as the gate-up units.
+//
+// Whole-forward form (kMega): the same kernel is all of moe_forward. Every
+// CTA first runs the local dispatch of the call's few routed slots itself
+// (histogram, scan, stable scatter into shared memory; CTA 0 also writes
+// expert_offsets and perm for the caller), so no other kernel precedes the
+// GEMMs. Down units publish their y rows on a GPU-wide count; when it is
+// full every CTA combines its share of tokens x 1024 columns. The last CTA
+// to leave returns every counter to zero (FlashInfer moe_ep page, launch-path
+// notes: workspaces are allocated zeroed and the kernel cleans its
+// counters and flags at its tail), also after a timed-out wait, so repeated
+// calls need no memset. The split down GEMM writes its two K halves to two
+// fp32 buffers that the combine adds (a + b: the same value the two-atomic
+// form produces), so y needs no zeroing either.
 template <int kTileRows, int kStages>
 struct FusedCfg {
     static constexpr int kActSlot = kTileRows * 128;          // one K block of the token tile
@@ -529,16 +543,189 @@ struct FusedCfg {
 struct FusedArgs {
     GemmArgs up;       // gate-up: act = x (gathered), out = h, K = H, n_out = I
     GemmArgs down;     // down: act = h, out = y, K = I, n_out = H
-    int32_t *ready;    // [E] finished gate-up units per expert, zero at launch
+    int32_t *ready;    // [E] finished gate-up units per expert, zero at launch and at exit
+    int32_t *exits;    // CTAs at the tail, zero at launch and at exit
+    // whole-forward form only
+    const int32_t *ids;            // [T_max, k] routed expert of each slot, -1 = dropped
+    const float *topk_w;           // [T_max, k]
+    const int32_t *d_num_tokens;   // device T, or null for T_max
+    int T_max;
+    int slots_max;                 // T_max * k: size of the shared-memory perm / inv tables
+    int32_t *expert_offsets_out;   // [E + 1] for the caller
+    int32_t *perm_out;             // [cap] for the caller
+    __nv_bfloat16 *out;            // [T_max, H]
+    int32_t *done;                 // epilogue warps that finished a down unit, zero at launch and at exit
 };
 
-template <int kTileRows, int kStages, int kSplitDown>
+// Local dispatch of all routed slots inside one CTA (every CTA of the
+// whole-forward kernel runs it on the same input and gets the same tables):
+// s_off[E+1] = exclusive prefix of the per-expert slot counts, s_perm[row] =
+// slot in ascending slot order inside each expert (stable scatter), s_inv[slot]
+// = row or -1. s_cur[E] is scratch. The ids of all T_max tokens are fetched
+// together with T (those past T are never used), so the prologue pays one
+// global round trip. Returns T.
+__device__ int cta_dispatch(const FusedArgs &fa, int E, int *s_off, int *s_cur, int *s_perm, int *s_inv)
+{
+    static_assert(4 * kThreads >= kMaxExperts, "the scan covers four experts per thread");
+    __shared__ int s_warp_sum[kThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k = fa.up.k;
+    int T = fa.d_num_tokens ? *fa.d_num_tokens : fa.T_max;
+    for (int s = tid; s < fa.slots_max; s += kThreads)
+        s_inv[s] = __ldg(fa.ids + s);                  // ids staged in s_inv, replaced by rows below
+    for (int e = tid; e < E; e += kThreads)
+        s_cur[e] = 0;
+    T = T < 0 ? 0 : (T > fa.T_max ? fa.T_max : T);
+    const int R = T * k;
+    __syncthreads();
+    bool bad = false;
+    for (int s = tid; s < R; s += kThreads) {
+        const int e = s_inv[s];
+        if (e >= 0 && e < E)
+            atomicAdd(&s_cur[e], 1);
+        else if (e != -1)
+            bad = true;
+    }
+    if (bad && blockIdx.x == 0)
+        atomicOr(fa.up.err, MOE_DEVERR_BAD_EXPERT_ID);
+    __syncthreads();
+    // exclusive scan over experts, four consecutive experts per thread (E <= 1024)
+    int c[4], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = 4 * tid + i;
+        c[i] = e < E ? s_cur[e] : 0;
+        sum += c[i];
+    }
+    int v = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, v, o);
+        if (lane >= o)
+            v += n;
+    }
+    if (lane == 31)
+        s_warp_sum[warp] = v;
+    __syncthreads();
+    int before = v - sum;
+    for (int w = 0; w < warp; ++w)
+        before += s_warp_sum[w];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = 4 * tid + i;
+        if (e < E) {
+            s_off[e] = before;
+            s_cur[e] = before;
+        }
+        before += c[i];
+    }
+    if (tid == kThreads - 1)
+        s_off[E] = before;
+    __syncthreads();
+    if (warp == 0) {
+        // 32 slots at a time in ascending order: a slot's row is its expert's
+        // cursor plus the same-expert slots on lower lanes
+        const unsigned lt = (1u << lane) - 1u;
+        for (int base = 0; base < R; base += 32) {
+            const int s = base + lane;
+            const int e = s < R ? s_inv[s] : -1;
+            const bool valid = e >= 0 && e < E;
+            const unsigned peers = __match_any_sync(kFull, valid ? e : -1 - lane);
+            const int rank = __popc(peers & lt);
+            if (valid) {
+                const int row = s_cur[e] + rank;
+                s_perm[row] = s;
+                s_inv[s] = row;
+            } else if (s < R) {
+                s_inv[s] = -1;
+            }
+            __syncwarp();
+            if (valid && rank == 0)
+                s_cur[e] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int i = tid; i <= E; i += kThreads)
+            fa.expert_offsets_out[i] = s_off[i];
+        for (int r = tid; r < s_off[E]; r += kThreads)
+            fa.perm_out[r] = s_perm[r];
+    }
+    return T;
+}
+
+// This CTA's share of the combine: work items of one token x 1024 columns,
+// out[t, m] = bf16( sum_j w[t, j] * y[inv[t*k + j], m] ), fp32, j ascending,
+// no fused multiply-add (the arithmetic of combine_kernel). y was written by
+// other CTAs during this launch: read through L2 (ld.global.cg), never the
+// read-only path. With a split down GEMM the row is y0 + y1.
+template <int kSplitDown>
+__device__ void cta_combine(const FusedArgs &fa, const int *s_inv, int T)
+{
+    const int k = fa.up.k;
+    const int H = fa.down.n_out;
+    const int vec = H / 4;
+    const int groups = (vec + kThreads - 1) / kThreads;
+    const float4 *y0 = static_cast<const float4 *>(fa.down.out);
+    const float4 *y1 = y0 + static_cast<size_t>(fa.down.cap) * vec;
+    const long long items = static_cast<long long>(T) * groups;
+    for (long long item = blockIdx.x; item < items; item += gridDim.x) {
+        const int t = static_cast<int>(item / groups);
+        const int c = static_cast<int>(item % groups) * kThreads + threadIdx.x;
+        if (c >= vec)
+            continue;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j0 = 0; j0 < k; j0 += 4) {
+            float4 a[4];
+            int row[4];
+            float wj[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                row[q] = (j0 + q < k) ? s_inv[t * k + j0 + q] : -1;
+                wj[q] = (j0 + q < k) ? __ldg(fa.topk_w + static_cast<size_t>(t) * k + j0 + q) : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (row[q] >= 0) {
+                    const size_t i = static_cast<size_t>(row[q]) * vec + c;
+                    a[q] = __ldcg(y0 + i);
+                    if (kSplitDown == 2) {
+                        const float4 b = __ldcg(y1 + i);
+                        a[q].x = __fadd_rn(a[q].x, b.x);
+                        a[q].y = __fadd_rn(a[q].y, b.y);
+                        a[q].z = __fadd_rn(a[q].z, b.z);
+                        a[q].w = __fadd_rn(a[q].w, b.w);
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (row[q] < 0)
+                    continue;
+                acc[0] = __fadd_rn(acc[0], __fmul_rn(wj[q], a[q].x));
+                acc[1] = __fadd_rn(acc[1], __fmul_rn(wj[q], a[q].y));
+                acc[2] = __fadd_rn(acc[2], __fmul_rn(wj[q], a[q].z));
+                acc[3] = __fadd_rn(acc[3], __fmul_rn(wj[q], a[q].w));
+            }
+        }
+        uint2 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        reinterpret_cast<uint2 *>(fa.out)[static_cast<size_t>(t) * vec + c] = o;
+    }
+}
+
+template <int kTileRows, int kStages, int kSplitDown, bool kMega>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w13,
                        const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w2,
                        const FusedArgs fa)
 {
     using C = FusedCfg<kTileRows, kStages>;
+    // the whole-forward form keeps its expert tables (sized by E and T_max * k)
+    // in dynamic shared memory after the stages
+    constexpr int kStaticTable = kMega ? 1 : kMaxExperts + 1;
     __shared__ __align__(16) int s_rows[kTileRows];
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
@@ -548,8 +735,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
-    __shared__ int s_off[kMaxExperts + 1];
-    __shared__ int s_tp[kMaxExperts + 1];
+    __shared__ int s_T;
+    __shared__ int s_last;
+    __shared__ int s_off_static[kStaticTable];
+    __shared__ int s_tp_static[kStaticTable];
 
     const GemmArgs &A1 = fa.up;
     const GemmArgs &A2 = fa.down;
@@ -557,6 +746,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int E = A1.E;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int *const tables = reinterpret_cast<int *>(smem + kStages * C::kStageBytes);
+    int *const s_off = kMega ? tables : s_off_static;
+    int *const s_tp = kMega ? tables + (E + 1) : s_tp_static;
+    int *const s_perm = tables + 2 * (E + 1);
+    int *const s_inv = s_perm + fa.slots_max;
     volatile int *abort_flag = &s_abort;
 
     if (threadIdx.x == 0) {
@@ -583,8 +777,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     pdl_wait();
-    for (int i = threadIdx.x; i <= E; i += kThreads)
-        s_off[i] = A1.expert_offsets[i];
+    if (kMega) {
+        const int T = cta_dispatch(fa, E, s_off, s_tp, s_perm, s_inv);
+        if (threadIdx.x == 0)
+            s_T = T;
+    } else {
+        for (int i = threadIdx.x; i <= E; i += kThreads)
+            s_off[i] = A1.expert_offsets[i];
+    }
     __syncthreads();
     if (warp == 3)
         build_tile_prefix(s_off, s_tp, E, kTileRows, lane);
@@ -617,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int steps = up ? kb1 : (kb2 + 1) / 2;   // down: two K blocks per stage
             if (up) {
                 for (int i = lane; i < kTileRows; i += 32)
-                    s_rows[i] = i < t.rows ? __ldg(A1.perm + t.row0 + i) / A1.k : 0;
+                    s_rows[i] = i < t.rows ? (kMega ? s_perm[t.row0 + i] : __ldg(A1.perm + t.row0 + i)) / A1.k : 0;
                 __syncwarp();
             }
             if (lane == 0) {
@@ -764,6 +964,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t t_row = tmem_base + buf * C::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
             const int col = t.n0 + q * 32 + lane;
+            float *const y_out = static_cast<float *>(A2.out) +
+                                 ((kMega && !up) ? static_cast<size_t>(v % kSplitDown) * A2.cap * A2.n_out : 0);
 #pragma unroll 1
             for (int c = 0; c < kTileRows; c += 16) {
                 uint32_t g[16], w[16];
@@ -780,8 +982,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<__nv_bfloat16 *>(A1.out)[static_cast<size_t>(row) * A1.n_out + col] =
                                 __float2bfloat16_rn(silu_mul(__uint_as_float(g[i]), __uint_as_float(w[i])));
                         } else {
-                            float *y = static_cast<float *>(A2.out) + static_cast<size_t>(row) * A2.n_out + col;
-                            if (kSplitDown == 1)
+                            float *y = y_out + static_cast<size_t>(row) * A2.n_out + col;
+                            if (kSplitDown == 1 || kMega)
                                 *y = __uint_as_float(g[i]);
                             else  // two K halves into a zeroed output: exact and order-free
                                 atomicAdd(y, __uint_as_float(g[i]));
@@ -791,24 +993,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_tempty[buf]));
-            if (up) {
-                // publish this warp's h rows: every storing lane fences, then one
-                // lane releases the count (4 warps per unit; no cross-warp wait)
+            if (up || kMega) {
+                // publish this warp's h (or y) rows: every storing lane fences,
+                // then one lane releases the count (4 warps per unit; no
+                // cross-warp wait)
                 __threadfence();
                 __syncwarp();
                 if (lane == 0)
-                    red_release_gpu_add(fa.ready + t.e, 1);
+                    red_release_gpu_add(up ? fa.ready + t.e : fa.done, 1);
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    pdl_trigger();
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
     }
+    if (kMega) {
+        // combine once every down unit of the call has published its rows
+        const int need = 4 * s_tp[E] * NT2 * kSplitDown;
+        if (threadIdx.x == 0 && !s_abort) {
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_gpu(fa.done) < need) {
+                if (global_timer_ns() - t0 > A1.wait_limit_ns) {
+                    s_abort = 1;
+                    break;
+                }
+            }
+        }
+        __syncthreads();
+        if (!s_abort)
+            cta_combine<kSplitDown>(fa, s_inv, s_T);
+        __syncthreads();
+    }
+    // tail clean-up: the last CTA out (every other CTA has passed all its
+    // waits on the counters) returns them to zero for the next launch
+    if (threadIdx.x == 0)
+        s_last = atom_add_acq_rel_gpu(fa.exits, 1) == static_cast<int>(gridDim.x) - 1;
+    __syncthreads();
+    if (s_last) {
+        for (int e = threadIdx.x; e < E; e += kThreads)
+            fa.ready[e] = 0;
+        if (threadIdx.x == 0) {
+            if (kMega)
+                *fa.done = 0;
+            *fa.exits = 0;
+        }
+    }
+    pdl_trigger();
     if (threadIdx.x == 0 && s_abort)
         atomicOr(A1.err, MOE_DEVERR_WAIT_TIMEOUT);
 }
@@ -1193,22 +1427,59 @@ GemmArgs make_args(const GemmProblem &p)
     return a;
 }
 
-template <int kTileRows, int kStages, int kSplitDown>
-cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *ready, int num_sms,
-                      cudaStream_t stream)
+// Shared memory the whole-forward form needs for its expert tables:
+// offsets and tile prefix [E + 1] each, perm and inv [T_max * k] each.
+long long mega_table_bytes(int E, long long slots) { return 4LL * (2LL * (E + 1) + 2LL * slots); }
+
+// Per-block shared memory the device grants (opt-in) minus the static shared
+// memory of the whole-forward kernel and its stages: what is left for the
+// tables. Cached per device; -1 if a query fails.
+template <int kTileRows, int kStages>
+long long mega_table_budget()
+{
+    static int cached_dev = -1;
+    static long long cached = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return -1;
+    if (dev != cached_dev) {
+        int optin = 0;
+        cudaFuncAttributes fa1 = {}, fa2 = {};
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa1, fused_small_kernel<kTileRows, kStages, 1, true>) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa2, fused_small_kernel<kTileRows, kStages, 2, true>) != cudaSuccess)
+            return -1;
+        const size_t st = fa1.sharedSizeBytes > fa2.sharedSizeBytes ? fa1.sharedSizeBytes : fa2.sharedSizeBytes;
+        cached = static_cast<long long>(optin) - static_cast<long long>(st) - FusedCfg<kTileRows, kStages>::kDynSmem;
+        cached_dev = dev;
+    }
+    return cached;
+}
+
+template <int kTileRows, int kStages, int kSplitDown, bool kMega>
+cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *ready, int32_t *counters,
+                      int num_sms, cudaStream_t stream, const MegaParams *mega)
 {
     using C = FusedCfg<kTileRows, kStages>;
-    auto kern = fused_small_kernel<kTileRows, kStages, kSplitDown>;
+    auto kern = fused_small_kernel<kTileRows, kStages, kSplitDown, kMega>;
+    const long long slots = mega ? static_cast<long long>(mega->T_max) * up.k : 0;
+    const long long tables = kMega ? mega_table_bytes(up.E, slots) : 0;
+    if (kMega && tables > mega_table_budget<kTileRows, kStages>())
+        return cudaErrorInvalidValue;
+    const int dyn_smem = C::kDynSmem + static_cast<int>(tables);
     static int attr_done_for_device = -1;
+    static int attr_bytes = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (attr_done_for_device != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
+    if (attr_done_for_device != dev || attr_bytes < dyn_smem) {
+        const int want = kMega ? C::kDynSmem + static_cast<int>(mega_table_budget<kTileRows, kStages>()) : C::kDynSmem;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
         if (e != cudaSuccess)
             return e;
         attr_done_for_device = dev;
+        attr_bytes = want;
     }
     CUtensorMap tm_x, tm_w13, tm_h, tm_w2;
     if (!make_map(&tm_x, up.act, static_cast<uint64_t>(up.act_rows), static_cast<uint64_t>(up.K), 1) ||
@@ -1216,15 +1487,27 @@ cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *r
         !make_map(&tm_h, down.act, static_cast<uint64_t>(down.cap), static_cast<uint64_t>(down.K), kTileRows) ||
         !make_weight_map(&tm_w2, down))
         return cudaErrorInvalidValue;
-    FusedArgs fa;
+    FusedArgs fa = {};
     fa.up = make_args(up);
     fa.down = make_args(down);
     fa.ready = ready;
+    fa.exits = counters + 1;
+    if (kMega) {
+        fa.ids = mega->ids;
+        fa.topk_w = mega->topk_w;
+        fa.d_num_tokens = mega->d_num_tokens;
+        fa.T_max = mega->T_max;
+        fa.slots_max = static_cast<int>(slots);
+        fa.expert_offsets_out = mega->expert_offsets_out;
+        fa.perm_out = mega->perm_out;
+        fa.out = static_cast<__nv_bfloat16 *>(mega->out);
+        fa.done = counters;
+    }
     // one CTA per SM: every CTA must be resident for the down units' waits
     const long long tiles = (static_cast<long long>(up.cap) + kTileRows - 1) / kTileRows + up.E;
     const long long max_units = tiles * (up.n_out / 128 + (down.n_out / 128) * kSplitDown);
     const int grid = static_cast<int>(max_units < num_sms ? (max_units < 1 ? 1 : max_units) : num_sms);
-    return launch_k(kern, dim3(grid), dim3(kThreads), C::kDynSmem, stream, up.pdl, tm_x, tm_w13, tm_h, tm_w2, fa);
+    return launch_k(kern, dim3(grid), dim3(kThreads), dyn_smem, stream, up.pdl, tm_x, tm_w13, tm_h, tm_w2, fa);
 }
 
 }  // namespace
@@ -1264,18 +1547,31 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t 
     }
 }
 
-cudaError_t launch_fused_small(const GemmProblem &up, const GemmProblem &down, int32_t *ready, int num_sms,
-                               cudaStream_t stream)
+cudaError_t launch_fused_small(const GemmProblem &up, const GemmProblem &down, int32_t *ready, int32_t *counters,
+                               int num_sms, cudaStream_t stream, const MegaParams *mega)
 {
-    if (!up.small_m || !down.small_m || !up.gated || down.gated || !up.gather || !up.perm || up.tile_rows != down.tile_rows ||
-        !ready || (down.split_k != 1 && down.split_k != 2))
+    if (!up.small_m || !down.small_m || !up.gated || down.gated || !up.gather || up.tile_rows != down.tile_rows ||
+        !ready || !counters || (down.split_k != 1 && down.split_k != 2))
+        return cudaErrorInvalidValue;
+    if (mega ? (!mega->ids || !mega->topk_w || !mega->expert_offsets_out || !mega->perm_out || !mega->out ||
+                mega->T_max < 1)
+             : !up.perm)
         return cudaErrorInvalidValue;
     // built for decode-size batches only (16-row token tiles): with 32-row
     // tiles (the Zipf small batch) two launches measured 2% faster
     if (up.tile_rows != 16)
         return cudaErrorInvalidValue;
-    return down.split_k == 2 ? run_fused<16, 6, 2>(up, down, ready, num_sms, stream)
-                             : run_fused<16, 6, 1>(up, down, ready, num_sms, stream);
+    if (mega)
+        return down.split_k == 2 ? run_fused<16, 6, 2, true>(up, down, ready, counters, num_sms, stream, mega)
+                                 : run_fused<16, 6, 1, true>(up, down, ready, counters, num_sms, stream, mega);
+    return down.split_k == 2 ? run_fused<16, 6, 2, false>(up, down, ready, counters, num_sms, stream, nullptr)
+                             : run_fused<16, 6, 1, false>(up, down, ready, counters, num_sms, stream, nullptr);
+}
+
+bool fused_mega_fits(int E, long long slots)
+{
+    const long long budget = mega_table_budget<16, 6>();
+    return budget >= 0 && mega_table_bytes(E, slots) <= budget;
 }
 
 }  // namespace moe

@@ -18,10 +18,29 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-    size_t err, block_counts, block_base, h, x_sorted, y_sorted, inv, ready, total;
+    size_t err, ready, counters, block_counts, block_base, h, x_sorted, y_sorted, inv, total;
 };
 
 int capacity_of(const moe_problem_t &p) { return p.capacity ? p.capacity : p.T_max * p.k; }
+
+// Workspace header, at fixed offsets so that moe_clear_device_error can clear
+// it without the problem: the error word, then the fused decode kernel's
+// per-expert readiness counts and its two GPU-wide counters. The kernels leave
+// the counters at zero after every launch.
+constexpr size_t kReadyOffset = kAlign;
+constexpr size_t kCountersOffset = kReadyOffset + sizeof(int32_t) * kMaxExperts;
+constexpr size_t kHeaderBytes = (kCountersOffset + 2 * sizeof(int32_t) + kAlign - 1) / kAlign * kAlign;
+
+void resolve(const moe_problem_t &p, int *path, int *tile_rows);
+
+// A split down GEMM is possible (the SM count decides): the fused kernel then
+// needs two fp32 y buffers.
+bool split_possible(const moe_problem_t &p)
+{
+    int path = 0, tile_rows = 0;
+    resolve(p, &path, &tile_rows);
+    return path == MOE_PATH_SMALL_M && tile_rows == 16 && (p.I / 64) % 2 == 0;
+}
 
 Layout layout_of(const moe_problem_t &p)
 {
@@ -29,9 +48,10 @@ Layout layout_of(const moe_problem_t &p)
     const size_t R = static_cast<size_t>(p.T_max) * p.k;
     const size_t n_blocks = (R + kDispatchSlotsPerBlock - 1) / kDispatchSlotsPerBlock;
     Layout L;
-    size_t o = 0;
-    L.err = o;
-    o += kAlign;
+    L.err = 0;
+    L.ready = kReadyOffset;
+    L.counters = kCountersOffset;
+    size_t o = kHeaderBytes;
     L.block_counts = o;
     o = align_up(o + sizeof(int32_t) * n_blocks * p.E);
     L.block_base = o;
@@ -41,11 +61,9 @@ Layout layout_of(const moe_problem_t &p)
     L.x_sorted = o;
     o = align_up(o + 2 * cap * p.H);
     L.y_sorted = o;
-    o = align_up(o + 4 * cap * p.H);
+    o = align_up(o + 4 * cap * p.H * (split_possible(p) ? 2 : 1));
     L.inv = o;
     o = align_up(o + sizeof(int32_t) * R);
-    L.ready = o;   // per-expert count of finished gate-up units (fused M-small kernel)
-    o = align_up(o + sizeof(int32_t) * p.E);
     L.total = o;
     return L;
 }
@@ -60,6 +78,8 @@ moe_status_t check_problem(const moe_problem_t *p)
     if (p->path < MOE_PATH_AUTO || p->path > MOE_PATH_TILED_1CTA)
         return MOE_ERR_SHAPE;
     if (p->weight_layout != MOE_WEIGHTS_ROW_MAJOR && p->weight_layout != MOE_WEIGHTS_PACKED)
+        return MOE_ERR_SHAPE;
+    if (p->forward_form < MOE_FORWARD_AUTO || p->forward_form > MOE_FORWARD_ONE_KERNEL)
         return MOE_ERR_SHAPE;
     const long long R = static_cast<long long>(p->T_max) * p->k;
     if (R > (1LL << 28))
@@ -160,7 +180,8 @@ bool down_split_k(const moe_problem_t &p, int path, int tile_rows, int sms)
 moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, const int32_t *expert_offsets,
                                     const void *W13, const void *W2, float *y_sorted, void *ws, cudaStream_t s,
                                     void *const *stage_events = nullptr, bool y_zeroed = false,
-                                    const int32_t *gather_perm = nullptr, bool fused = false)
+                                    const int32_t *gather_perm = nullptr, bool fused = false,
+                                    const MegaParams *mega = nullptr)
 {
     const Layout L = layout_of(p);
     int path = 0, tile_rows = 0;
@@ -169,7 +190,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
     if (sms <= 0)
         return MOE_ERR_CUDA;
     const bool split = down_split_k(p, path, tile_rows, sms);
-    if (split && !y_zeroed &&
+    if (split && !y_zeroed && !mega &&
         cudaMemsetAsync(y_sorted, 0, sizeof(float) * static_cast<size_t>(capacity_of(p)) * p.H, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     GemmProblem g;
@@ -185,10 +206,10 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
     g.pdl = path == MOE_PATH_SMALL_M;
     // gate-up with the fused SiLU(gate) * up epilogue: x_sorted[cap, H] x W13[E, 2I, H] -> h[cap, I]
     g.act = act;
-    g.gather = gather_perm != nullptr;
+    g.gather = gather_perm != nullptr || mega != nullptr;
     g.perm = gather_perm;
     g.k = p.k;
-    g.act_rows = gather_perm ? p.T_max : g.cap;
+    g.act_rows = g.gather ? p.T_max : g.cap;
     g.w = W13;
     g.out = at<void>(ws, L.h);
     g.K = p.H;
@@ -221,10 +242,53 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
     if (!fused)
         return cuda_status(launch_grouped_gemm(g, sms, s));
     // both GEMMs in one persistent launch; its stage marks share one instant
-    st = cuda_status(launch_fused_small(up, g, at<int32_t>(ws, L.ready), sms, s));
+    st = cuda_status(launch_fused_small(up, g, at<int32_t>(ws, L.ready), at<int32_t>(ws, L.counters), sms, s, mega));
     if (st != MOE_OK)
         return st;
     return record_stage(stage_events, 3, s);
+}
+
+// moe_forward can run as one kernel: decode-size batches whose dispatch
+// tables fit in the fused kernel's shared memory.
+bool megakernel_possible(const moe_problem_t &p)
+{
+    int path = 0, tile_rows = 0;
+    resolve(p, &path, &tile_rows);
+    return path == MOE_PATH_SMALL_M && tile_rows == 16 &&
+           fused_mega_fits(p.E, static_cast<long long>(p.T_max) * p.k);
+}
+
+// moe_forward runs as one kernel: asked for, or (AUTO) where the down GEMM
+// splits K, the one case where one kernel measured faster than three chained
+// by programmatic dependent launch.
+bool use_megakernel(const moe_problem_t &p)
+{
+    if (p.forward_form == MOE_FORWARD_SEPARATE || !megakernel_possible(p))
+        return false;
+    if (p.forward_form == MOE_FORWARD_ONE_KERNEL)
+        return true;
+    int path = 0, tile_rows = 0;
+    resolve(p, &path, &tile_rows);
+    return down_split_k(p, path, tile_rows, device_sm_count());
+}
+
+moe_status_t check_form(const moe_problem_t &p)
+{
+    return (p.forward_form == MOE_FORWARD_ONE_KERNEL && !megakernel_possible(p)) ? MOE_ERR_UNSUPPORTED : MOE_OK;
+}
+
+// Kernel launches one moe_forward call enqueues (memsets not counted).
+int forward_launches(const moe_problem_t &p)
+{
+    int path = 0, tile_rows = 0;
+    resolve(p, &path, &tile_rows);
+    if (use_megakernel(p))
+        return 1;
+    const long long R = static_cast<long long>(p.T_max) * p.k;
+    int n = R <= kDispatchSlotsPerBlock ? 1 : 3;            // dispatch
+    n += path == MOE_PATH_SMALL_M ? 0 : 1;                  // row gather (fused into the M-small GEMM)
+    n += (path == MOE_PATH_SMALL_M && tile_rows == 16) ? 1 : 2;
+    return n + 1;                                           // combine
 }
 
 }  // namespace
@@ -298,6 +362,8 @@ moe_status_t moe_resolve_profile(const moe_problem_t *problem, moe_profile_t *pr
     const int sms = device_sm_count();
     if (sms <= 0)
         return MOE_ERR_CUDA;
+    if (check_form(*problem) != MOE_OK)
+        return MOE_ERR_UNSUPPORTED;
     int path = 0, tile_rows = 0;
     resolve(*problem, &path, &tile_rows);
     std::memset(profile, 0, sizeof *profile);
@@ -308,6 +374,8 @@ moe_status_t moe_resolve_profile(const moe_problem_t *problem, moe_profile_t *pr
     profile->fused_gather = path == MOE_PATH_SMALL_M ? 1 : 0;
     profile->cta_pair = path == MOE_PATH_TILED ? 1 : 0;
     profile->fused_mlp = (path == MOE_PATH_SMALL_M && tile_rows == 16) ? 1 : 0;
+    profile->megakernel = use_megakernel(*problem) ? 1 : 0;
+    profile->kernel_launches = forward_launches(*problem);
     return MOE_OK;
 }
 
@@ -394,6 +462,8 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
         return st;
     if ((st = check_device()) != MOE_OK)
         return st;
+    if ((st = check_form(p)) != MOE_OK)
+        return st;
     const Layout L = layout_of(p);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int sms = device_sm_count();
@@ -403,17 +473,36 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
     auto mark = [&](int i) { return record_stage(stage_events, i, s); };
     int path = 0, tile_rows = 0;
     resolve(p, &path, &tile_rows);
+    // decode-size batches (M-small, 16-row token tiles) whose dispatch tables
+    // fit in shared memory: the whole call is one persistent kernel (local
+    // dispatch in every CTA, both GEMMs, combine); its stage marks all fall
+    // after it.
+    if (use_megakernel(p)) {
+        MegaParams mp;
+        mp.ids = topk_ids;
+        mp.topk_w = topk_weights;
+        mp.d_num_tokens = d_num_tokens;
+        mp.T_max = p.T_max;
+        mp.expert_offsets_out = expert_offsets;
+        mp.perm_out = perm;
+        mp.out = out;
+        if ((st = mark(0)) != MOE_OK)
+            return st;
+        st = enqueue_expert_compute(p, x, nullptr, W13, W2, y_sorted, ws, s, nullptr, true, nullptr, true, &mp);
+        for (int i = 1; st == MOE_OK && i < 6; ++i)
+            st = mark(i);
+        return st;
+    }
     const bool split = down_split_k(p, path, tile_rows, sms);
     if (split && cudaMemsetAsync(y_sorted, 0, sizeof(float) * static_cast<size_t>(capacity_of(p)) * p.H, s) !=
                      cudaSuccess)
         return MOE_ERR_CUDA;
     // decode-size batches (M-small, 16-row token tiles): both GEMMs run as one
-    // persistent kernel whose down units wait on per-expert counts; those start
-    // from zero every call. Measured in one process against two launches:
-    // -1.3% per decode step; +2% on 32-row tiles, which keep two launches.
+    // persistent kernel whose down units wait on per-expert counts (zero at
+    // every launch: the kernel clears them at its tail). Measured in one
+    // process against two launches: -1.3% per decode step; +2% on 32-row
+    // tiles, which keep two launches.
     const bool fused_mlp = path == MOE_PATH_SMALL_M && tile_rows == 16;
-    if (fused_mlp && cudaMemsetAsync(at<int32_t>(ws, L.ready), 0, sizeof(int32_t) * p.E, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
     if ((st = mark(0)) != MOE_OK)
         return st;
     st = cuda_status(launch_dispatch(topk_ids, d_num_tokens, p.T_max, p.k, p.E, at<int32_t>(ws, L.block_counts),
@@ -499,8 +588,10 @@ moe_status_t moe_clear_device_error(void *ws, void *stream)
 {
     if (!ws)
         return MOE_ERR_NULL;
-    return cudaMemsetAsync(ws, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK
-                                                                                                    : MOE_ERR_CUDA;
+    // the error word and the fused decode kernel's counters: afterwards a
+    // workspace of any former contents is ready for moe_forward
+    return cudaMemsetAsync(ws, 0, kHeaderBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK
+                                                                                                 : MOE_ERR_CUDA;
 }
 
 const char *moe_status_string(moe_status_t status)

@@ -96,10 +96,31 @@ struct GemmProblem {
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);
 
+// The rest of moe_forward for the whole-forward form of the fused kernel:
+// the dispatch inputs and outputs and the combine's weights and output.
+struct MegaParams {
+    const int32_t *ids;            // [T_max, k]
+    const float *topk_w;           // [T_max, k]
+    const int32_t *d_num_tokens;   // nullable
+    int T_max;
+    int32_t *expert_offsets_out;   // [E + 1]
+    int32_t *perm_out;             // [cap]
+    void *out;                     // [T_max, H] bf16
+};
+
 // Both M-small GEMMs in one persistent launch (gate-up with gathered rows, then
-// down); ready[E] must be zero when the kernel starts.
-cudaError_t launch_fused_small(const GemmProblem &up, const GemmProblem &down, int32_t *ready, int num_sms,
-                               cudaStream_t stream);
+// down). ready[E] and counters[2] must be zero when the kernel starts; the
+// kernel leaves them at zero (the last CTA out clears them), so a workspace
+// that starts zeroed needs no clearing between calls. With `mega`, the launch
+// is the whole forward (dispatch, both GEMMs, combine); up.perm and the
+// expert_offsets of both problems are then not read, and a split down GEMM
+// writes its halves to down.out and down.out + cap * H (no zeroing needed).
+cudaError_t launch_fused_small(const GemmProblem &up, const GemmProblem &down, int32_t *ready, int32_t *counters,
+                               int num_sms, cudaStream_t stream, const MegaParams *mega = nullptr);
+
+// Whether the whole-forward kernel's shared-memory expert tables for E experts
+// and `slots` = T_max * k routed slots fit next to its pipeline on this device.
+bool fused_mega_fits(int E, long long slots);
 
 // number of SMs of the current device (cached)
 int device_sm_count();

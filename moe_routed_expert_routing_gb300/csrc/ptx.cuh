@@ -131,6 +131,14 @@ __device__ __forceinline__ void red_release_gpu_add(int32_t *p, int v)
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t *p, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Order this thread's earlier generic-proxy accesses (e.g. the acquire that
 // saw another CTA's stores) before its later async-proxy (TMA) reads of global memory.
 __device__ __forceinline__ void fence_proxy_async_global()

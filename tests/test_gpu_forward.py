@@ -149,25 +149,41 @@ def test_launch_profile_table(B):
     """The static profile follows from the shape alone (a = T_max*k/E rows per expert)."""
     P = B.Problem.make
     dec1 = B.moe_resolve_profile(P(1, 384, 6, 7168, 3072))
-    assert dec1 == dict(path=2, tile_rows=16, down_split_k=2, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1)
+    assert dec1 == dict(path=2, tile_rows=16, down_split_k=2, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1,
+                        megakernel=1, kernel_launches=1)
     dec8 = B.moe_resolve_profile(P(8, 384, 6, 7168, 3072))
-    assert dec8 == dict(path=2, tile_rows=16, down_split_k=1, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1)
+    assert dec8 == dict(path=2, tile_rows=16, down_split_k=1, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1,
+                        megakernel=0, kernel_launches=3)
+    assert B.moe_resolve_profile(P(8, 384, 6, 7168, 3072, forward_form=B.MOE_FORWARD_ONE_KERNEL))["megakernel"] == 1
+    assert B.moe_resolve_profile(P(1, 384, 6, 7168, 3072, forward_form=B.MOE_FORWARD_SEPARATE))["megakernel"] == 0
+    with pytest.raises(B.MoeError) as ei:      # not decode-size: one kernel is refused, not ignored
+        B.moe_resolve_profile(P(128, 256, 8, 7168, 2048, forward_form=B.MOE_FORWARD_ONE_KERNEL))
+    assert ei.value.status == 5
     small = B.moe_resolve_profile(P(128, 256, 8, 7168, 2048))
     assert small["path"] == 2 and small["tile_rows"] == 32 and small["down_split_k"] == 1 and small["fused_mlp"] == 0
+    assert small["megakernel"] == 0 and small["kernel_launches"] == 4    # dispatch, 2 GEMMs, combine
     prefill = B.moe_resolve_profile(P(2048, 384, 6, 7168, 3072))
-    assert prefill == dict(path=3, tile_rows=128, down_split_k=1, pdl=0, fused_gather=0, cta_pair=0, fused_mlp=0)
+    assert prefill == dict(path=3, tile_rows=128, down_split_k=1, pdl=0, fused_gather=0, cta_pair=0, fused_mlp=0,
+                           megakernel=0, kernel_launches=7)
     large = B.moe_resolve_profile(P(8192, 128, 8, 4096, 1536))
-    assert large == dict(path=1, tile_rows=128, down_split_k=1, pdl=0, fused_gather=0, cta_pair=1, fused_mlp=0)
+    assert large == dict(path=1, tile_rows=128, down_split_k=1, pdl=0, fused_gather=0, cta_pair=1, fused_mlp=0,
+                         megakernel=0, kernel_launches=7)
+    # 16-row tiles whose shared-memory dispatch tables do not fit: fused GEMMs, separate dispatch and combine
+    wide = B.moe_resolve_profile(P(256, 1024, 8, 512, 256))
+    assert wide["fused_mlp"] == 1 and wide["megakernel"] == 0 and wide["kernel_launches"] == 5   # 3 dispatch
 
 
-def test_fused_decode_kernel_graph_replay_token_counts(B):
+@pytest.mark.parametrize("form", [1, 2], ids=["separate", "one_kernel"])
+def test_fused_decode_kernel_graph_replay_token_counts(B, form):
     """Decode-size batches run both GEMMs as one persistent kernel with per-expert
-    readiness counts: captured once, replayed with T in {8, 3, 1, 0}, every
-    replay equals an eager call bit for bit and the oracle within tolerance."""
+    readiness counts (and, in the one-kernel form, dispatch and combine too):
+    captured once, replayed with T in {8, 3, 1, 0}, every replay equals an
+    eager call bit for bit and the oracle within tolerance."""
     wl = wlm.custom("fusedgraph", 8, 64, 4, 512, 256, seed=44)
     dw = DeviceWorkload(wl)
-    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, forward_form=form)
     assert B.moe_resolve_profile(p)["fused_mlp"] == 1
+    assert B.moe_resolve_profile(p)["megakernel"] == (form == 2)
     bufs = B.Buffers(p)
     d_T = torch.tensor([wl.T], dtype=torch.int32, device="cuda")
     forward(B, p, dw, bufs, d_T=d_T)
@@ -193,3 +209,92 @@ def test_fused_decode_kernel_graph_replay_token_counts(B):
         assert torch.equal(bufs.out[:T_dev].view(torch.int16), eager.out[:T_dev].view(torch.int16))
         ref_acc, _ = dw.oracle_out(np.arange(T_dev, dtype=np.int32))
         assert_within_tolerance(wlm.bf16_bits(bufs.out[:T_dev]), ref_acc, f"fused T={T_dev}")
+
+
+def _separate_entry_points(B, p, dw, d_T=None):
+    """dispatch -> expert compute -> combine through the three separate calls."""
+    bufs = B.Buffers(p)
+    B.moe_dispatch(p, dw.ids, bufs.expert_offsets, bufs.perm, bufs.inv, bufs.ws, x=dw.x, x_sorted=bufs.x_sorted,
+                   d_num_tokens=d_T)
+    B.moe_expert_compute(p, bufs.x_sorted, bufs.expert_offsets, dw.W13, dw.W2, bufs.y_sorted, bufs.ws)
+    bufs.out.fill_(3.0)
+    B.moe_combine(p, bufs.y_sorted, bufs.inv, dw.w, bufs.out, d_num_tokens=d_T)
+    torch.cuda.synchronize()
+    return bufs
+
+
+# (T, E, k, H, I): one token (split down GEMM), a decode batch (unsplit), a wide top-k (split)
+MEGA_SHAPES = [(1, 64, 4, 512, 256), (8, 64, 4, 4096, 256), (24, 256, 16, 256, 128)]
+
+
+@pytest.mark.parametrize("shape", MEGA_SHAPES, ids=["T1_split", "T8", "k16"])
+def test_megakernel_equals_separate_entry_points(B, shape):
+    """The one-kernel forward gives the same bits as dispatch + expert compute +
+    combine launched separately (same GEMM arithmetic, same combine order), and
+    the same expert_offsets and perm."""
+    wl = wlm.custom("mega", *shape, seed=sum(shape))
+    dw = DeviceWorkload(wl)
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, forward_form=B.MOE_FORWARD_ONE_KERNEL)
+    prof = B.moe_resolve_profile(p)
+    assert prof["megakernel"] == 1 and prof["kernel_launches"] == 1
+    got = forward(B, p, dw)
+    assert B.moe_last_device_error(got.ws) == 0
+    ref = _separate_entry_points(B, p, dw)
+    assert torch.equal(got.expert_offsets, ref.expert_offsets)
+    n = int(ref.expert_offsets[-1])
+    assert torch.equal(got.perm[:n], ref.perm[:n])
+    assert torch.equal(got.out.view(torch.int16), ref.out.view(torch.int16))
+    ref_acc, _ = dw.oracle_out()
+    assert_within_tolerance(wlm.bf16_bits(got.out), ref_acc, f"megakernel {shape}")
+
+
+def test_megakernel_tail_clears_its_counters(B):
+    """Workspace header after every call: error word, readiness counts and the
+    two GPU-wide counters all back at zero; repeated calls bit-identical. A
+    workspace of garbage is readied by moe_clear_device_error."""
+    wl = wlm.custom("megatail", 8, 128, 6, 512, 256, seed=61)
+    dw = DeviceWorkload(wl)
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, forward_form=B.MOE_FORWARD_ONE_KERNEL)
+    assert B.moe_resolve_profile(p)["megakernel"] == 1
+    bufs = B.Buffers(p)
+    header = 256 + 4 * (1024 + 2)
+    first = None
+    for _ in range(4):
+        forward(B, p, dw, bufs)
+        assert int(bufs.ws[:header].count_nonzero()) == 0
+        if first is None:
+            first = bufs.out.clone()
+        assert torch.equal(first.view(torch.int16), bufs.out.view(torch.int16))
+    bufs.ws.fill_(0x5A)
+    B.moe_clear_device_error(bufs.ws)
+    forward(B, p, dw, bufs)
+    assert B.moe_last_device_error(bufs.ws) == 0
+    assert torch.equal(first.view(torch.int16), bufs.out.view(torch.int16))
+    assert int(bufs.ws[:header].count_nonzero()) == 0
+
+
+def test_megakernel_dropped_invalid_and_repeated_slots(B):
+    """Degenerate routing inside the one-kernel forward: a repeated expert in
+    one token, dropped slots (-1), an out-of-range id (dropped and flagged),
+    and a device token count below T_max (rows >= T untouched)."""
+    wl = wlm.custom("megaedge", 12, 64, 4, 512, 256, seed=62)
+    dw = DeviceWorkload(wl)
+    ids_np, w_np = dw.ids_np.copy(), dw.w_np.copy()
+    ids_np[0] = [7, 7, 1, 2]
+    ids_np[1] = [-1, 3, -1, 4]
+    ids_np[2] = [5, 99, 6, 0]
+    ids = torch.from_numpy(ids_np).cuda()
+    w = torch.from_numpy(w_np).cuda()
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, forward_form=B.MOE_FORWARD_ONE_KERNEL)
+    assert B.moe_resolve_profile(p)["megakernel"] == 1
+    d_T = torch.tensor([10], dtype=torch.int32, device="cuda")
+    bufs = B.Buffers(p)
+    bufs.out.fill_(9.0)
+    forward(B, p, dw, bufs, d_T=d_T, ids=ids, w=w)
+    assert B.moe_last_device_error(bufs.ws) & B.MOE_DEVERR_BAD_EXPERT_ID
+    assert torch.all(bufs.out[10:] == 9.0)
+    valid = int(np.count_nonzero((ids_np[:10] >= 0) & (ids_np[:10] < wl.E)))
+    assert int(bufs.expert_offsets[-1]) == valid
+    tokens = np.arange(10, dtype=np.int32)
+    ref_acc, _ = dw.oracle_out(tokens, ids_np=ids_np, w_np=w_np)
+    assert_within_tolerance(wlm.bf16_bits(bufs.out[:10]), ref_acc, "megakernel degenerate routing")
