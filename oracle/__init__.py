@@ -16,7 +16,11 @@ computed and which passage each step follows is written at the top of
   follow-up (fused-gated epilogue): ``a = bf16(SiLU(x W1^T) * (x W3^T))``,
   ``y = a W2^T`` in fp32;
 * combine -- same page, Summary (routing weights kept outside expert compute):
-  ``out = bf16(sum_j w_j y_j)`` in fp32, j ascending.
+  ``out = bf16(sum_j w_j y_j)`` in fp32, j ascending;
+* MXFP8 weights -- FlashInfer moe_ep page (PR #3980), MXFP8 path with
+  prequantized weights, format 32 e4m3 x e8m0 (OCP MX v1.0): ``mx_quantize``
+  and the exact ``mx_dequantize``; the MXFP8 forward is the bf16 forward on
+  dequantized weights.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against values
 that do not come from the oracle itself (see that file's docstring).
@@ -41,11 +45,15 @@ __all__ = [
     "moe_tokens",
     "moe_forward_streamed",
     "bf16_bits_to_f32",
+    "e4m3_values",
+    "mx_quantize",
+    "mx_dequantize",
 ]
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _f32p = ctypes.POINTER(ctypes.c_float)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 
 
 def _c(a: np.ndarray, dtype) -> np.ndarray:
@@ -87,6 +95,12 @@ class Oracle:
         lib.oracle_moe_tokens.argtypes = [ctypes.c_int32] * 5 + [_u16p, _i32p, _f32p, _u16p, _u16p,
                                                                  ctypes.c_int32, _i32p, _f32p, _u16p]
         lib.oracle_moe_tokens.restype = ctypes.c_int32
+        lib.oracle_e4m3_values.argtypes = [_f32p]
+        lib.oracle_e4m3_values.restype = None
+        lib.oracle_mx_quantize.argtypes = [ctypes.c_int64, ctypes.c_int32, _u16p, _u8p, _u8p]
+        lib.oracle_mx_quantize.restype = None
+        lib.oracle_mx_dequantize.argtypes = [ctypes.c_int64, ctypes.c_int32, _u8p, _u8p, _u16p]
+        lib.oracle_mx_dequantize.restype = None
         self.lib = lib
         self.path = path
 
@@ -189,6 +203,38 @@ class Oracle:
                                              _p(out_acc, _f32p), _p(out, _u16p))
         return out_acc, out, int(bad)
 
+    def e4m3_values(self) -> np.ndarray:
+        """float32[256]: the value of every E4M3 code (NaN for 0x7F and 0xFF)."""
+        out = np.empty(256, dtype=np.float32)
+        self.lib.oracle_e4m3_values(_p(out, _f32p))
+        return out
+
+    def mx_quantize(self, w: np.ndarray):
+        """MXFP8 quantization along the last axis of bf16 bits ``w[..., K]``
+        (K a multiple of 32): returns ``(q[..., K] E4M3 codes, s[..., K/32]
+        E8M0 scale codes)``, both uint8."""
+        w = _c(w, np.uint16)
+        K = w.shape[-1]
+        assert K % 32 == 0
+        rows = w.size // K
+        q = np.empty(w.shape, dtype=np.uint8)
+        s = np.empty(w.shape[:-1] + (K // 32,), dtype=np.uint8)
+        if rows:
+            self.lib.oracle_mx_quantize(rows, K, _p(w, _u16p), _p(q, _u8p), _p(s, _u8p))
+        return q, s
+
+    def mx_dequantize(self, q: np.ndarray, s: np.ndarray) -> np.ndarray:
+        """bf16 bits of X * P for MXFP8 codes ``q[..., K]`` and scales ``s[..., K/32]``."""
+        q = _c(q, np.uint8)
+        s = _c(s, np.uint8)
+        K = q.shape[-1]
+        assert s.shape == q.shape[:-1] + (K // 32,)
+        rows = q.size // K
+        out = np.empty(q.shape, dtype=np.uint16)
+        if rows:
+            self.lib.oracle_mx_dequantize(rows, K, _p(q, _u8p), _p(s, _u8p), _p(out, _u16p))
+        return out
+
     def moe_forward_streamed(self, x, topk_ids, topk_weights, fetch_expert, E, tokens=None):
         """Same result as :meth:`moe_tokens`, with expert weights fetched one at a time.
 
@@ -256,3 +302,15 @@ def moe_tokens(x, topk_ids, topk_weights, W13, W2, tokens=None):
 
 def moe_forward_streamed(x, topk_ids, topk_weights, fetch_expert, E, tokens=None):
     return load().moe_forward_streamed(x, topk_ids, topk_weights, fetch_expert, E, tokens)
+
+
+def e4m3_values():
+    return load().e4m3_values()
+
+
+def mx_quantize(w):
+    return load().mx_quantize(w)
+
+
+def mx_dequantize(q, s):
+    return load().mx_dequantize(q, s)

@@ -33,6 +33,24 @@
  *     compute"): out_acc[t, m] = sum_{j ascending} w[t, j] * y_{t,j}[m] in
  *     fp32, then out[t, m] = bf16(out_acc[t, m]). Weights are used as given.
  *
+ *  4. MXFP8 weights -- the pages' MXFP8 path (FlashInfer moe_ep page, PR
+ *     #3980: MXFP8 mega MoE with prequantized weight packs; its quantized
+ *     combine wire spells the format out as 'mxfp8' = 32 e4m3 x e8m0). The
+ *     format is the OCP Microscaling (MX) v1.0 one: each block of 32
+ *     consecutive elements along K shares one E8M0 scale X = 2^e, each
+ *     element is an FP8 E4M3 value P, and the block stands for X * P. One
+ *     block is quantized the way the MX spec describes:
+ *       e = floor(log2(max |V|)) - 8      (8 = exponent of E4M3's largest
+ *                                          normal, 448 = 1.75 * 2^8),
+ *           clamped to E8M0's [-127, 127], stored as e + 127;
+ *       P = E4M3(V / X), round to nearest, ties to even; a magnitude above
+ *           448 becomes 448 (V / X of the block maximum lies in [256, 512)).
+ *     A block of zeros gets e = -127 and zero elements. E4M3 (OCP FP8):
+ *     sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0
+ *     holds the subnormals m * 2^-9; no infinities; S.1111.111 is NaN.
+ *     Dequantization X * P is exact in bf16 (3 mantissa bits fit in 7), so
+ *     the MXFP8 forward is the bf16 forward above on dequantized weights.
+ *
  * Parity pins (tests/test_oracle_pins.py): dispatch invariants and a brute
  * force restatement; bf16 rounding against an independent library cast; the
  * one-expert k=1 special case against a dense MLP built from library matmuls;
@@ -272,4 +290,99 @@ int32_t oracle_moe_tokens(int32_t T, int32_t E, int32_t k, int32_t H, int32_t I,
         free(scratch);
     }
     return bad;
+}
+
+/* ---- 4. MXFP8 weights (OCP MX v1.0: E4M3 elements, one E8M0 scale per 32) ---- */
+
+/* Value of an E4M3 code, from the format's fields. */
+static float e4m3_value(uint8_t c)
+{
+    int sign = (c >> 7) & 1, ex = (c >> 3) & 15, man = c & 7;
+    float mag;
+    if (ex == 15 && man == 7)
+        mag = NAN;
+    else if (ex == 0)
+        mag = ldexpf((float)man, -9);                   /* subnormal: m * 2^-9 */
+    else
+        mag = ldexpf(1.0f + (float)man / 8.0f, ex - 7);
+    return sign ? -mag : mag;
+}
+
+void oracle_e4m3_values(float *out)
+{
+    for (int c = 0; c < 256; ++c)
+        out[c] = e4m3_value((uint8_t)c);
+}
+
+/* Nearest E4M3 code to a finite v, ties to the even mantissa, magnitudes
+ * above 448 saturated to 448. The spacing of the codes around |v| is
+ * 2^(floor(log2|v|) - 3) among the normals and 2^-9 among the subnormals;
+ * |v| divided by that spacing is rounded to an integer (rintf rounds to
+ * nearest even), and a carry into the next binade is renormalised. */
+static uint8_t e4m3_encode(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    float a = fabsf(v);
+    if (a >= 448.0f)
+        return sign | 0x7E;
+    if (a < ldexpf(1.0f, -6)) {
+        int q = (int)rintf(ldexpf(a, 9));              /* 0..8; 8 is the smallest normal, code 0x08 */
+        return sign | (uint8_t)q;
+    }
+    int ex2;
+    frexpf(a, &ex2);                                    /* a = f * 2^ex2, f in [0.5, 1) */
+    int e = ex2 - 1;                                    /* a in [2^e, 2^(e+1)) */
+    int q = (int)rintf(ldexpf(a, 3 - e));               /* 8..16 */
+    if (q == 16) {
+        q = 8;
+        e += 1;
+    }
+    int field = e + 7, man = q - 8;
+    if (field > 15 || (field == 15 && man == 7))
+        return sign | 0x7E;
+    return sign | (uint8_t)((field << 3) | man);
+}
+
+/* rows x K bf16 weights (K a multiple of 32) -> q[rows, K] E4M3 codes and
+ * s[rows, K/32] E8M0 scale codes, both row-major. */
+void oracle_mx_quantize(int64_t rows, int32_t K, const uint16_t *w, uint8_t *q, uint8_t *s)
+{
+    int32_t nb = K / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int32_t b = 0; b < nb; ++b) {
+            const uint16_t *v = w + r * K + (int64_t)b * 32;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                float a = fabsf(bf16_bits_to_f32(v[i]));
+                if (a > amax)
+                    amax = a;
+            }
+            int e = -127;
+            if (amax > 0.0f) {
+                int ex2;
+                frexpf(amax, &ex2);
+                e = (ex2 - 1) - 8;
+                if (e < -127)
+                    e = -127;
+                if (e > 127)
+                    e = 127;
+            }
+            s[r * nb + b] = (uint8_t)(e + 127);
+            for (int i = 0; i < 32; ++i)
+                q[r * K + (int64_t)b * 32 + i] = e4m3_encode(ldexpf(bf16_bits_to_f32(v[i]), -e));
+        }
+    }
+}
+
+/* q[rows, K], s[rows, K/32] -> bf16 bits of X * P. */
+void oracle_mx_dequantize(int64_t rows, int32_t K, const uint8_t *q, const uint8_t *s, uint16_t *out)
+{
+    int32_t nb = K / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int32_t k = 0; k < K; ++k) {
+            int e = (int)s[r * nb + k / 32] - 127;
+            out[r * K + k] = f32_to_bf16_bits_rne(ldexpf(e4m3_value(q[r * K + k]), e));
+        }
 }

@@ -14,6 +14,15 @@
                        ``(sum_j w[t,j]) * x[t]`` (closed form).
 * whole forward     -- a naive fp64 restatement in pure Python loops on tiny
                        shapes, several experts, dropped slots included.
+* MXFP8 (E4M3 codes, E8M0 scale per 32, OCP MX v1.0; FlashInfer moe_ep page
+  PR #3980, MXFP8 path) --
+                       the E4M3 values the OCP FP8 spec prints (largest and
+                       smallest normal and subnormal, NaN, zeros) and the
+                       powers of two; element rounding against a brute-force
+                       nearest-code search (ties to the even mantissa,
+                       saturation at 448); the scale rule as the bound
+                       256 <= max|V| / X < 512; grid values round-tripping
+                       exactly; a block of zeros.
 
 ``test_planted_mistakes`` then builds mutated copies of ``moe_oracle.c``
 (a dropped term, a swapped operand, a wrong sign, a wrong index ...) and
@@ -297,8 +306,117 @@ def pin_streamed_equals_tokens(o: Oracle):
     assert np.array_equal(acc_c.view(np.uint32), acc_a[sub].view(np.uint32))
 
 
+def pin_e4m3_values(o: Oracle):
+    """The E4M3 values the OCP 8-bit floating point spec prints for the format:
+    max normal S.1111.110 = 448, min normal S.0001.000 = 2^-6, max subnormal
+    S.0000.111 = 0.875 * 2^-6, min subnormal S.0000.001 = 2^-9, NaN
+    S.1111.111, zeros S.0000.000; exponent bias 7, so 2^p is code (p+7) << 3."""
+    v = o.e4m3_values().astype(np.float64)
+    assert v[0x00] == 0.0 and not math.copysign(1.0, v[0x00]) < 0
+    assert v[0x80] == 0.0 and math.copysign(1.0, v[0x80]) < 0
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0
+    assert v[0x08] == 2.0 ** -6 and v[0x07] == 0.875 * 2.0 ** -6 and v[0x01] == 2.0 ** -9
+    assert math.isnan(v[0x7F]) and math.isnan(v[0xFF])
+    for p in range(-6, 9):
+        assert v[(p + 7) << 3] == 2.0 ** p, p
+    assert v[0x3C] == 1.5 and v[0x30] == 0.5 and v[0x44] == 3.0
+    pos = v[1:0x7F]
+    assert np.all(np.diff(pos) > 0)                       # codes increase with magnitude
+    assert np.array_equal(v[0x81:0xFF], -pos)              # sign bit mirrors
+    # within a binade the 8 codes are evenly spaced by 2^(p-3)
+    for p in range(-6, 8):
+        b = v[(p + 7) << 3: ((p + 8) << 3) + 1]
+        assert np.allclose(np.diff(b), 2.0 ** (p - 3), rtol=0, atol=0), p
+
+
+def _mx_block_with_unit_scale(vals):
+    """bf16 bits of blocks of 32 whose largest magnitude is 256 (element 0), so
+    the MX scale is 2^0 and each element is encoded as E4M3(value) itself."""
+    vals = np.asarray(vals, dtype=np.float32).reshape(-1, 31)
+    blocks = np.concatenate([np.full((vals.shape[0], 1), 256.0, np.float32), vals], axis=1)
+    return torch_bf16_bits(blocks)
+
+
+def pin_e4m3_rounding_brute(o: Oracle):
+    """Element rounding = the nearest finite E4M3 value, found by searching all
+    codes; a tie goes to the code with the even mantissa; |v| > 448 -> 448."""
+    table = o.e4m3_values().astype(np.float64)
+    finite = [c for c in range(256) if not math.isnan(table[c])]
+    rng = np.random.default_rng(11)
+    parts = [rng.uniform(-255, 255, 31 * 40), rng.uniform(-2, 2, 31 * 40),
+             rng.uniform(-2 ** -5, 2 ** -5, 31 * 40),            # subnormal region
+             np.sign(rng.uniform(-1, 1, 31 * 4)) * 2.0 ** rng.integers(-12, 8, 31 * 4)]
+    # exact midpoints between neighbouring codes (ties), representable in bf16
+    m = (table[1:0x7E] + table[2:0x7F]) / 2
+    m = m[m < 255]
+    m = m[bf16_bits_to_f32(torch_bf16_bits(m.astype(np.float32))).astype(np.float64) == m]
+    mids = np.concatenate([m, -m])
+    assert mids.size > 100
+    mids = mids[: 31 * (mids.size // 31)]
+    vals = np.concatenate(parts + [mids])
+    vals = vals[: 31 * (vals.size // 31)]
+    bits = _mx_block_with_unit_scale(vals)
+    q, sc = o.mx_quantize(bits)
+    assert np.all(sc == 127)
+    vb = bf16_bits_to_f32(bits).astype(np.float64)
+    for v, c in zip(vb.reshape(-1), q.reshape(-1)):
+        d = np.array([abs(v - table[f]) for f in finite])
+        best = np.flatnonzero(d == d.min())
+        cand = [finite[i] for i in best]
+        if v == 0.0:
+            want = 0x80 if math.copysign(1.0, v) < 0 else 0x00
+        elif len(cand) == 1:
+            want = cand[0]
+        else:
+            even = [x for x in cand if (x & 1) == 0 and (x & 0x80) == (0x80 if v < 0 else 0)]
+            want = even[0]
+        assert c == want, (v, c, want)
+    # saturation: magnitudes in (448, 512) with the block scale still 2^0
+    sat = torch_bf16_bits(np.array([[500.0, -460.0, 449.0, 300.0] + [1.0] * 28], np.float32))
+    q, sc = o.mx_quantize(sat)
+    assert sc[0, 0] == 127 and q[0, 0] == 0x7E and q[0, 1] == 0xFE and q[0, 2] == 0x7E
+
+
+def pin_mx_scale_rule(o: Oracle):
+    """Per block: X = 2^(s - 127) with 256 <= max|V| / X < 512 (the scale puts
+    the block maximum in E4M3's top binade); a block of zeros gets s = 0 and
+    zero codes."""
+    rng = np.random.default_rng(12)
+    w = rng.standard_normal((64, 256)).astype(np.float32) * (2.0 ** rng.integers(-20, 20, (64, 1)))
+    w[3, 32:64] = 0.0
+    bits = torch_bf16_bits(w)
+    q, sc = o.mx_quantize(bits)
+    wb = bf16_bits_to_f32(bits).astype(np.float64).reshape(64, 8, 32)
+    amax = np.abs(wb).max(axis=2)
+    X = np.ldexp(1.0, sc.astype(np.int64) - 127)
+    nz = amax > 0
+    assert np.all(amax[nz] / X[nz] >= 256) and np.all(amax[nz] / X[nz] < 512)
+    assert sc[3, 1] == 0 and np.all(q[3, 32:64] & 0x7F == 0)
+
+
+def pin_mx_round_trip(o: Oracle):
+    """Weights already on the MX grid (codes times a power of two, block
+    maximum in the top binade) come back with the same codes and scale, and
+    dequantize to exactly themselves."""
+    rng = np.random.default_rng(13)
+    rows, nb = 16, 4
+    codes = rng.integers(0, 0x7F, (rows, nb * 32)).astype(np.uint8) | (rng.integers(0, 2, (rows, nb * 32)) << 7).astype(np.uint8)
+    codes[:, ::32] = (0x78 + rng.integers(0, 7, (rows, nb))).astype(np.uint8)    # 256..448: top binade
+    e = rng.integers(-30, 10, (rows, nb))
+    table = o.e4m3_values().astype(np.float64)
+    vals = table[codes] * np.repeat(np.ldexp(1.0, e), 32, axis=1)
+    bits = torch_bf16_bits(vals.astype(np.float32))
+    assert np.array_equal(bf16_bits_to_f32(bits).astype(np.float64), vals)      # exact in bf16
+    q, sc = o.mx_quantize(bits)
+    assert np.array_equal(sc.astype(np.int64) - 127, e)
+    same = (q == codes) | ((q & 0x7F) == 0) & ((codes & 0x7F) == 0)
+    assert np.all(same)
+    assert np.array_equal(o.mx_dequantize(q, sc), bits)
+
+
 PINS = [pin_round_bf16, pin_dispatch_hand, pin_dispatch_brute, pin_dense_mlp,
-        pin_identity_expert, pin_naive_fp64, pin_streamed_equals_tokens]
+        pin_identity_expert, pin_naive_fp64, pin_streamed_equals_tokens,
+        pin_e4m3_values, pin_e4m3_rounding_brute, pin_mx_scale_rule, pin_mx_round_trip]
 
 
 # ----------------------------------------------------------------------------- tests
@@ -335,6 +453,13 @@ MUTATIONS = [
     ("offsets_inclusive", "offsets[e + 1] = offsets[e] + counts[e];", "offsets[e + 1] = offsets[e] + counts[e] + (e == 0);"),
     ("round_half_up", "u += 0x7fffu + keep_lsb;", "u += 0x8000u;"),
     ("round_truncate", "u += 0x7fffu + keep_lsb;", "u += 0u * keep_lsb;"),
+    ("mx_emax_7", "e = (ex2 - 1) - 8;", "e = (ex2 - 1) - 7;"),
+    ("e4m3_round_half_up", "int q = (int)rintf(ldexpf(a, 3 - e));", "int q = (int)floorf(ldexpf(a, 3 - e) + 0.5f);"),
+    ("e4m3_subnormal_step", "int q = (int)rintf(ldexpf(a, 9));", "int q = (int)rintf(ldexpf(a, 8));"),
+    ("e4m3_saturate_to_nan", "if (a >= 448.0f)\n        return sign | 0x7E;", "if (a >= 448.0f)\n        return sign | 0x7F;"),
+    ("e4m3_value_bias", "mag = ldexpf(1.0f + (float)man / 8.0f, ex - 7);", "mag = ldexpf(1.0f + (float)man / 8.0f, ex - 8);"),
+    ("mx_dequant_scale_bias", "int e = (int)s[r * nb + k / 32] - 127;", "int e = (int)s[r * nb + k / 32] - 126;"),
+    ("mx_block_stride", "const uint16_t *v = w + r * K + (int64_t)b * 32;", "const uint16_t *v = w + r * K + (int64_t)b * 31;"),
     ("invalid_id_kept", "if (e >= 0 && e < E)\n            counts[e] += 1;", "if (e >= 0 && e < E + 1 && e != E)\n            counts[e] += 1;\n        if (e == E) counts[0] += 1;"),
 ]
 
