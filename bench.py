@@ -70,17 +70,19 @@ NCU_TRAFFIC = {
 
 # ----------------------------------------------------------------------------- accounting
 
-def call_accounting(wl: wlm.Workload, ids_np: np.ndarray) -> dict:
-    """FLOPs and algorithmic bytes of one forward over this routing."""
+def call_accounting(wl: wlm.Workload, ids_np: np.ndarray, weight_bytes: float = 2.0) -> dict:
+    """FLOPs and algorithmic bytes of one forward over this routing;
+    weight_bytes per weight element: 2 (bf16), 33/32 (MXFP8 codes + scales)."""
     R = int(np.count_nonzero(ids_np >= 0))
     touched = int(np.unique(ids_np[ids_np >= 0]).size)
     T, H, I = wl.T, wl.H, wl.I
+    wb = weight_bytes
     return {
         "flops": 6.0 * R * H * I,
-        "bytes": touched * 6.0 * H * I + 2.0 * T * H * 2 + 8.0 * R,
+        "bytes": touched * 3.0 * wb * H * I + 2.0 * T * H * 2 + 8.0 * R,
         "gemm1_flops": 4.0 * R * H * I,
-        "gemm1_bytes": touched * 4.0 * I * H + 2.0 * R * H + 2.0 * R * I,
-        "gemm2_bytes": touched * 2.0 * H * I + 2.0 * R * I + 2.0 * R * H,
+        "gemm1_bytes": touched * 2.0 * wb * I * H + 2.0 * R * H + 2.0 * R * I,
+        "gemm2_bytes": touched * wb * H * I + 2.0 * R * I + 2.0 * R * H,
         "touched_experts": touched,
         "R": R,
     }
@@ -277,7 +279,8 @@ def run_ours(args, world, rank, local):
     init_dist(world, local)
     names = WORKLOAD_SETS[args.workload]
     inputs = make_inputs(names, device, args.experts, args.tokens)
-    layout = B.MOE_WEIGHTS_PACKED if args.packed else B.MOE_WEIGHTS_ROW_MAJOR
+    layout = (B.MOE_WEIGHTS_MXFP8 if args.weights == "mxfp8" else
+              B.MOE_WEIGHTS_PACKED if args.packed else B.MOE_WEIGHTS_ROW_MAJOR)
     for d in inputs:
         wl = d["wl"]
         d["problem"] = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path, weight_layout=layout,
@@ -286,6 +289,11 @@ def run_ours(args, world, rank, local):
             d["W13"], d["W2"] = B.moe_pack_weights(d["problem"], d["W13"], d["W2"])
             torch.cuda.synchronize(device)
             torch.cuda.empty_cache()
+        if args.weights == "mxfp8":   # quantized once at model load; the bf16 copy is released
+            d["W13"], d["W2"] = B.moe_quantize_weights(d["problem"], d["W13"], d["W2"])
+            torch.cuda.synchronize(device)
+            torch.cuda.empty_cache()
+            d["acct"] = call_accounting(wl, d["ids_np"], weight_bytes=33.0 / 32.0)
         d["bufs"] = B.Buffers(d["problem"], device)
         d["path"] = B.moe_resolve_path(d["problem"])
         d["profile"] = B.moe_resolve_profile(d["problem"])
@@ -421,7 +429,8 @@ def run_ours(args, world, rank, local):
     roof["algorithmic_per_step"] = g1_flops if roof["bound"] == "tensor" else g1_bytes
     traffic = None
     key = "small_m_fused_bytes_per_touched_expert" if fused else "small_m_gate_up_bytes_per_touched_expert"
-    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and key in NCU_TRAFFIC and all(d["path"][0] == 2 for d in inputs):
+    if (NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and key in NCU_TRAFFIC and args.weights == "bf16"
+            and all(d["path"][0] == 2 for d in inputs)):
         per = [d["acct"]["touched_experts"] * NCU_TRAFFIC[key] for d in inputs]
         traffic = float(sum(per)) / len(per)
     roof["traffic"] = traffic
@@ -456,7 +465,8 @@ def run_ours(args, world, rank, local):
             "timing": (f"CUDA graph of {G} step(s) replayed {n_replays}x between CUDA events; kernel and stage "
                        f"times from a second graph of the same steps with stage events, replayed {prof_replays}x"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "weights": "packed (access-ordered)" if args.packed else "row-major",
+            "weights": ("MXFP8 (E4M3 codes + E8M0 scale per 32, expanded to bf16 on chip)"
+                        if args.weights == "mxfp8" else "packed (access-ordered)" if args.packed else "row-major"),
         },
         "us_per_call": {d["wl"].name: float(sum(s)) for d, s in zip(inputs, stage_us)},
         "profiled_ms_per_step": prof_ms_per_step,
@@ -467,16 +477,19 @@ def run_ours(args, world, rank, local):
                             for d, s in zip(inputs, stage_us)},
         "call_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": ms_per_step * 1e3,
                           "frac": t_roof * 1e3 / ms_per_step,
-                          "touched_expert_weights_gb": {d["wl"].name: d["acct"]["touched_experts"] * 6 * d["wl"].H
-                                                        * d["wl"].I / 1e9 for d in inputs}},
+                          "touched_expert_weights_gb": {d["wl"].name: d["acct"]["touched_experts"] * 3 * d["wl"].H
+                                                        * d["wl"].I * (33 / 32 if args.weights == "mxfp8" else 2)
+                                                        / 1e9 for d in inputs}},
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": sum(d["profile"]["kernel_launches"] for d in inputs) * K,
         "clocks": clk,
     }
-    if rank == 0 and args.packed:
+    if args.weights == "mxfp8":
+        result["dtype"] = "bf16 (weights mxfp8)"
+    if rank == 0 and (args.packed or args.weights == "mxfp8"):
         result["cpu_baseline"] = None
-        result["cpu_baseline_note"] = "not run with --packed (the oracle reads row-major weights)"
+        result["cpu_baseline_note"] = "not run with --packed / --weights mxfp8 (see the row-major bf16 line)"
     elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = time_oracle(inputs, args.cpu_seconds,
                                              tokens_cap=args.cpu_tokens if args.cpu_tokens > 0 else None)
@@ -717,6 +730,8 @@ def parse_args(argv=None):
     ap.add_argument("--sweep", action="store_true", help="token-count sweep at the 384-expert shape (not the bench line)")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3],
                     help="expert-GEMM path: 0 auto, 1 tiled CTA pairs, 2 M-small, 3 tiled single CTA")
+    ap.add_argument("--weights", choices=["bf16", "mxfp8"], default="bf16",
+                    help="expert weights: bf16, or MXFP8 quantized at load (M-small path only)")
     ap.add_argument("--form", type=int, default=0, choices=[0, 1, 2],
                     help="decode-size forward: 0 auto, 1 separate kernels, 2 one kernel")
     ap.add_argument("--compare-forms", action="store_true",

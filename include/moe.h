@@ -116,8 +116,28 @@ typedef enum moe_forward_form {
  *  are bitwise identical to ROW_MAJOR. */
 typedef enum moe_weight_layout {
     MOE_WEIGHTS_ROW_MAJOR = 0,
-    MOE_WEIGHTS_PACKED = 1
+    MOE_WEIGHTS_PACKED = 1,
+    MOE_WEIGHTS_MXFP8 = 2
 } moe_weight_layout_t;
+
+/* MXFP8: the pages' MXFP8 path with prequantized expert weights (FlashInfer
+ * moe_ep page, PR #3980; format 32 e4m3 x e8m0), OCP Microscaling v1.0. Each
+ * 32 consecutive elements of a row along K (H for W13, I for W2) share one
+ * E8M0 scale X = 2^e; each element is an FP8 E4M3 code P; the weight is X * P.
+ * The output of moe_quantize_weights, one buffer per matrix:
+ *   codes:  [E, 2I, H] (W13) or [E, H, I] (W2) bytes, row-major;
+ *   scales: right after the codes, rows*K/32 bytes in the order the decode
+ *           GEMMs read them: for each 128-row tile (rows counted over all
+ *           experts), each 128-wide K block: 128 rows x 4 bytes, the scales of
+ *           the row's four 32-element sub-blocks; scale code = e + 127.
+ * moe_forward reads MXFP8 weights on the M-small path (a = T_max*k/E <= 16,
+ * the HBM-bound decode shapes, where the weights are nearly all the bytes):
+ * it streams the 1-byte codes and expands X * P to bf16 on the chip, exactly,
+ * then multiplies by the bf16 activations as for bf16 weights. Activations,
+ * h and the output stay bf16 (SiLU(gate)*up rounded to bf16 as before), so
+ * the result is the bf16 forward on the dequantized weights. Other paths and
+ * moe_expert_compute return MOE_ERR_UNSUPPORTED for this layout. Weights must
+ * be finite with every block maximum in [2^-110, 2^24). */
 
 /* Bytes of workspace every entry point below needs for `problem` (pure host
  * arithmetic, no CUDA call). The same workspace serves all entry points; it
@@ -271,6 +291,19 @@ moe_status_t moe_dispatch_noalloc(const moe_problem_t *problem, const int32_t *t
  */
 moe_status_t moe_pack_weights(const moe_problem_t *problem, const void *W13, const void *W2, void *W13_packed,
                               void *W2_packed, void *stream);
+
+/* Bytes of W13 and W2 in `layout` (ROW_MAJOR and PACKED: 2 per element;
+ * MXFP8: 1 per element plus one scale byte per 32). Pure host. */
+moe_status_t moe_weight_bytes(const moe_problem_t *problem, int32_t layout, size_t *w13_bytes,
+                              size_t *w2_bytes);
+
+/* Quantize W13 and W2 (row-major bf16) to the MXFP8 layout, once, at model
+ * load. W13_mx and W2_mx have moe_weight_bytes(MXFP8) bytes and must not
+ * overlap the sources. Only problem->E, H and I matter. Enqueued on `stream`.
+ * Bit-exact with the OCP MX definition above (round to nearest even,
+ * saturation at 448). */
+moe_status_t moe_quantize_weights(const moe_problem_t *problem, const void *W13, const void *W2,
+                                  void *W13_mx, void *W2_mx, void *stream);
 
 /* Read the sticky device error word of `ws` into *host_code (0 = none).
  * Synchronises `stream` (the only entry point that does). */

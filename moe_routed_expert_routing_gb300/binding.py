@@ -22,6 +22,7 @@ MOE_PATH_SMALL_M = 2
 MOE_PATH_TILED_1CTA = 3
 MOE_WEIGHTS_ROW_MAJOR = 0
 MOE_WEIGHTS_PACKED = 1
+MOE_WEIGHTS_MXFP8 = 2
 MOE_FORWARD_AUTO = 0
 MOE_FORWARD_SEPARATE = 1
 MOE_FORWARD_ONE_KERNEL = 2
@@ -40,6 +41,8 @@ EXPORTED_SYMBOLS = (
     "moe_forward_profiled",
     "moe_dispatch_noalloc",
     "moe_pack_weights",
+    "moe_weight_bytes",
+    "moe_quantize_weights",
     "moe_last_device_error",
     "moe_clear_device_error",
     "moe_status_string",
@@ -132,6 +135,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.moe_dispatch_noalloc.restype = st
     lib.moe_pack_weights.argtypes = [_P, _vp, _vp, _vp, _vp, _vp]
     lib.moe_pack_weights.restype = st
+    lib.moe_weight_bytes.argtypes = [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t),
+                                     ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_weight_bytes.restype = st
+    lib.moe_quantize_weights.argtypes = [_P, _vp, _vp, _vp, _vp, _vp]
+    lib.moe_quantize_weights.restype = st
     lib.moe_last_device_error.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
     lib.moe_last_device_error.restype = st
     lib.moe_clear_device_error.argtypes = [_vp, _vp]
@@ -246,6 +254,26 @@ def moe_pack_weights(problem, W13, W2, W13_packed=None, W2_packed=None, stream=N
     _check(load_library().moe_pack_weights(ctypes.byref(problem), _ptr(W13), _ptr(W2), _ptr(W13_packed),
                                            _ptr(W2_packed), _stream(stream)), "moe_pack_weights")
     return W13_packed, W2_packed
+
+
+def moe_weight_bytes(problem, layout):
+    """(W13 bytes, W2 bytes) of the weights in ``layout``."""
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(load_library().moe_weight_bytes(ctypes.byref(problem), int(layout), ctypes.byref(a), ctypes.byref(b)),
+           "moe_weight_bytes")
+    return a.value, b.value
+
+
+def moe_quantize_weights(problem, W13, W2, W13_mx=None, W2_mx=None, stream=None):
+    """Quantize row-major bf16 W13/W2 to the MXFP8 layout; returns (W13_mx, W2_mx) uint8 buffers."""
+    b13, b2 = moe_weight_bytes(problem, MOE_WEIGHTS_MXFP8)
+    if W13_mx is None:
+        W13_mx = torch.empty(b13, dtype=torch.uint8, device=W13.device)
+    if W2_mx is None:
+        W2_mx = torch.empty(b2, dtype=torch.uint8, device=W2.device)
+    _check(load_library().moe_quantize_weights(ctypes.byref(problem), _ptr(W13), _ptr(W2), _ptr(W13_mx),
+                                               _ptr(W2_mx), _stream(stream)), "moe_quantize_weights")
+    return W13_mx, W2_mx
 
 
 def moe_last_device_error(ws, stream=None) -> int:

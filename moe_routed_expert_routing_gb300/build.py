@@ -19,7 +19,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["moe_api.cu", "dispatch.cu", "dispatch_noalloc.cu", "combine.cu", "grouped_gemm.cu", "weights_pack.cu"]
+SOURCES = ["moe_api.cu", "dispatch.cu", "dispatch_noalloc.cu", "combine.cu", "grouped_gemm.cu", "weights_pack.cu",
+           "weights_mx.cu"]
 HEADERS = ["ptx.cuh", "moe_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

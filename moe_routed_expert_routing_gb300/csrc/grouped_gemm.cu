@@ -527,17 +527,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 // calls need no memset. The split down GEMM writes its two K halves to two
 // fp32 buffers that the combine adds (a + b: the same value the two-atomic
 // form produces), so y needs no zeroing either.
-template <int kTileRows, int kStages>
+//
+// MXFP8 weights (kFp8): a weight block is 128 K elements (one 128-byte row of
+// E4M3 codes) plus its 4 scale bytes per row; a stage holds two such 16 KB
+// tiles (gate and up, or two K blocks of a down tile), their two 512-byte
+// scale blocks and the matching bf16 token tiles (64-wide K blocks). Eight
+// converter warps (two per TMEM lane quarter, one per weight tile) expand
+// each row's 128 codes times its scales to bf16, exactly, into a ring of TMEM
+// slots; the MMAs read their A operand (the weights) from there and the token
+// tile from shared memory as before. Weight bytes in flight per SM stay at
+// 32 KB per stage, which now hold twice the K of the bf16 stages.
+template <int kTileRows, int kStages, bool kFp8 = false>
 struct FusedCfg {
-    static constexpr int kActSlot = kTileRows * 128;          // one K block of the token tile
+    static constexpr int kThreadsCta = kFp8 ? 512 : 256;      // fp8: + 8 converter warps
+    static constexpr int kWK = kFp8 ? 128 : 64;               // K elements of one weight block
+    static constexpr int kActSlot = kTileRows * 128;          // one 64-wide K block of the token tile
+    static constexpr int kActSlots = kFp8 ? 4 : 2;
     static constexpr int kWBytes = 256 * 128;                 // gate + up tile, or two K blocks of a down tile
-    static constexpr int kStageBytes = kWBytes + 2 * kActSlot;
+    static constexpr int kScaleOffset = kWBytes + kActSlots * kActSlot;
+    static constexpr int kStageBytes = kScaleOffset + (kFp8 ? 1024 : 0);
     static constexpr int kAccCols = 2 * kTileRows;           // gate-up: two accumulators; down: one
-    static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);
+    static constexpr int kASlotCols = 128;                    // fp8: the two bf16 weight tiles of one stage
+    static constexpr int kASlots = kFp8 ? (512 - 2 * kAccCols) / kASlotCols : 0;
+    static constexpr int kTmemCols = kFp8 ? 512 : pow2_at_least(2 * kAccCols);
     static constexpr uint32_t kIdesc = idesc_bf16_f32(128, kTileRows);
     static constexpr int kDynSmem = 1024 + kStages * kStageBytes;
     static_assert(kTileRows % 16 == 0 && kTileRows >= 16 && kTileRows <= 64, "token tile");
-    static_assert(kActSlot % 1024 == 0, "1024-byte aligned tiles");
+    static_assert(kActSlot % 1024 == 0 && kStageBytes % 1024 == 0, "1024-byte aligned tiles");
+    static_assert(!kFp8 || kASlots >= 2, "fp8: at least two TMEM weight slots");
 };
 
 struct FusedArgs {
@@ -545,6 +562,8 @@ struct FusedArgs {
     GemmArgs down;     // down: act = h, out = y, K = I, n_out = H
     int32_t *ready;    // [E] finished gate-up units per expert, zero at launch and at exit
     int32_t *exits;    // CTAs at the tail, zero at launch and at exit
+    const uint8_t *sc13;   // MXFP8: scale blocks of W13 and W2 (512 B per 128-row tile and 128-wide K block)
+    const uint8_t *sc2;
     // whole-forward form only
     const int32_t *ids;            // [T_max, k] routed expert of each slot, -1 = dropped
     const float *topk_w;           // [T_max, k]
@@ -564,6 +583,7 @@ struct FusedArgs {
 // = row or -1. s_cur[E] is scratch. The ids of all T_max tokens are fetched
 // together with T (those past T are never used), so the prologue pays one
 // global round trip. Returns T.
+template <int kThreads>
 __device__ int cta_dispatch(const FusedArgs &fa, int E, int *s_off, int *s_cur, int *s_perm, int *s_inv)
 {
     static_assert(4 * kThreads >= kMaxExperts, "the scan covers four experts per thread");
@@ -660,7 +680,7 @@ __device__ int cta_dispatch(const FusedArgs &fa, int E, int *s_off, int *s_cur, 
 // no fused multiply-add (the arithmetic of combine_kernel). y was written by
 // other CTAs during this launch: read through L2 (ld.global.cg), never the
 // read-only path. With a split down GEMM the row is y0 + y1.
-template <int kSplitDown>
+template <int kSplitDown, int kThreads>
 __device__ void cta_combine(const FusedArgs &fa, const int *s_inv, int T)
 {
     const int k = fa.up.k;
@@ -716,13 +736,15 @@ __device__ void cta_combine(const FusedArgs &fa, const int *s_inv, int T)
     }
 }
 
-template <int kTileRows, int kStages, int kSplitDown, bool kMega>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kTileRows, int kStages, int kSplitDown, bool kMega, bool kFp8>
+__global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCta, 1)
     fused_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w13,
                        const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w2,
                        const FusedArgs fa)
 {
-    using C = FusedCfg<kTileRows, kStages>;
+    using C = FusedCfg<kTileRows, kStages, kFp8>;
+    constexpr int kThreads = C::kThreadsCta;
+    constexpr int kASlotsRing = kFp8 ? C::kASlots : 1;
     // the whole-forward form keeps its expert tables (sized by E and T_max * k)
     // in dynamic shared memory after the stages
     constexpr int kStaticTable = kMega ? 1 : kMaxExperts + 1;
@@ -733,6 +755,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(8) uint64_t bar_tfull[2];
     __shared__ __align__(8) uint64_t bar_tempty[2];
     __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ __align__(8) uint64_t bar_conv_full[kASlotsRing];    // fp8: weights expanded into a TMEM slot
+    __shared__ __align__(8) uint64_t bar_conv_empty[kASlotsRing];   // fp8: the MMAs reading a slot are done
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
     __shared__ int s_T;
@@ -763,6 +787,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bar_tempty[b]), 128);
         }
         mbar_init(smem_u32(&bar_drain), 1);
+        if (kFp8)
+            for (int i = 0; i < kASlotsRing; ++i) {
+                mbar_init(smem_u32(&bar_conv_full[i]), 8);
+                mbar_init(smem_u32(&bar_conv_empty[i]), 1);
+            }
         s_abort = 0;
         fence_barrier_init();
     }
@@ -778,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     pdl_wait();
     if (kMega) {
-        const int T = cta_dispatch(fa, E, s_off, s_tp, s_perm, s_inv);
+        const int T = cta_dispatch<kThreads>(fa, E, s_off, s_tp, s_perm, s_inv);
         if (threadIdx.x == 0)
             s_T = T;
     } else {
@@ -797,8 +826,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int NT2 = A2.n_out / 128;                 // down column tiles (H / 128)
     const int units1 = s_tp[E] * NT1;
     const int total_units = units1 + s_tp[E] * NT2 * kSplitDown;
-    const int kb1 = A1.K / kBK;
-    const int kb2 = A2.K / kBK / kSplitDown;
+    const int kb1 = A1.K / C::kWK;
+    const int kb2 = A2.K / C::kWK / kSplitDown;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -842,7 +871,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t full = smem_u32(&bar_full[stage]);
                     const uint32_t w_dst = smem_u32(smem + stage * C::kStageBytes);
                     const uint32_t a_dst = w_dst + C::kWBytes;
-                    if (up) {
+                    const uint32_t sc_dst = w_dst + C::kScaleOffset;
+                    if (kFp8 && up) {
+                        // gate and up code tiles of K block st, their scales, two token K blocks
+                        mbar_arrive_expect_tx(full, C::kWBytes + 1024 + 2 * C::kActSlot);
+                        const int wr = t.e * A1.w_rows_per_expert + t.n0;
+                        const long long kbt = A1.K / 128;
+                        tma_load_2d(w_dst, &tm_w13, full, st * 128, wr, pol_w);
+                        tma_load_2d(w_dst + 128 * 128, &tm_w13, full, st * 128, wr + A1.up_row_offset, pol_w);
+                        bulk_load(sc_dst, fa.sc13 + ((wr / 128) * kbt + st) * 512, 512, full, pol_w);
+                        bulk_load(sc_dst + 512, fa.sc13 + (((wr + A1.up_row_offset) / 128) * kbt + st) * 512, 512,
+                                  full, pol_w);
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+#pragma unroll
+                            for (int q = 0; q < kTileRows / 4; ++q)
+                                tma_gather4(a_dst + j * C::kActSlot + q * 512, &tm_x, full, st * 128 + 64 * j,
+                                            reinterpret_cast<const int4 *>(s_rows)[q], pol_a);
+                    } else if (kFp8) {
+                        const int nkb = (2 * st + 1 < kb2) ? 2 : 1;
+                        mbar_arrive_expect_tx(full, nkb * (C::kWBytes / 2 + 512 + 2 * C::kActSlot));
+                        const int wr = t.e * A2.w_rows_per_expert + t.n0;
+                        const long long kbt = A2.K / 128;
+                        for (int j = 0; j < nkb; ++j) {
+                            const int kb = kb0 + 2 * st + j;
+                            tma_load_2d(w_dst + j * 128 * 128, &tm_w2, full, kb * 128, wr, pol_w);
+                            bulk_load(sc_dst + j * 512, fa.sc2 + ((wr / 128) * kbt + kb) * 512, 512, full, pol_w);
+                            tma_load_2d(a_dst + (2 * j) * C::kActSlot, &tm_h, full, kb * 128, t.row0, pol_a);
+                            tma_load_2d(a_dst + (2 * j + 1) * C::kActSlot, &tm_h, full, kb * 128 + 64, t.row0,
+                                        pol_a);
+                        }
+                    } else if (up) {
                         mbar_arrive_expect_tx(full, C::kWBytes + C::kActSlot);
                         const int wr = t.e * A1.w_rows_per_expert + t.n0;
                         const int2 g = weight_coords(A1, true, wr, st);
@@ -888,6 +947,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            int slot = 0;
+            uint32_t slot_phase = 0;
             bool ok = true;
             int local = 0;
             for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++local) {
@@ -902,14 +963,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * C::kAccCols;
                 for (int st = 0; st < steps; ++st) {
-                    if (!mbar_wait_bounded(smem_u32(&bar_full[stage]), phase, abort_flag, A1.wait_limit_ns)) {
+                    if (!mbar_wait_bounded(smem_u32(&bar_full[stage]), phase, abort_flag, A1.wait_limit_ns) ||
+                        (kFp8 && !mbar_wait_bounded(smem_u32(&bar_conv_full[slot]), slot_phase, abort_flag,
+                                                    A1.wait_limit_ns))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t w_addr = smem_u32(smem + stage * C::kStageBytes);
                     const uint32_t a_addr = w_addr + C::kWBytes;
-                    if (up) {
+                    if (kFp8) {
+                        // weights (A) from the TMEM slot the converters filled, 8 K steps of 16 per block
+                        const uint32_t a_tm = tmem_base + 2 * C::kAccCols + slot * C::kASlotCols;
+                        const int nkb = up ? 1 : ((2 * st + 1 < kb2) ? 2 : 1);
+                        for (int j = 0; j < nkb; ++j) {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint32_t acc = (st > 0 || j > 0 || kk > 0) ? 1u : 0u;
+                                const uint64_t b_desc =
+                                    smem_desc_kmajor_sw128(a_addr + (2 * j + (kk >> 2)) * C::kActSlot + (kk & 3) * 32);
+                                umma_bf16_tmem_a(d_tmem, a_tm + 64 * j + 8 * kk, b_desc, C::kIdesc, acc);
+                                if (up)
+                                    umma_bf16_tmem_a(d_tmem + kTileRows, a_tm + 64 + 8 * kk, b_desc, C::kIdesc, acc);
+                            }
+                        }
+                        umma_commit(smem_u32(&bar_conv_empty[slot]));
+                        if (++slot == kASlotsRing) {
+                            slot = 0;
+                            slot_phase ^= 1u;
+                        }
+                    } else if (up) {
 #pragma unroll
                         for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
                             const uint32_t acc = (st > 0 || kk > 0) ? 1u : 0u;
@@ -944,6 +1027,73 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (kFp8 && warp >= 8) {
+        // ------------------------------------------------------------ converters (MXFP8 weights)
+        // warp 8 + 4h + q expands rows 32q..32q+31 of weight tile h of each
+        // stage (gate / up, or the stage's first / second K block) into TMEM
+        // lanes 32q.. of the slot: lane i owns row 32q + i, 128 codes -> 64
+        // columns of bf16 pairs.
+        const int quarter = warp & 3;
+        const int half = (warp - 8) >> 2;
+        const int row = quarter * 32 + lane;
+        int stage = 0;
+        uint32_t phase = 0;
+        int slot = 0;
+        uint32_t slot_phase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+            const bool up = u < units1;
+            const int steps = up ? kb1 : (kb2 + 1) / 2;
+            for (int st = 0; st < steps; ++st) {
+                const bool good = mbar_wait_bounded(smem_u32(&bar_full[stage]), phase, abort_flag, A1.wait_limit_ns) &&
+                                  mbar_wait_bounded(smem_u32(&bar_conv_empty[slot]), slot_phase ^ 1u, abort_flag,
+                                                    A1.wait_limit_ns);
+                if (!__all_sync(kFull, good)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int nkb = up ? 2 : ((2 * st + 1 < kb2) ? 2 : 1);
+                if (half < nkb) {
+                    const uint8_t *tile = smem + stage * C::kStageBytes + half * 128 * 128 + row * 128;
+                    const uint32_t codes4 =
+                        *reinterpret_cast<const uint32_t *>(smem + stage * C::kStageBytes + C::kScaleOffset +
+                                                             half * 512 + row * 4);
+                    const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                            2 * C::kAccCols + slot * C::kASlotCols + half * 64;
+#pragma unroll
+                    for (int c0 = 0; c0 < 8; c0 += 4) {
+                        uint32_t out[32];
+#pragma unroll
+                        for (int c = c0; c < c0 + 4; ++c) {
+                            // 16 codes of K [16c, 16c + 16), at the 128-byte swizzled position of chunk c
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(tile + ((c ^ (row & 7)) << 4));
+                            const uint32_t sbyte = (codes4 >> (8 * (c >> 1))) & 0xffu;
+                            const uint32_t scale2 = ((sbyte + 112u) << 7) * 0x00010001u;
+                            const int o = (c - c0) * 8;
+                            e4m3x4_to_bf16x4(raw.x, scale2, out[o + 0], out[o + 1]);
+                            e4m3x4_to_bf16x4(raw.y, scale2, out[o + 2], out[o + 3]);
+                            e4m3x4_to_bf16x4(raw.z, scale2, out[o + 4], out[o + 5]);
+                            e4m3x4_to_bf16x4(raw.w, scale2, out[o + 6], out[o + 7]);
+                        }
+                        tmem_st_32x32b_x32(t_addr + c0 * 8, out);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&bar_conv_full[slot]));
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (++slot == kASlotsRing) {
+                    slot = 0;
+                    slot_phase ^= 1u;
+                }
+            }
+        }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
         const int q = warp - 4;
@@ -1025,7 +1175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         if (!s_abort)
-            cta_combine<kSplitDown>(fa, s_inv, s_T);
+            cta_combine<kSplitDown, kThreads>(fa, s_inv, s_T);
         __syncthreads();
     }
     // tail clean-up: the last CTA out (every other CTA has passed all its
@@ -1434,7 +1584,7 @@ long long mega_table_bytes(int E, long long slots) { return 4LL * (2LL * (E + 1)
 // Per-block shared memory the device grants (opt-in) minus the static shared
 // memory of the whole-forward kernel and its stages: what is left for the
 // tables. Cached per device; -1 if a query fails.
-template <int kTileRows, int kStages>
+template <int kTileRows, int kStages, bool kFp8>
 long long mega_table_budget()
 {
     static int cached_dev = -1;
@@ -1446,26 +1596,46 @@ long long mega_table_budget()
         int optin = 0;
         cudaFuncAttributes fa1 = {}, fa2 = {};
         if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-            cudaFuncGetAttributes(&fa1, fused_small_kernel<kTileRows, kStages, 1, true>) != cudaSuccess ||
-            cudaFuncGetAttributes(&fa2, fused_small_kernel<kTileRows, kStages, 2, true>) != cudaSuccess)
+            cudaFuncGetAttributes(&fa1, fused_small_kernel<kTileRows, kStages, 1, true, kFp8>) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa2, fused_small_kernel<kTileRows, kStages, 2, true, kFp8>) != cudaSuccess)
             return -1;
         const size_t st = fa1.sharedSizeBytes > fa2.sharedSizeBytes ? fa1.sharedSizeBytes : fa2.sharedSizeBytes;
-        cached = static_cast<long long>(optin) - static_cast<long long>(st) - FusedCfg<kTileRows, kStages>::kDynSmem;
+        cached = static_cast<long long>(optin) - static_cast<long long>(st) -
+                 FusedCfg<kTileRows, kStages, kFp8>::kDynSmem;
         cached_dev = dev;
     }
     return cached;
 }
 
-template <int kTileRows, int kStages, int kSplitDown, bool kMega>
+// E4M3 codes [rows, K] as a 2-D byte tensor: 128-byte x 128-row boxes, 128-byte swizzle.
+bool make_map_codes(CUtensorMap *m, const void *base, uint64_t rows, uint64_t K)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {K};
+    const cuuint32_t box[2] = {128, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int kTileRows, int kStages, int kSplitDown, bool kMega, bool kFp8>
 cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *ready, int32_t *counters,
                       int num_sms, cudaStream_t stream, const MegaParams *mega)
 {
-    using C = FusedCfg<kTileRows, kStages>;
-    auto kern = fused_small_kernel<kTileRows, kStages, kSplitDown, kMega>;
+    using C = FusedCfg<kTileRows, kStages, kFp8>;
+    auto kern = fused_small_kernel<kTileRows, kStages, kSplitDown, kMega, kFp8>;
     const long long slots = mega ? static_cast<long long>(mega->T_max) * up.k : 0;
     const long long tables = kMega ? mega_table_bytes(up.E, slots) : 0;
-    if (kMega && tables > mega_table_budget<kTileRows, kStages>())
-        return cudaErrorInvalidValue;
+    long long budget = 0;
+    if constexpr (kMega) {
+        budget = mega_table_budget<kTileRows, kStages, kFp8>();
+        if (tables > budget)
+            return cudaErrorInvalidValue;
+    }
     const int dyn_smem = C::kDynSmem + static_cast<int>(tables);
     static int attr_done_for_device = -1;
     static int attr_bytes = 0;
@@ -1474,7 +1644,7 @@ cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *r
     if (e != cudaSuccess)
         return e;
     if (attr_done_for_device != dev || attr_bytes < dyn_smem) {
-        const int want = kMega ? C::kDynSmem + static_cast<int>(mega_table_budget<kTileRows, kStages>()) : C::kDynSmem;
+        const int want = C::kDynSmem + static_cast<int>(budget);
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
         if (e != cudaSuccess)
             return e;
@@ -1482,15 +1652,22 @@ cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *r
         attr_bytes = want;
     }
     CUtensorMap tm_x, tm_w13, tm_h, tm_w2;
-    if (!make_map(&tm_x, up.act, static_cast<uint64_t>(up.act_rows), static_cast<uint64_t>(up.K), 1) ||
-        !make_weight_map(&tm_w13, up) ||
-        !make_map(&tm_h, down.act, static_cast<uint64_t>(down.cap), static_cast<uint64_t>(down.K), kTileRows) ||
-        !make_weight_map(&tm_w2, down))
+    const uint64_t rows13 = static_cast<uint64_t>(up.E) * up.w_rows_per_expert;
+    const uint64_t rows2 = static_cast<uint64_t>(down.E) * down.w_rows_per_expert;
+    const bool maps = kFp8 ? make_map_codes(&tm_w13, up.w, rows13, static_cast<uint64_t>(up.K)) &&
+                                 make_map_codes(&tm_w2, down.w, rows2, static_cast<uint64_t>(down.K))
+                           : make_weight_map(&tm_w13, up) && make_weight_map(&tm_w2, down);
+    if (!maps || !make_map(&tm_x, up.act, static_cast<uint64_t>(up.act_rows), static_cast<uint64_t>(up.K), 1) ||
+        !make_map(&tm_h, down.act, static_cast<uint64_t>(down.cap), static_cast<uint64_t>(down.K), kTileRows))
         return cudaErrorInvalidValue;
     FusedArgs fa = {};
     fa.up = make_args(up);
     fa.down = make_args(down);
     fa.ready = ready;
+    if (kFp8) {   // scale blocks follow the codes
+        fa.sc13 = static_cast<const uint8_t *>(up.w) + rows13 * static_cast<uint64_t>(up.K);
+        fa.sc2 = static_cast<const uint8_t *>(down.w) + rows2 * static_cast<uint64_t>(down.K);
+    }
     fa.exits = counters + 1;
     if (kMega) {
         fa.ids = mega->ids;
@@ -1507,13 +1684,16 @@ cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *r
     const long long tiles = (static_cast<long long>(up.cap) + kTileRows - 1) / kTileRows + up.E;
     const long long max_units = tiles * (up.n_out / 128 + (down.n_out / 128) * kSplitDown);
     const int grid = static_cast<int>(max_units < num_sms ? (max_units < 1 ? 1 : max_units) : num_sms);
-    return launch_k(kern, dim3(grid), dim3(kThreads), dyn_smem, stream, up.pdl, tm_x, tm_w13, tm_h, tm_w2, fa);
+    return launch_k(kern, dim3(grid), dim3(C::kThreadsCta), dyn_smem, stream, up.pdl, tm_x, tm_w13, tm_h, tm_w2,
+                    fa);
 }
 
 }  // namespace
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream)
 {
+    if (p.w_mxfp8)   // MXFP8 weights run through the fused M-small kernel only
+        return cudaErrorInvalidValue;
     if (p.split_k != 1 && (p.split_k != 2 || !p.small_m || p.gated || p.tile_rows != 16 || (p.K / kBK) % 2 != 0))
         return cudaErrorInvalidValue;
     if (p.gather && (!p.gated || !p.perm || p.k < 1))
@@ -1557,20 +1737,49 @@ cudaError_t launch_fused_small(const GemmProblem &up, const GemmProblem &down, i
                 mega->T_max < 1)
              : !up.perm)
         return cudaErrorInvalidValue;
-    // built for decode-size batches only (16-row token tiles): with 32-row
-    // tiles (the Zipf small batch) two launches measured 2% faster
+    if (up.w_mxfp8 != down.w_mxfp8)
+        return cudaErrorInvalidValue;
+    if (up.w_mxfp8) {
+        // MXFP8 weights: every M-small tile height (this kernel is their only GEMM)
+        if (up.K % 128 != 0 || down.K % 128 != 0 || (down.split_k == 2 && (down.K / 128) % 2 != 0))
+            return cudaErrorInvalidValue;
+        if (mega && (up.tile_rows != 16))
+            return cudaErrorInvalidValue;
+        switch (up.tile_rows) {
+        case 16:
+            if (mega)
+                return down.split_k == 2
+                           ? run_fused<16, 5, 2, true, true>(up, down, ready, counters, num_sms, stream, mega)
+                           : run_fused<16, 5, 1, true, true>(up, down, ready, counters, num_sms, stream, mega);
+            return down.split_k == 2
+                       ? run_fused<16, 5, 2, false, true>(up, down, ready, counters, num_sms, stream, nullptr)
+                       : run_fused<16, 5, 1, false, true>(up, down, ready, counters, num_sms, stream, nullptr);
+        case 32:
+            return down.split_k == 1
+                       ? run_fused<32, 4, 1, false, true>(up, down, ready, counters, num_sms, stream, nullptr)
+                       : cudaErrorInvalidValue;
+        case 64:
+            return down.split_k == 1
+                       ? run_fused<64, 3, 1, false, true>(up, down, ready, counters, num_sms, stream, nullptr)
+                       : cudaErrorInvalidValue;
+        default:
+            return cudaErrorInvalidValue;
+        }
+    }
+    // bf16 weights: built for decode-size batches only (16-row token tiles):
+    // with 32-row tiles (the Zipf small batch) two launches measured 2% faster
     if (up.tile_rows != 16)
         return cudaErrorInvalidValue;
     if (mega)
-        return down.split_k == 2 ? run_fused<16, 6, 2, true>(up, down, ready, counters, num_sms, stream, mega)
-                                 : run_fused<16, 6, 1, true>(up, down, ready, counters, num_sms, stream, mega);
-    return down.split_k == 2 ? run_fused<16, 6, 2, false>(up, down, ready, counters, num_sms, stream, nullptr)
-                             : run_fused<16, 6, 1, false>(up, down, ready, counters, num_sms, stream, nullptr);
+        return down.split_k == 2 ? run_fused<16, 6, 2, true, false>(up, down, ready, counters, num_sms, stream, mega)
+                                 : run_fused<16, 6, 1, true, false>(up, down, ready, counters, num_sms, stream, mega);
+    return down.split_k == 2 ? run_fused<16, 6, 2, false, false>(up, down, ready, counters, num_sms, stream, nullptr)
+                             : run_fused<16, 6, 1, false, false>(up, down, ready, counters, num_sms, stream, nullptr);
 }
 
-bool fused_mega_fits(int E, long long slots)
+bool fused_mega_fits(int E, long long slots, bool mxfp8)
 {
-    const long long budget = mega_table_budget<16, 6>();
+    const long long budget = mxfp8 ? mega_table_budget<16, 5, true>() : mega_table_budget<16, 6, false>();
     return budget >= 0 && mega_table_bytes(E, slots) <= budget;
 }
 

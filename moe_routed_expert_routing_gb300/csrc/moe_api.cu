@@ -77,7 +77,8 @@ moe_status_t check_problem(const moe_problem_t *p)
         return MOE_ERR_SHAPE;
     if (p->path < MOE_PATH_AUTO || p->path > MOE_PATH_TILED_1CTA)
         return MOE_ERR_SHAPE;
-    if (p->weight_layout != MOE_WEIGHTS_ROW_MAJOR && p->weight_layout != MOE_WEIGHTS_PACKED)
+    if (p->weight_layout != MOE_WEIGHTS_ROW_MAJOR && p->weight_layout != MOE_WEIGHTS_PACKED &&
+        p->weight_layout != MOE_WEIGHTS_MXFP8)
         return MOE_ERR_SHAPE;
     if (p->forward_form < MOE_FORWARD_AUTO || p->forward_form > MOE_FORWARD_ONE_KERNEL)
         return MOE_ERR_SHAPE;
@@ -165,7 +166,8 @@ moe_status_t record_stage(void *const *stage_events, int i, cudaStream_t s)
 // order-independent for two terms. Decided from static shapes only.
 bool down_split_k(const moe_problem_t &p, int path, int tile_rows, int sms)
 {
-    if (path != MOE_PATH_SMALL_M || tile_rows != 16 || (p.I / 64) % 2 != 0)
+    const int k_block = p.weight_layout == MOE_WEIGHTS_MXFP8 ? 128 : 64;   // K of one weight block
+    if (path != MOE_PATH_SMALL_M || tile_rows != 16 || (p.I / k_block) % 2 != 0)
         return false;
     const long long R_max = static_cast<long long>(p.T_max) * p.k;
     const long long max_experts = R_max < p.E ? R_max : p.E;
@@ -201,6 +203,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
     g.small_m = path == MOE_PATH_SMALL_M;
     g.cta_pair = path == MOE_PATH_TILED;
     g.w_packed = p.weight_layout == MOE_WEIGHTS_PACKED;
+    g.w_mxfp8 = p.weight_layout == MOE_WEIGHTS_MXFP8;
     g.tile_rows = tile_rows;
     g.split_k = 1;
     g.pdl = path == MOE_PATH_SMALL_M;
@@ -255,7 +258,22 @@ bool megakernel_possible(const moe_problem_t &p)
     int path = 0, tile_rows = 0;
     resolve(p, &path, &tile_rows);
     return path == MOE_PATH_SMALL_M && tile_rows == 16 &&
-           fused_mega_fits(p.E, static_cast<long long>(p.T_max) * p.k);
+           fused_mega_fits(p.E, static_cast<long long>(p.T_max) * p.k, p.weight_layout == MOE_WEIGHTS_MXFP8);
+}
+
+// Both GEMMs in one persistent kernel: 16-row token tiles, or any M-small
+// tile with MXFP8 weights (that kernel is their only GEMM).
+bool fused_mlp_of(const moe_problem_t &p, int path, int tile_rows)
+{
+    return path == MOE_PATH_SMALL_M && (tile_rows == 16 || p.weight_layout == MOE_WEIGHTS_MXFP8);
+}
+
+// MXFP8 weights are read by the M-small path only.
+moe_status_t check_layout_path(const moe_problem_t &p)
+{
+    int path = 0, tile_rows = 0;
+    resolve(p, &path, &tile_rows);
+    return (p.weight_layout == MOE_WEIGHTS_MXFP8 && path != MOE_PATH_SMALL_M) ? MOE_ERR_UNSUPPORTED : MOE_OK;
 }
 
 // moe_forward runs as one kernel: asked for, or (AUTO) where the down GEMM
@@ -287,7 +305,7 @@ int forward_launches(const moe_problem_t &p)
     const long long R = static_cast<long long>(p.T_max) * p.k;
     int n = R <= kDispatchSlotsPerBlock ? 1 : 3;            // dispatch
     n += path == MOE_PATH_SMALL_M ? 0 : 1;                  // row gather (fused into the M-small GEMM)
-    n += (path == MOE_PATH_SMALL_M && tile_rows == 16) ? 1 : 2;
+    n += fused_mlp_of(p, path, tile_rows) ? 1 : 2;
     return n + 1;                                           // combine
 }
 
@@ -362,7 +380,7 @@ moe_status_t moe_resolve_profile(const moe_problem_t *problem, moe_profile_t *pr
     const int sms = device_sm_count();
     if (sms <= 0)
         return MOE_ERR_CUDA;
-    if (check_form(*problem) != MOE_OK)
+    if (check_form(*problem) != MOE_OK || check_layout_path(*problem) != MOE_OK)
         return MOE_ERR_UNSUPPORTED;
     int path = 0, tile_rows = 0;
     resolve(*problem, &path, &tile_rows);
@@ -373,7 +391,7 @@ moe_status_t moe_resolve_profile(const moe_problem_t *problem, moe_profile_t *pr
     profile->pdl = use_pdl(*problem) ? 1 : 0;
     profile->fused_gather = path == MOE_PATH_SMALL_M ? 1 : 0;
     profile->cta_pair = path == MOE_PATH_TILED ? 1 : 0;
-    profile->fused_mlp = (path == MOE_PATH_SMALL_M && tile_rows == 16) ? 1 : 0;
+    profile->fused_mlp = fused_mlp_of(*problem, path, tile_rows) ? 1 : 0;
     profile->megakernel = use_megakernel(*problem) ? 1 : 0;
     profile->kernel_launches = forward_launches(*problem);
     return MOE_OK;
@@ -420,6 +438,8 @@ moe_status_t moe_expert_compute(const moe_problem_t *problem, const void *x_sort
         return MOE_ERR_NULL;
     if (!aligned16(x_sorted) || !aligned16(W13) || !aligned16(W2) || !aligned16(y_sorted))
         return MOE_ERR_ALIGN;
+    if (p.weight_layout == MOE_WEIGHTS_MXFP8)   // read by moe_forward's fused M-small kernel only
+        return MOE_ERR_UNSUPPORTED;
     if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK)
         return st;
     if ((st = check_device()) != MOE_OK)
@@ -462,7 +482,7 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
         return st;
     if ((st = check_device()) != MOE_OK)
         return st;
-    if ((st = check_form(p)) != MOE_OK)
+    if ((st = check_form(p)) != MOE_OK || (st = check_layout_path(p)) != MOE_OK)
         return st;
     const Layout L = layout_of(p);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -502,7 +522,7 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
     // every launch: the kernel clears them at its tail). Measured in one
     // process against two launches: -1.3% per decode step; +2% on 32-row
     // tiles, which keep two launches.
-    const bool fused_mlp = path == MOE_PATH_SMALL_M && tile_rows == 16;
+    const bool fused_mlp = fused_mlp_of(p, path, tile_rows);
     if ((st = mark(0)) != MOE_OK)
         return st;
     st = cuda_status(launch_dispatch(topk_ids, d_num_tokens, p.T_max, p.k, p.E, at<int32_t>(ws, L.block_counts),
@@ -568,6 +588,44 @@ moe_status_t moe_pack_weights(const moe_problem_t *problem, const void *W13, con
         return st;
     return cuda_status(launch_pack_weights(W13, W2, W13_packed, W2_packed, p.E, p.H, p.I, device_sm_count(),
                                            static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_weight_bytes(const moe_problem_t *problem, int32_t layout, size_t *w13_bytes, size_t *w2_bytes)
+{
+    if (!w13_bytes || !w2_bytes)
+        return MOE_ERR_NULL;
+    const moe_status_t st = check_problem(problem);
+    if (st != MOE_OK)
+        return st;
+    if (layout != MOE_WEIGHTS_ROW_MAJOR && layout != MOE_WEIGHTS_PACKED && layout != MOE_WEIGHTS_MXFP8)
+        return MOE_ERR_SHAPE;
+    const size_t n13 = static_cast<size_t>(problem->E) * 2 * problem->I * problem->H;
+    const size_t n2 = static_cast<size_t>(problem->E) * problem->H * problem->I;
+    if (layout == MOE_WEIGHTS_MXFP8) {
+        *w13_bytes = n13 + n13 / 32;
+        *w2_bytes = n2 + n2 / 32;
+    } else {
+        *w13_bytes = 2 * n13;
+        *w2_bytes = 2 * n2;
+    }
+    return MOE_OK;
+}
+
+moe_status_t moe_quantize_weights(const moe_problem_t *problem, const void *W13, const void *W2, void *W13_mx,
+                                  void *W2_mx, void *stream)
+{
+    moe_status_t st = check_problem(problem);
+    if (st != MOE_OK)
+        return st;
+    const moe_problem_t &p = *problem;
+    if (!W13 || !W2 || !W13_mx || !W2_mx)
+        return MOE_ERR_NULL;
+    if (!aligned16(W13) || !aligned16(W2) || !aligned16(W13_mx) || !aligned16(W2_mx))
+        return MOE_ERR_ALIGN;
+    if ((st = check_device()) != MOE_OK)
+        return st;
+    return cuda_status(launch_quantize_weights_mxfp8(W13, W2, W13_mx, W2_mx, p.E, p.H, p.I, device_sm_count(),
+                                                     static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_last_device_error(const void *ws, void *stream, int32_t *host_code)

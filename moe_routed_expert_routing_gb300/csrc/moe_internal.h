@@ -71,6 +71,13 @@ cudaError_t launch_combine(const float *y_sorted, const int32_t *inv, const floa
 cudaError_t launch_pack_weights(const void *W13, const void *W2, void *W13_packed, void *W2_packed, int E, int H,
                                 int I, int num_sms, cudaStream_t stream);
 
+// ---- MXFP8 weights (weights_mx.cu) ----
+// W13[E, 2I, H] and W2[E, H, I] bf16 -> the MOE_WEIGHTS_MXFP8 buffers: E4M3
+// codes (row-major), then the E8M0 scale codes in (128-row tile, 128-wide K
+// block, row, sub-block) order.
+cudaError_t launch_quantize_weights_mxfp8(const void *W13, const void *W2, void *W13_mx, void *W2_mx, int E, int H,
+                                          int I, int num_sms, cudaStream_t stream);
+
 // ---- expert GEMMs (grouped_gemm.cu) ----
 struct GemmProblem {
     const void *act;          // [act_rows, K] bf16: sorted rows, or x itself when gather is set
@@ -92,6 +99,7 @@ struct GemmProblem {
     bool pdl;                 // programmatic dependent launch
     bool cta_pair;            // tiled path on 2-CTA clusters (tcgen05 cta_group::2)
     bool w_packed;            // `w` is in the access-ordered PACKED layout
+    bool w_mxfp8;             // `w` is in the MXFP8 layout (codes, then scale blocks): fused kernel only
 };
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);
@@ -120,7 +128,7 @@ cudaError_t launch_fused_small(const GemmProblem &up, const GemmProblem &down, i
 
 // Whether the whole-forward kernel's shared-memory expert tables for E experts
 // and `slots` = T_max * k routed slots fit next to its pipeline on this device.
-bool fused_mega_fits(int E, long long slots);
+bool fused_mega_fits(int E, long long slots, bool mxfp8);
 
 // number of SMs of the current device (cached)
 int device_sm_count();

@@ -67,7 +67,7 @@ def test_workspace_size_and_path(lib):
 @pytest.mark.parametrize("bad,status", [
     (dict(T_max=0), 2), (dict(E=0), 2), (dict(E=1025), 2), (dict(k=0), 2), (dict(k=9, E=8), 2),
     (dict(H=300), 3), (dict(I=100), 3), (dict(capacity=5), 2), (dict(path=7), 2), (dict(path=-1), 2),
-    (dict(weight_layout=2), 2),
+    (dict(weight_layout=3), 2), (dict(forward_form=3), 2), (dict(forward_form=-1), 2),
 ])
 def test_problem_validation(lib, bad, status):
     args = dict(T_max=64, E=8, k=2, H=256, I=512, capacity=0, path=0, weight_layout=0)
@@ -104,3 +104,16 @@ def test_entry_points_fail_closed_without_touching_the_device(lib):
     assert so.moe_last_device_error(None, None, ctypes.byref(code)) == 1
     assert so.moe_pack_weights(P, fake, fake, None, fake, None) == 1
     assert so.moe_pack_weights(P, fake, fake, fake + 8, fake, None) == 3
+
+
+def test_weight_bytes_pure_host(lib):
+    """Weight buffer sizes per layout, without a device: bf16 (row-major or
+    packed) 2 bytes per element; MXFP8 1 byte per code plus 1 scale byte per 32."""
+    p = lib.Problem.make(8, 384, 6, 7168, 3072)
+    n13, n2 = 384 * 6144 * 7168, 384 * 7168 * 3072
+    assert lib.moe_weight_bytes(p, lib.MOE_WEIGHTS_ROW_MAJOR) == (2 * n13, 2 * n2)
+    assert lib.moe_weight_bytes(p, lib.MOE_WEIGHTS_PACKED) == (2 * n13, 2 * n2)
+    assert lib.moe_weight_bytes(p, lib.MOE_WEIGHTS_MXFP8) == (n13 + n13 // 32, n2 + n2 // 32)
+    with pytest.raises(lib.MoeError) as ei:
+        lib.moe_weight_bytes(p, 7)
+    assert ei.value.status == 2
