@@ -56,15 +56,17 @@ GRAPH_STEPS = 10
 # DRAM traffic of the dominant kernel from ncu captures of the decode T=8 shape
 # with E=24 (20 touched experts; dram__bytes_read.sum + dram__bytes_write.sum per
 # launch): the fused M-small kernel (both GEMMs; separate and one-kernel forms
-# alike) 2.6439 GB (profiles/fused_small_decode8_E24.md), the gate-up GEMM alone
-# 1.7647 GB (profiles/packed_weights_decode.md). Both read each touched
-# expert's weights exactly once, so a capture is scaled to a launch by its
-# touched experts. Keyed to the sha256 of the GEMM sources at capture time:
-# after any change, traffic reports null.
+# alike) 2.6439 GB with bf16 weights and 1.3638 GB with MXFP8 weights
+# (profiles/fused_small_decode8_E24.md, profiles/mxfp8_decode8_E24.md), the
+# gate-up GEMM alone 1.7647 GB (profiles/packed_weights_decode.md). Each reads
+# every touched expert's weights exactly once, so a capture is scaled to a
+# launch by its touched experts. Keyed to the sha256 of the GEMM sources at
+# capture time: after any change, traffic reports null.
 NCU_TRAFFIC = {
-    "kernel_sha256": "ffe54f89261158667c5696bbaf227efb8ff9f85cc001733a966de17dbafba6b9",
+    "kernel_sha256": "bc2c6f893b0e03bd34501bb3c527590e1134b87e3a6d1aeaad58e7fbfd3736d6",
     "small_m_gate_up_bytes_per_touched_expert": 1.7647e9 / 20,
     "small_m_fused_bytes_per_touched_expert": 2.6439e9 / 20,
+    "small_m_fused_mxfp8_bytes_per_touched_expert": 1.3638e9 / 20,
 }
 
 
@@ -428,8 +430,9 @@ def run_ours(args, world, rank, local):
                       if fused else "grouped_gemm_kernel (gate-up, SiLU*up epilogue)")
     roof["algorithmic_per_step"] = g1_flops if roof["bound"] == "tensor" else g1_bytes
     traffic = None
-    key = "small_m_fused_bytes_per_touched_expert" if fused else "small_m_gate_up_bytes_per_touched_expert"
-    if (NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and key in NCU_TRAFFIC and args.weights == "bf16"
+    key = ("small_m_fused_mxfp8_bytes_per_touched_expert" if args.weights == "mxfp8" else
+           "small_m_fused_bytes_per_touched_expert" if fused else "small_m_gate_up_bytes_per_touched_expert")
+    if (NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and key in NCU_TRAFFIC
             and all(d["path"][0] == 2 for d in inputs)):
         per = [d["acct"]["touched_experts"] * NCU_TRAFFIC[key] for d in inputs]
         traffic = float(sum(per)) / len(per)
