@@ -107,7 +107,9 @@ struct Cfg {
     static constexpr int kAccCols = kSmallM ? (kGated ? 2 * kTileRows : kTileRows) : 256;
     static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);
     static constexpr uint32_t kIdesc = kSmallM ? idesc_bf16_f32(128, kTileRows) : idesc_bf16_f32(128, 256);
-    static constexpr int kDynSmem = 1024 + kStages * kStageBytes;
+    // fp32 output (tiled down GEMM): a 32 x 36-float transpose scratch per epilogue warp
+    static constexpr int kEpiScratch = (!kSmallM && !kGated) ? 4 * 32 * 36 * 4 : 0;
+    static constexpr int kDynSmem = 1024 + kStages * kStageBytes + kEpiScratch;
     static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0, "tiles must keep 1024-byte alignment");
     static_assert(kTmemCols <= 512, "TMEM has 512 columns");
     static_assert(!kSmallM || (kTileRows % 16 == 0 && kTileRows >= 16 && kTileRows <= 256), "MMA N");
@@ -198,10 +200,15 @@ __device__ __forceinline__ void build_tile_prefix(const int *s_off, int *s_tp, i
 }
 
 // Epilogue of a 128-row tiled unit: this thread owns accumulator row `row`
-// (TMEM lane base already in t_row). Gate-up: columns [0,128) gate, [128,256)
-// up -> bf16 SiLU(gate)*up into h; down: 256 fp32 columns into y.
+// (TMEM lane base already in t_row); the warp's 32 rows are consecutive.
+// Gate-up: columns [0,128) gate, [128,256) up -> bf16 SiLU(gate)*up into h.
+// Down: 256 fp32 columns into y, 32 at a time, turned through the warp's
+// 32 x 36-float shared-memory scratch so that each store instruction writes
+// four whole 128-byte row segments (a thread-per-row store would write 32
+// rows x 16 bytes: 32 partial lines per instruction).
 template <bool kGated>
-__device__ __forceinline__ void tiled_epilogue(uint32_t t_row, const GemmArgs &args, int row, bool valid, int n0)
+__device__ __forceinline__ void tiled_epilogue(uint32_t t_row, const GemmArgs &args, int row, bool valid, int n0,
+                                               float *scratch)
 {
     if (kGated) {
         __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(args.out) + static_cast<size_t>(row) * args.n_out + n0;
@@ -229,18 +236,31 @@ __device__ __forceinline__ void tiled_epilogue(uint32_t t_row, const GemmArgs &a
             }
         }
     } else {
-        float *orow = static_cast<float *>(args.out) + static_cast<size_t>(row) * args.n_out + n0;
+        const int lane = threadIdx.x & 31;
+        const int row0 = row - lane;                       // the warp's first row
+        const unsigned valid_rows = __ballot_sync(0xffffffffu, valid);
+        float4 *const mine = reinterpret_cast<float4 *>(scratch + lane * 36);
+        float *const y = static_cast<float *>(args.out);
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
             uint32_t d[32];
             tmem_ld_32x32b_x32(t_row + c, d);
             tmem_wait_ld();
-            if (valid) {
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    dst[i] = make_uint4(d[4 * i + 0], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
+            for (int i = 0; i < 8; ++i)
+                mine[i] = make_float4(__uint_as_float(d[4 * i]), __uint_as_float(d[4 * i + 1]),
+                                      __uint_as_float(d[4 * i + 2]), __uint_as_float(d[4 * i + 3]));
+            __syncwarp();
+            // lanes 8m..8m+7 take row 4*it + m, 16 bytes each: 128 contiguous bytes per row
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int rr = 4 * it + (lane >> 3);
+                const float4 v = *reinterpret_cast<const float4 *>(scratch + rr * 36 + (lane & 7) * 4);
+                if ((valid_rows >> rr) & 1u)
+                    *reinterpret_cast<float4 *>(y + static_cast<size_t>(row0 + rr) * args.n_out + n0 + c +
+                                                (lane & 7) * 4) = v;
             }
+            __syncwarp();
         }
     }
 }
@@ -450,7 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!kSmallM) {
                 const int r = q * 32 + lane;
                 const int row = t.row0 + r;
-                tiled_epilogue<kGated>(t_row, args, row, r < t.rows && row >= 0 && row < args.cap, t.n0);
+                tiled_epilogue<kGated>(t_row, args, row, r < t.rows && row >= 0 && row < args.cap, t.n0,
+                                       reinterpret_cast<float *>(smem + kStages * C::kStageBytes) + q * 32 * 36);
             } else {
                 // lane = weight row = output column t.n0 + 32q + lane; TMEM column = token row of the tile
                 const int col = t.n0 + q * 32 + lane;
@@ -1225,7 +1246,8 @@ struct PairCfg {
     static constexpr int kAccCols = 256;
     static constexpr int kTmemCols = 512;
     static constexpr uint32_t kIdesc = idesc_bf16_f32(256, 256);
-    static constexpr int kDynSmem = 1024 + kStages * kStageBytes;
+    static constexpr int kEpiScratch = kGated ? 0 : 4 * 32 * 36 * 4;   // fp32 output: transpose scratch
+    static constexpr int kDynSmem = 1024 + kStages * kStageBytes + kEpiScratch;
 };
 
 template <bool kGated, int kStages>
@@ -1388,7 +1410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t t_row = tmem_base + buf * C::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
             const int r = 128 * static_cast<int>(rank) + q * 32 + lane;   // row within the 256-row pair tile
             const int row = t.row0 + r;
-            tiled_epilogue<kGated>(t_row, args, row, r < t.rows && row >= 0 && row < args.cap, t.n0);
+            tiled_epilogue<kGated>(t_row, args, row, r < t.rows && row >= 0 && row < args.cap, t.n0,
+                                   reinterpret_cast<float *>(smem + kStages * C::kStageBytes) + q * 32 * 36);
             tc_fence_before();
             __syncwarp();
             if (lane == 0)

@@ -140,3 +140,58 @@ def test_mxfp8_refused_outside_the_m_small_path(B):
     with pytest.raises(B.MoeError) as ei:
         B.moe_expert_compute(q, bufs.x_sorted, bufs.expert_offsets, W, W, bufs.y_sorted, bufs.ws)
     assert ei.value.status == 5
+
+
+def test_mxfp8_degenerate_routing_and_graph_replay(B):
+    """MXFP8 weights under the edge cases of the method: a repeated expert in
+    one token, dropped (-1) and out-of-range ids, and a device token count
+    replayed from one captured graph with T in {12, 5, 1, 0} (rows >= T
+    untouched); every replay against an eager call (bit for bit) and the
+    oracle on the dequantized weights."""
+    T, E, k, H, I = 12, 64, 4, 512, 256
+    wl = wlm.custom("mxedge", T, E, k, H, I, seed=91)
+    x = wlm.make_x(wl, "cuda")
+    W13, W2 = wlm.make_weights(wl, "cuda")
+    ids_np, w_np = wlm.make_routing(wl)
+    ids_np[0] = [7, 7, 1, 2]
+    ids_np[1] = [-1, 3, -1, 4]
+    ids_np[2] = [5, 99, 6, 0]
+    ids, w = torch.from_numpy(ids_np).cuda(), torch.from_numpy(w_np).cuda()
+    for form in (1, 2):
+        p = B.Problem.make(T, E, k, H, I, weight_layout=B.MOE_WEIGHTS_MXFP8, forward_form=form)
+        W13_mx, W2_mx, (q13, s13), (q2, s2) = quantized(B, p, W13, W2)
+        W13_d = oracle.mx_dequantize(q13, s13).view(np.uint16).reshape(W13.shape)
+        W2_d = oracle.mx_dequantize(q2, s2).view(np.uint16).reshape(W2.shape)
+        bufs = B.Buffers(p)
+        d_T = torch.tensor([T], dtype=torch.int32, device="cuda")
+        B.moe_forward(p, x, ids, w, W13_mx, W2_mx, bufs.expert_offsets, bufs.perm, bufs.out, bufs.ws,
+                      d_num_tokens=d_T)
+        torch.cuda.synchronize()
+        assert B.moe_last_device_error(bufs.ws) & B.MOE_DEVERR_BAD_EXPERT_ID
+        B.moe_clear_device_error(bufs.ws)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                B.moe_forward(p, x, ids, w, W13_mx, W2_mx, bufs.expert_offsets, bufs.perm, bufs.out, bufs.ws,
+                              d_num_tokens=d_T, stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        for T_dev in (12, 5, 1, 0):
+            d_T.fill_(T_dev)
+            bufs.out.fill_(4.0)
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.all(bufs.out[T_dev:] == 4.0)
+            valid = int(np.count_nonzero((ids_np[:T_dev] >= 0) & (ids_np[:T_dev] < E)))
+            assert int(bufs.expert_offsets[-1]) == valid
+            if T_dev == 0:
+                continue
+            eager = B.Buffers(p)
+            B.moe_forward(p, x, ids, w, W13_mx, W2_mx, eager.expert_offsets, eager.perm, eager.out, eager.ws,
+                          d_num_tokens=d_T)
+            torch.cuda.synchronize()
+            assert torch.equal(bufs.out[:T_dev].view(torch.int16), eager.out[:T_dev].view(torch.int16))
+            ref_acc, _, bad = oracle.moe_tokens(wlm.bf16_bits(x), ids_np, w_np, W13_d, W2_d,
+                                                tokens=np.arange(T_dev, dtype=np.int32))
+            assert_within_tolerance(wlm.bf16_bits(bufs.out[:T_dev]), ref_acc, f"mxfp8 edge form {form} T={T_dev}")
