@@ -65,6 +65,8 @@ typedef enum moe_status {
 /* Bits of the device error word (moe_last_device_error). */
 #define MOE_DEVERR_BAD_EXPERT_ID 0x1 /* an id outside [0, E) and not -1: slot dropped */
 #define MOE_DEVERR_WAIT_TIMEOUT 0x2  /* a pipeline wait gave up: results of that call are invalid */
+#define MOE_DEVERR_Y_RANGE 0x4       /* moe_forward, tiled paths: a down-GEMM output beyond the fp16
+                                        range of its intermediate y was clipped to +-65504 */
 
 /* Expert-GEMM path. AUTO picks from the static shape, a = T_max*k/E routed
  * rows per expert on average: M-small for a <= 16, single-CTA tiles for
@@ -229,7 +231,12 @@ moe_status_t moe_combine(const moe_problem_t *problem, const float *y_sorted, co
  * The whole routed expert execution in one call: dispatch (with the row
  * gather) -> expert compute -> combine, all on `stream`, with the sorted
  * batches and inv held in the workspace. Arguments as above; perm and
- * expert_offsets are still returned to the caller. For decode-size batches
+ * expert_offsets are still returned to the caller. On the tiled paths
+ * (prefill- and large-batch shapes) the intermediate y between the down GEMM
+ * and the combine is kept in fp16 (round to nearest, saturating at +-65504:
+ * a clipped value sets MOE_DEVERR_Y_RANGE), which halves its HBM traffic;
+ * the separate moe_expert_compute / moe_combine keep y in fp32. Decode-size
+ * batches keep y in fp32. For decode-size batches
  * (moe_profile_t.megakernel) the call is a single persistent kernel: every
  * CTA dispatches the call's slots itself, then runs its share of both GEMMs
  * and of the combine; its CTAs wait on one another (bounded), so it expects

@@ -28,6 +28,7 @@ MOE_FORWARD_SEPARATE = 1
 MOE_FORWARD_ONE_KERNEL = 2
 MOE_DEVERR_BAD_EXPERT_ID = 0x1
 MOE_DEVERR_WAIT_TIMEOUT = 0x2
+MOE_DEVERR_Y_RANGE = 0x4
 
 #: every symbol include/moe.h declares
 EXPORTED_SYMBOLS = (

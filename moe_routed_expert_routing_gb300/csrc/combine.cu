@@ -7,13 +7,15 @@
 //
 //   out[t, m] = bf16( sum_{j = 0..k-1} w[t, j] * y_sorted[inv[t*k + j], m] )
 //
-// y_sorted is the fp32 output of the down GEMM. fp32 products and sums in
+// y_sorted is the down GEMM's output: fp32, or fp16 on moe_forward's tiled
+// paths (widened exactly before use). fp32 products and sums in
 // ascending j (no fused multiply-add), one rounding at the end: the result
 // is deterministic (no atomics) and identical to a plain sequential loop.
 // Work item = one token x 1024 columns, so even a single token spreads over
 // several SMs; each thread owns 8 consecutive columns, read as two 16-byte
 // loads per routed row and written as one 16-byte store.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "moe_internal.h"
 
@@ -30,7 +32,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 constexpr int kCombineThreads = 128;
 constexpr int kColsPerItem = kCombineThreads * 8;   // one work item = one token x 1024 columns
 
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float4 *__restrict__ y_sorted,
+// Eight consecutive columns of one y row as fp32: two 16-byte loads (fp32 y)
+// or one (fp16 y, widened exactly).
+__device__ __forceinline__ void load8(const float *y, size_t i, float (&f)[8])
+{
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(y + i));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(y + i) + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__device__ __forceinline__ void load8(const __half *y, size_t i, float (&f)[8])
+{
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(y + i));
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 p = __half22float2(*reinterpret_cast<const __half2 *>(&u[q]));
+        f[2 * q] = p.x;
+        f[2 * q + 1] = p.y;
+    }
+}
+
+template <typename Y>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Y *__restrict__ y_sorted,
                                                                   const int32_t *__restrict__ inv,
                                                                   const float *__restrict__ w,
                                                                   const int32_t *d_num_tokens, int T_max, int k,
@@ -56,7 +81,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float4 *
         // loads of up to four routed rows are issued together, then summed in
         // ascending j, so the sum is the same sequence of roundings as a plain loop
         for (int j0 = 0; j0 < k; j0 += 4) {
-            float4 a[4], b[4];
+            float f[4][8];
             int row[4];
             float wj[4];
 #pragma unroll
@@ -65,21 +90,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float4 *
                 wj[q] = (j0 + q < k) ? __ldg(w_t + j0 + q) : 0.f;
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (row[q] >= 0) {
-                    const float4 *src = y_sorted + (static_cast<size_t>(row[q]) * vec_per_row + c) * 2;
-                    a[q] = __ldg(src);
-                    b[q] = __ldg(src + 1);
-                }
-            }
+            for (int q = 0; q < 4; ++q)
+                if (row[q] >= 0)
+                    load8(y_sorted, (static_cast<size_t>(row[q]) * vec_per_row + c) * 8, f[q]);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (row[q] < 0)
                     continue;
-                const float f[8] = {a[q].x, a[q].y, a[q].z, a[q].w, b[q].x, b[q].y, b[q].z, b[q].w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    acc[i] = __fadd_rn(acc[i], __fmul_rn(wj[q], f[i]));
+                    acc[i] = __fadd_rn(acc[i], __fmul_rn(wj[q], f[q][i]));
             }
         }
         uint4 o;
@@ -93,7 +113,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float4 *
 
 }  // namespace
 
-cudaError_t launch_combine(const float *y_sorted, const int32_t *inv, const float *topk_weights,
+cudaError_t launch_combine(const void *y_sorted, bool y_f16, const int32_t *inv, const float *topk_weights,
                            const int32_t *d_num_tokens, int T_max, int k, int H, void *out, int num_sms,
                            cudaStream_t stream, bool pdl)
 {
@@ -102,8 +122,12 @@ cudaError_t launch_combine(const float *y_sorted, const int32_t *inv, const floa
     int blocks = static_cast<int>(items < num_sms * 16LL ? items : num_sms * 16LL);
     if (blocks < 1)
         blocks = 1;
-    return launch_k(combine_kernel, dim3(blocks), dim3(kCombineThreads), 0, stream, pdl,
-                    reinterpret_cast<const float4 *>(y_sorted), inv, topk_weights, d_num_tokens, T_max, k, H / 8,
+    if (y_f16)
+        return launch_k(combine_kernel<__half>, dim3(blocks), dim3(kCombineThreads), 0, stream, pdl,
+                        static_cast<const __half *>(y_sorted), inv, topk_weights, d_num_tokens, T_max, k, H / 8,
+                        static_cast<uint4 *>(out));
+    return launch_k(combine_kernel<float>, dim3(blocks), dim3(kCombineThreads), 0, stream, pdl,
+                    static_cast<const float *>(y_sorted), inv, topk_weights, d_num_tokens, T_max, k, H / 8,
                     static_cast<uint4 *>(out));
 }
 

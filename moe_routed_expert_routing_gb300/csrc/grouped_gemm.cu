@@ -66,6 +66,7 @@ struct GemmArgs {
     int w_rows_per_expert;
     int up_row_offset;
     int w_packed;       // weights in the PACKED layout (see include/moe.h)
+    int out_f16;        // tiled down GEMM: y stored as fp16 (saturated at +-65504) instead of fp32
 };
 
 // TMA coordinates {column, row} of the 128-row weight tile starting at
@@ -235,6 +236,45 @@ __device__ __forceinline__ void tiled_epilogue(uint32_t t_row, const GemmArgs &a
                 }
             }
         }
+    } else if (args.out_f16) {
+        // fp16 y: 64 columns per pass, so that each row's piece is one 128-byte line
+        const int lane = threadIdx.x & 31;
+        const int row0 = row - lane;
+        const unsigned valid_rows = __ballot_sync(0xffffffffu, valid);
+        uint4 *const mine = reinterpret_cast<uint4 *>(scratch + lane * 36);
+        __half *const y = static_cast<__half *>(args.out);
+        bool clipped = false;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 64) {
+            uint32_t d[64];
+            tmem_ld_32x32b_x32(t_row + c, *reinterpret_cast<uint32_t(*)[32]>(d));
+            tmem_ld_32x32b_x32(t_row + c + 32, *reinterpret_cast<uint32_t(*)[32]>(d + 32));
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint32_t h[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float lo = __uint_as_float(d[8 * i + 2 * j]), hi = __uint_as_float(d[8 * i + 2 * j + 1]);
+                    clipped |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+                    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h[j]) : "f"(hi), "f"(lo));
+                }
+                mine[i] = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+            __syncwarp();
+            // lanes 8m..8m+7 take row 4*it + m, 16 bytes each: one whole 128-byte line per row
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int rr = 4 * it + (lane >> 3);
+                const uint4 v = *reinterpret_cast<const uint4 *>(scratch + rr * 36 + (lane & 7) * 4);
+                if ((valid_rows >> rr) & 1u)
+                    *reinterpret_cast<uint4 *>(y + static_cast<size_t>(row0 + rr) * args.n_out + n0 + c +
+                                               (lane & 7) * 8) = v;
+            }
+            __syncwarp();
+        }
+        if (__any_sync(0xffffffffu, clipped && valid) && lane == 0)
+            atomicOr(args.err, MOE_DEVERR_Y_RANGE);
     } else {
         const int lane = threadIdx.x & 31;
         const int row0 = row - lane;                       // the warp's first row
@@ -1518,6 +1558,7 @@ cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
     a.w_rows_per_expert = p.w_rows_per_expert;
     a.up_row_offset = p.up_row_offset;
     a.w_packed = p.w_packed ? 1 : 0;
+    a.out_f16 = p.out_f16 ? 1 : 0;
     // Upper bound of the units any routing can produce; no more CTAs than that.
     const long long max_row_tiles = (static_cast<long long>(p.cap) + kTileRows - 1) / kTileRows + p.E;
     const long long max_units = max_row_tiles * (p.n_out / C::kOutCols) * kSplitK;
@@ -1578,6 +1619,7 @@ cudaError_t run_pair(const GemmProblem &p, int num_sms, cudaStream_t stream)
     a.w_rows_per_expert = p.w_rows_per_expert;
     a.up_row_offset = p.up_row_offset;
     a.w_packed = p.w_packed ? 1 : 0;
+    a.out_f16 = p.out_f16 ? 1 : 0;
     const long long max_units = ((static_cast<long long>(p.cap) + 255) / 256 + p.E) * (p.n_out / C::kOutCols);
     long long clusters = max_units < max_clusters ? max_units : max_clusters;
     if (clusters < 1)
@@ -1603,6 +1645,7 @@ GemmArgs make_args(const GemmProblem &p)
     a.w_rows_per_expert = p.w_rows_per_expert;
     a.up_row_offset = p.up_row_offset;
     a.w_packed = p.w_packed ? 1 : 0;
+    a.out_f16 = 0;
     return a;
 }
 
@@ -1722,6 +1765,8 @@ cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *r
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream)
 {
     if (p.w_mxfp8)   // MXFP8 weights run through the fused M-small kernel only
+        return cudaErrorInvalidValue;
+    if (p.out_f16 && (p.small_m || p.gated))   // fp16 y: tiled down GEMM only
         return cudaErrorInvalidValue;
     if (p.split_k != 1 && (p.split_k != 2 || !p.small_m || p.gated || p.tile_rows != 16 || (p.K / kBK) % 2 != 0))
         return cudaErrorInvalidValue;

@@ -183,7 +183,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
                                     const void *W13, const void *W2, float *y_sorted, void *ws, cudaStream_t s,
                                     void *const *stage_events = nullptr, bool y_zeroed = false,
                                     const int32_t *gather_perm = nullptr, bool fused = false,
-                                    const MegaParams *mega = nullptr)
+                                    const MegaParams *mega = nullptr, bool y_f16 = false)
 {
     const Layout L = layout_of(p);
     int path = 0, tile_rows = 0;
@@ -204,6 +204,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
     g.cta_pair = path == MOE_PATH_TILED;
     g.w_packed = p.weight_layout == MOE_WEIGHTS_PACKED;
     g.w_mxfp8 = p.weight_layout == MOE_WEIGHTS_MXFP8;
+    g.out_f16 = false;
     g.tile_rows = tile_rows;
     g.split_k = 1;
     g.pdl = path == MOE_PATH_SMALL_M;
@@ -229,7 +230,8 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
         if ((st = record_stage(stage_events, 3, s)) != MOE_OK)
             return st;
     }
-    // down: h[cap, I] x W2[E, H, I] -> y_sorted[cap, H] (fp32)
+    // down: h[cap, I] x W2[E, H, I] -> y_sorted[cap, H] (fp32, or fp16 for moe_forward's tiled paths)
+    g.out_f16 = y_f16;
     g.act = at<void>(ws, L.h);
     g.gather = false;
     g.perm = nullptr;
@@ -461,7 +463,7 @@ moe_status_t moe_combine(const moe_problem_t *problem, const float *y_sorted, co
         return MOE_ERR_ALIGN;
     if ((st = check_device()) != MOE_OK)
         return st;
-    return cuda_status(launch_combine(y_sorted, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out,
+    return cuda_status(launch_combine(y_sorted, false, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out,
                                       device_sm_count(), static_cast<cudaStream_t>(stream), use_pdl(p)));
 }
 
@@ -540,12 +542,16 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
                                             use_pdl(p)));
     if (st != MOE_OK || (st = mark(2)) != MOE_OK)
         return st;
+    // tiled paths: y between the down GEMM and the combine in fp16 (half the
+    // bytes of the largest intermediate; within the output tolerance). The
+    // M-small path keeps fp32 (its y is small).
+    const bool y_f16 = path != MOE_PATH_SMALL_M;
     st = enqueue_expert_compute(p, fused_gather ? x : x_sorted, expert_offsets, W13, W2, y_sorted, ws, s,
-                                stage_events, true, fused_gather ? perm : nullptr, fused_mlp);
+                                stage_events, true, fused_gather ? perm : nullptr, fused_mlp, nullptr, y_f16);
     if (st != MOE_OK || (st = mark(4)) != MOE_OK)
         return st;
-    st = cuda_status(
-        launch_combine(y_sorted, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out, sms, s, use_pdl(p)));
+    st = cuda_status(launch_combine(y_sorted, y_f16, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out, sms,
+                                    s, use_pdl(p)));
     if (st != MOE_OK)
         return st;
     return mark(5);

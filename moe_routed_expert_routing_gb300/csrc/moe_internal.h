@@ -63,7 +63,8 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *perm, const int32_t
                                int H, int cap, void *x_sorted, int num_sms, cudaStream_t stream, bool pdl);
 
 // ---- combine (combine.cu) ----
-cudaError_t launch_combine(const float *y_sorted, const int32_t *inv, const float *topk_weights,
+// y_sorted is fp32, or fp16 when y_f16 is set (moe_forward's tiled paths).
+cudaError_t launch_combine(const void *y_sorted, bool y_f16, const int32_t *inv, const float *topk_weights,
                            const int32_t *d_num_tokens, int T_max, int k, int H, void *out, int num_sms,
                            cudaStream_t stream, bool pdl);
 
@@ -100,6 +101,7 @@ struct GemmProblem {
     bool cta_pair;            // tiled path on 2-CTA clusters (tcgen05 cta_group::2)
     bool w_packed;            // `w` is in the access-ordered PACKED layout
     bool w_mxfp8;             // `w` is in the MXFP8 layout (codes, then scale blocks): fused kernel only
+    bool out_f16;             // tiled down GEMM: y as fp16 (saturated; MOE_DEVERR_Y_RANGE if clipped)
 };
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);

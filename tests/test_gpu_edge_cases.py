@@ -124,3 +124,21 @@ def test_smallest_sizes_and_wide_topk(B, path):
     bufs = run_forward(B, p, x, ids_np, w_np, W13, W2)
     ref, _ = oracle_ref(x, ids_np, w_np, W13, W2)
     assert_within_tolerance(wlm.bf16_bits(bufs.out), ref, f"H=256 I=128 k=16 path {path}")
+
+
+def test_fp16_intermediate_y_range_is_reported(B):
+    """moe_forward's tiled paths keep y in fp16: a down-GEMM output beyond
+    +-65504 is clipped and MOE_DEVERR_Y_RANGE is set; in range, no flag."""
+    T, E, k, H, I = 512, 8, 2, 256, 256          # a = 128 rows per expert: single-CTA tiles
+    wl = wlm.custom("yrange", T, E, k, H, I, seed=13)
+    ids_np, w_np = wlm.make_routing(wl)
+    x = torch.ones((T, H), dtype=torch.bfloat16, device="cuda")
+    W13 = torch.full((E, 2 * I, H), 0.01, dtype=torch.bfloat16, device="cuda")
+    p = B.Problem.make(T, E, k, H, I)
+    assert B.moe_resolve_path(p)[0] != 2
+    for scale, flagged in [(1.0, False), (100.0, True)]:   # y ~ 256 * 6.1 * scale: 1.6e3 or 1.6e5
+        W2 = torch.full((E, H, I), scale, dtype=torch.bfloat16, device="cuda")
+        bufs = run_forward(B, p, x, ids_np, w_np, W13, W2)
+        err = B.moe_last_device_error(bufs.ws)
+        assert bool(err & B.MOE_DEVERR_Y_RANGE) == flagged, err
+        assert torch.isfinite(bufs.out[:T].float()).all()
