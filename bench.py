@@ -63,7 +63,7 @@ GRAPH_STEPS = 10
 # launch by its touched experts. Keyed to the sha256 of the GEMM sources at
 # capture time: after any change, traffic reports null.
 NCU_TRAFFIC = {
-    "kernel_sha256": "bc2c6f893b0e03bd34501bb3c527590e1134b87e3a6d1aeaad58e7fbfd3736d6",
+    "kernel_sha256": "973ace43042a3f2903d632124a158a2e1ef4d55eb778b634fe9f7f142dc0c44c",
     "small_m_gate_up_bytes_per_touched_expert": 1.7647e9 / 20,
     "small_m_fused_bytes_per_touched_expert": 2.6439e9 / 20,
     "small_m_fused_mxfp8_bytes_per_touched_expert": 1.3638e9 / 20,
