@@ -61,6 +61,10 @@ def test_call_accounting():
     assert a["gemm1_flops"] == 4 * 7 * 256 * 128
     assert a["bytes"] == 4 * 6 * 256 * 128 + 2 * 4 * 256 * 2 + 8 * 7
     assert a["gemm1_bytes"] == 4 * 4 * 128 * 256 + 2 * 7 * 256 + 2 * 7 * 128
+    # MXFP8 weights: one code byte per element plus one scale byte per 32
+    m = bench.call_accounting(wl, ids, weight_bytes=33 / 32)
+    assert m["bytes"] == 4 * 3 * (33 / 32) * 256 * 128 + 2 * 4 * 256 * 2 + 8 * 7
+    assert m["flops"] == a["flops"]
 
 
 def test_defaults():
