@@ -298,3 +298,38 @@ def test_megakernel_dropped_invalid_and_repeated_slots(B):
     tokens = np.arange(10, dtype=np.int32)
     ref_acc, _ = dw.oracle_out(tokens, ids_np=ids_np, w_np=w_np)
     assert_within_tolerance(wlm.bf16_bits(bufs.out[:10]), ref_acc, "megakernel degenerate routing")
+
+
+def test_prefill_graph_replay_device_token_counts(B):
+    """Prefill shape captured once as a CUDA graph at T_max = 2048 (static
+    capacity T_max*k), replayed with device T in {2048, 1024, 1}: each replay
+    equals an eager call bit for bit, leaves rows >= T untouched, and matches
+    the oracle on sampled tokens."""
+    wl = wlm.WORKLOADS["prefill"]
+    dw = DeviceWorkload(wl)
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
+    bufs = B.Buffers(p)
+    d_T = torch.tensor([wl.T], dtype=torch.int32, device="cuda")
+    forward(B, p, dw, bufs, d_T=d_T)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            B.moe_forward(p, dw.x, dw.ids, dw.w, dw.W13, dw.W2, bufs.expert_offsets, bufs.perm, bufs.out, bufs.ws,
+                          d_num_tokens=d_T, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    eager = B.Buffers(p)
+    for T_dev in (2048, 1024, 1):
+        d_T.fill_(T_dev)
+        bufs.out.fill_(2.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert B.moe_last_device_error(bufs.ws) == 0
+        assert int(bufs.expert_offsets[-1]) == T_dev * wl.k
+        assert torch.all(bufs.out[T_dev:] == 2.0)
+        forward(B, p, dw, eager, d_T=d_T)
+        assert torch.equal(bufs.out[:T_dev].view(torch.int16), eager.out[:T_dev].view(torch.int16))
+        tokens = np.sort(np.random.default_rng(T_dev + 7).choice(T_dev, min(T_dev, 32), replace=False)).astype(np.int32)
+        ref_acc, _ = dw.oracle_out(tokens, ids_np=dw.ids_np[:T_dev], w_np=dw.w_np[:T_dev])
+        assert_within_tolerance(wlm.bf16_bits(bufs.out)[tokens], ref_acc, f"prefill graph T={T_dev}")
