@@ -233,20 +233,29 @@ def time_oracle(inputs, seconds: float, tokens_cap: int | None = None) -> dict:
         samples.append(dict(wl=wl, tok=tok, ids=ids, w=d["w_np"], x=x_bits, host_w=host_w,
                             flops=6.0 * int(np.count_nonzero(ids[tok] >= 0)) * wl.H * wl.I))
     t0 = time.perf_counter()
+    for s in samples:
+        s["t"] = 0.0
     while True:
         for s in samples:
             ts = time.perf_counter()
             oracle.moe_forward_streamed(s["x"], s["ids"], s["w"], lambda e, hw=s["host_w"]: hw[e], s["wl"].E,
                                         s["tok"])
-            t_total += time.perf_counter() - ts
+            dt = time.perf_counter() - ts
+            s["t"] += dt
+            t_total += dt
             flops_done += s["flops"]
         runs += 1
         if time.perf_counter() - t0 >= seconds:
             break
     sample_desc = "; ".join(f"{s['wl'].name}: {s['tok'].size}/{s['wl'].T} tokens" for s in samples)
+    # per call at the full token count, scaled from the sample by tokens (the
+    # oracle's work is per token): extrapolated, not measured at full size
+    us_full = {s["wl"].name: s["t"] / runs * s["wl"].T / s["tok"].size * 1e6 for s in samples}
     return {"value": flops_done / t_total / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{sample_desc}; repeated {runs}x ({t_total:.1f} s of oracle time)",
-            "seconds": t_total, "flops": flops_done}
+            "seconds": t_total, "flops": flops_done,
+            "us_per_call_extrapolated": us_full,
+            "us_per_call_note": "extrapolated from the token sample to the full T"}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -693,10 +702,13 @@ def run_reference(args, world, rank, local):
     for _ in range(args.warmup):
         time_oracle(inputs, 0.0, tokens_cap=tokens)
     flops, secs = 0.0, 0.0
+    us_full = {}
     for _ in range(args.steps):
         r = time_oracle(inputs, 0.0, tokens_cap=tokens)
         flops += r["flops"]
         secs += r["seconds"]
+        for name, us in r["us_per_call_extrapolated"].items():
+            us_full[name] = us_full.get(name, 0.0) + us / args.steps
     value = flops / secs / 1e12
     full_flops = sum(d["acct"]["flops"] for d in inputs)
     ms_per_step = full_flops / (value * 1e12) * 1e3
@@ -709,7 +721,8 @@ def run_reference(args, world, rank, local):
         "config": {"workload": " + ".join(d["wl"].describe() for d in inputs),
                    "note": "ms_per_step extrapolated to the full step from the oracle's FLOP rate"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
-                         "sample": f"{tokens} token(s) of each batch per step ({r['sample']})"},
+                         "sample": f"each step, at most {tokens} token(s) of each batch ({r['sample']})",
+                         "us_per_call_extrapolated": us_full, "us_per_call_note": r["us_per_call_note"]},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
