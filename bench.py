@@ -53,20 +53,22 @@ WORKLOAD_SETS = {
 STAGES = ["dispatch", "gather", "gemm_gate_up", "gemm_down", "combine"]
 GRAPH_STEPS = 10
 
-# DRAM traffic of the dominant kernel from ncu captures of the decode T=8 shape
-# with E=24 (20 touched experts; dram__bytes_read.sum + dram__bytes_write.sum per
-# launch): the fused M-small kernel (both GEMMs; separate and one-kernel forms
-# alike) 2.6439 GB with bf16 weights and 1.3638 GB with MXFP8 weights
-# (profiles/fused_small_decode8_E24.md, profiles/mxfp8_decode8_E24.md), the
-# gate-up GEMM alone 1.7647 GB (profiles/packed_weights_decode.md). Each reads
-# every touched expert's weights exactly once, so a capture is scaled to a
-# launch by its touched experts. Keyed to the sha256 of the GEMM sources at
-# capture time: after any change, traffic reports null.
+# DRAM traffic of the dominant kernel (dram__bytes_read.sum + dram__bytes_write.sum
+# per launch) from ncu captures of small cases of each workload that keep its
+# per-expert shape and rows per expert, with that kernel's algorithmic bytes per
+# launch in the same case (the `roofline.algorithmic_bytes_per_launch` of the
+# captured command's own bench line). A full launch's traffic is the captured
+# ratio times its own algorithmic bytes: the units (touched experts, row tiles)
+# grow and the bytes with them. Keyed to the sha256 of the GEMM sources at
+# capture time: after any change, traffic reports null. Commands and raw
+# figures: profiles/traffic_dominant_kernels.md.
 NCU_TRAFFIC = {
-    "kernel_sha256": "973ace43042a3f2903d632124a158a2e1ef4d55eb778b634fe9f7f142dc0c44c",
-    "small_m_gate_up_bytes_per_touched_expert": 1.7647e9 / 20,
-    "small_m_fused_bytes_per_touched_expert": 2.6439e9 / 20,
-    "small_m_fused_mxfp8_bytes_per_touched_expert": 1.3638e9 / 20,
+    "kernel_sha256": "4d3f80877df6796b4da6bd0e7d8d6a9bfa9a2fbbe0dc0a726707b49b428e79a1",
+    "fused_small": {"case": "decode T=8 shape with E=24", "traffic": 2.644432e+09, "algorithmic": 2.644378e+09},
+    "fused_small_mxfp8": {"case": "decode T=8 shape with E=24, MXFP8 weights", "traffic": 1.364374e+09, "algorithmic": 1.364460e+09},
+    "gate_up_small_m": {"case": "Zipf small batch with E=128", "traffic": 6.938417e+09, "algorithmic": 6.947865e+09},
+    "gate_up_tiled": {"case": "prefill shape with T=256, E=48", "traffic": 4.260360e+09, "algorithmic": 4.259316e+09},
+    "gate_up_pair": {"case": "large shape with T=4096, E=64", "traffic": 2.309426e+09, "algorithmic": 1.979711e+09},
 }
 
 
@@ -88,6 +90,15 @@ def call_accounting(wl: wlm.Workload, ids_np: np.ndarray, weight_bytes: float = 
         "touched_experts": touched,
         "R": R,
     }
+
+
+def traffic_key(inputs, weights: str, fused: bool):
+    """Which captured kernel the dominant kernel of these inputs is."""
+    if fused:
+        return "fused_small_mxfp8" if weights == "mxfp8" else "fused_small"
+    paths = {d["path"][0] for d in inputs}
+    return {frozenset({2}): "gate_up_small_m", frozenset({3}): "gate_up_tiled",
+            frozenset({1}): "gate_up_pair"}.get(frozenset(paths))
 
 
 def load_peaks() -> dict:
@@ -438,17 +449,16 @@ def run_ours(args, world, rank, local):
                          if any(mega) else "") + ")"
                       if fused else "grouped_gemm_kernel (gate-up, SiLU*up epilogue)")
     roof["algorithmic_per_step"] = g1_flops if roof["bound"] == "tensor" else g1_bytes
-    traffic = None
-    key = ("small_m_fused_mxfp8_bytes_per_touched_expert" if args.weights == "mxfp8" else
-           "small_m_fused_bytes_per_touched_expert" if fused else "small_m_gate_up_bytes_per_touched_expert")
-    if (NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and key in NCU_TRAFFIC
-            and all(d["path"][0] == 2 for d in inputs)):
-        per = [d["acct"]["touched_experts"] * NCU_TRAFFIC[key] for d in inputs]
-        traffic = float(sum(per)) / len(per)
-    roof["traffic"] = traffic
-    roof["traffic_note"] = ("ncu dram read+write bytes per launch, scaled from a 20-expert capture by touched experts"
-                            if traffic is not None else "no capture for this kernel version/workload")
     roof["algorithmic_per_launch"] = roof["algorithmic_per_step"] / len(inputs)
+    roof["algorithmic_bytes_per_launch"] = g1_bytes / len(inputs)
+    traffic = None
+    key = traffic_key(inputs, args.weights, fused)
+    cap = NCU_TRAFFIC.get(key) if key else None
+    if cap and NCU_TRAFFIC["kernel_sha256"] == kernel_sha():
+        traffic = cap["traffic"] / cap["algorithmic"] * roof["algorithmic_bytes_per_launch"]
+    roof["traffic"] = traffic
+    roof["traffic_note"] = (f"ncu dram read+write bytes per launch of {cap['case']}, scaled by algorithmic bytes"
+                            if traffic is not None else "no capture for this kernel version/workload")
     # whole-call roofline: slower of FLOPs at tensor peak and touched bytes at HBM bandwidth
     t_roof = sum(max(d["acct"]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12),
                      d["acct"]["bytes"] / (peaks["hbm_gbs"] * 1e9)) for d in inputs)

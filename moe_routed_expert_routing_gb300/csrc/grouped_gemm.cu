@@ -1135,13 +1135,22 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                             // 16 codes of K [16c, 16c + 16), at the 128-byte swizzled position of chunk c
                             const int c = c0 + i;
                             const uint4 raw = *reinterpret_cast<const uint4 *>(tile + ((c ^ (row & 7)) << 4));
-                            // 2^(code - 127) as fp32 (codes >= 1: the block maxima are >= 2^-100)
-                            const float scale = __uint_as_float(((codes4 >> (8 * (c >> 1))) & 0xffu) << 23);
                             const int o = i * 8;
-                            e4m3x4_to_bf16x4(raw.x, scale, out[o + 0], out[o + 1]);
-                            e4m3x4_to_bf16x4(raw.y, scale, out[o + 2], out[o + 3]);
-                            e4m3x4_to_bf16x4(raw.z, scale, out[o + 4], out[o + 5]);
-                            e4m3x4_to_bf16x4(raw.w, scale, out[o + 6], out[o + 7]);
+// E8M0 code sc: 2^(sc - 127). One bf16 multiply by 2^(sc - 7) when that is
+                            // a normal bf16 (sc <= 134), else by 2^127 and then by 2^(sc - 134)
+                            const uint32_t sc = (codes4 >> (8 * (c >> 1))) & 0xffu;
+                            const bool big = sc > 134u;
+                            const uint32_t s1 = ((big ? 254u : sc + 120u) << 7) * 0x00010001u;
+                            e4m3x4_to_bf16x4(raw.x, s1, out[o + 0], out[o + 1]);
+                            e4m3x4_to_bf16x4(raw.y, s1, out[o + 2], out[o + 3]);
+                            e4m3x4_to_bf16x4(raw.z, s1, out[o + 4], out[o + 5]);
+                            e4m3x4_to_bf16x4(raw.w, s1, out[o + 6], out[o + 7]);
+                            if (big) {
+                                const uint32_t s2 = ((sc - 7u) << 7) * 0x00010001u;
+#pragma unroll
+                                for (int z = 0; z < 8; ++z)
+                                    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(out[o + z]) : "r"(s2));
+                            }
                         }
                         tmem_st_32x32b_x32(t_addr + c0 * 8, out);
                     }

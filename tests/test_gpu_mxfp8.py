@@ -129,6 +129,45 @@ def test_mxfp8_forward_equals_bf16_forward_on_dequantized(B, case):
     assert_within_tolerance(wlm.bf16_bits(outs[0]), ref_acc, f"mxfp8 {case}")
 
 
+def test_mxfp8_forward_scale_extremes(B):
+    """Blocks at the ends of the scale range the expansion handles: maxima >= 2^16
+    (scale exponent e > 7, expanded with two bf16 multiplies), a block at 2^-90
+    (e = -98), blocks whose small entries quantize to E4M3 subnormal codes, a zero
+    block and signed zeros; in both GEMMs of touched experts. The forward on the
+    MXFP8 weights equals the bf16 forward on the dequantized weights bit for bit."""
+    T, E, k, H, I = 8, 8, 2, 512, 256
+    wl = wlm.custom("mxext", T, E, k, H, I, seed=57)
+    x = wlm.make_x(wl, "cuda")
+    W13, W2 = wlm.make_weights(wl, "cuda")
+    ids_np, w_np = wlm.make_routing(wl)
+    ids_np[0] = [0, 1]
+    ids_np[1] = [1, 2]
+    ids, w = torch.from_numpy(ids_np).cuda(), torch.from_numpy(w_np).cuda()
+    W13[0, 3, :32] *= 2.0 ** 24                     # gate row: max ~2^19, e = 11
+    W13[1, I + 9, 64:96] *= 2.0 ** 17               # up row: e around 4..5, and one block pushed above 2^16
+    W13[1, I + 9, 64] = 70000.0
+    W13[2, 5, 32:64] = 2.0 ** -90                   # tiny block: e = -98
+    W13[0, 7, 96:128] = torch.tensor([1.0, -1e-5, 3e-6, -2e-6] + [0.0] * 14 + [-0.0] * 14)   # subnormal codes
+    W2[0, 11, :32] *= 2.0 ** 24                     # down GEMM: e > 7 as well
+    W2[1, 2, 32:64] = torch.tensor([-0.5, 1e-5] + [0.0] * 30)
+    W2[2, 4, :32] = 0
+    p_mx = B.Problem.make(T, E, k, H, I, weight_layout=B.MOE_WEIGHTS_MXFP8)
+    W13_mx, W2_mx, (q13, s13), (q2, s2) = quantized(B, p_mx, W13, W2)
+    assert s13.max() > 127 + 7 and s2.max() > 127 + 7 and s13.min() < 127 - 90
+    assert np.any((q13 & 0x78) == 0) and np.any(((q13 & 0x78) == 0) & ((q13 & 0x07) != 0))   # subnormal codes
+    W13_d = dequantized_device(q13, s13, W13.shape)
+    W2_d = dequantized_device(q2, s2, W2.shape)
+    outs = []
+    for p, a, b in [(p_mx, W13_mx, W2_mx), (B.Problem.make(T, E, k, H, I), W13_d, W2_d)]:
+        bufs = B.Buffers(p)
+        B.moe_forward(p, x, ids, w, a, b, bufs.expert_offsets, bufs.perm, bufs.out, bufs.ws)
+        torch.cuda.synchronize()
+        assert B.moe_last_device_error(bufs.ws) == 0
+        outs.append(bufs.out.clone())
+    assert torch.isfinite(outs[0].float()).all()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
 def test_mxfp8_refused_outside_the_m_small_path(B):
     p = B.Problem.make(2048, 384, 6, 7168, 3072, weight_layout=B.MOE_WEIGHTS_MXFP8)
     with pytest.raises(B.MoeError) as ei:
