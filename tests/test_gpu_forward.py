@@ -89,10 +89,12 @@ def test_capacity_tail_poison_does_not_leak(B):
             assert torch.equal(bufs.out.view(torch.int16), clean.view(torch.int16))
 
 
-def test_graph_replay_new_routing_and_token_count(B):
+@pytest.mark.parametrize("shape", [(256, 16, 4, 512, 256), (1024, 8, 2, 512, 256)], ids=["tiled", "cta_pair"])
+def test_graph_replay_new_routing_and_token_count(B, shape):
     """Capture one forward with a device token count; replay with new routing
-    contents and other counts: bit-identical to eager calls (no host sync inside)."""
-    wl = wlm.custom("graph", 256, 16, 4, 512, 256, seed=10)
+    contents and other counts: bit-identical to eager calls (no host sync inside).
+    Single-CTA tiles (64 rows per expert) and CTA-pair tiles (256)."""
+    wl = wlm.custom("graph", *shape, seed=10)
     dw = DeviceWorkload(wl)
     p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
     bufs = B.Buffers(p)
@@ -300,12 +302,14 @@ def test_megakernel_dropped_invalid_and_repeated_slots(B):
     assert_within_tolerance(wlm.bf16_bits(bufs.out[:10]), ref_acc, "megakernel degenerate routing")
 
 
-def test_prefill_graph_replay_device_token_counts(B):
-    """Prefill shape captured once as a CUDA graph at T_max = 2048 (static
-    capacity T_max*k), replayed with device T in {2048, 1024, 1}: each replay
-    equals an eager call bit for bit, leaves rows >= T untouched, and matches
-    the oracle on sampled tokens."""
-    wl = wlm.WORKLOADS["prefill"]
+@pytest.mark.parametrize("name", ["prefill", "large"])
+def test_prefill_graph_replay_device_token_counts(B, name):
+    """Prefill shape (single-CTA tiles) and large shape (CTA-pair tiles)
+    captured once as a CUDA graph at T_max (static capacity T_max*k), replayed
+    with device T in {T_max, T_max/2, 1}: each replay equals an eager call bit
+    for bit, leaves rows >= T untouched, and matches the oracle on sampled
+    tokens."""
+    wl = wlm.WORKLOADS[name]
     dw = DeviceWorkload(wl)
     p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
     bufs = B.Buffers(p)
@@ -320,7 +324,7 @@ def test_prefill_graph_replay_device_token_counts(B):
                           d_num_tokens=d_T, stream=s)
     torch.cuda.current_stream().wait_stream(s)
     eager = B.Buffers(p)
-    for T_dev in (2048, 1024, 1):
+    for T_dev in (wl.T, wl.T // 2, 1):
         d_T.fill_(T_dev)
         bufs.out.fill_(2.0)
         g.replay()
@@ -332,4 +336,4 @@ def test_prefill_graph_replay_device_token_counts(B):
         assert torch.equal(bufs.out[:T_dev].view(torch.int16), eager.out[:T_dev].view(torch.int16))
         tokens = np.sort(np.random.default_rng(T_dev + 7).choice(T_dev, min(T_dev, 32), replace=False)).astype(np.int32)
         ref_acc, _ = dw.oracle_out(tokens, ids_np=dw.ids_np[:T_dev], w_np=dw.w_np[:T_dev])
-        assert_within_tolerance(wlm.bf16_bits(bufs.out)[tokens], ref_acc, f"prefill graph T={T_dev}")
+        assert_within_tolerance(wlm.bf16_bits(bufs.out)[tokens], ref_acc, f"{name} graph T={T_dev}")
