@@ -1136,7 +1136,7 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                             const int c = c0 + i;
                             const uint4 raw = *reinterpret_cast<const uint4 *>(tile + ((c ^ (row & 7)) << 4));
                             const int o = i * 8;
-// E8M0 code sc: 2^(sc - 127). One bf16 multiply by 2^(sc - 7) when that is
+                            // E8M0 code sc: 2^(sc - 127). One bf16 multiply by 2^(sc - 7) when that is
                             // a normal bf16 (sc <= 134), else by 2^127 and then by 2^(sc - 134)
                             const uint32_t sc = (codes4 >> (8 * (c >> 1))) & 0xffu;
                             const bool big = sc > 134u;
