@@ -28,6 +28,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import time
@@ -60,10 +61,11 @@ GRAPH_STEPS = 10
 # captured command's own bench line). A full launch's traffic is the captured
 # ratio times its own algorithmic bytes: the units (touched experts, row tiles)
 # grow and the bytes with them. Keyed to the sha256 of the GEMM sources at
-# capture time: after any change, traffic reports null. Commands and raw
+# capture time, comments and layout left out: after any change to the code,
+# traffic reports null. Commands and raw
 # figures: profiles/traffic_dominant_kernels.md.
 NCU_TRAFFIC = {
-    "kernel_sha256": "4d3f80877df6796b4da6bd0e7d8d6a9bfa9a2fbbe0dc0a726707b49b428e79a1",
+    "kernel_sha256": "81ca1e992f936f144c15be6ef721b899c395a39c9003253edb7f4074fab62beb",
     "fused_small": {"case": "decode T=8 shape with E=24", "traffic": 2.644432e+09, "algorithmic": 2.644378e+09},
     "fused_small_mxfp8": {"case": "decode T=8 shape with E=24, MXFP8 weights", "traffic": 1.364374e+09, "algorithmic": 1.364460e+09},
     "gate_up_small_m": {"case": "Zipf small batch with E=128", "traffic": 6.938417e+09, "algorithmic": 6.947865e+09},
@@ -112,11 +114,19 @@ def load_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def code_only(text: str) -> str:
+    """C++ source without comments and with whitespace collapsed: edits to
+    comments or layout leave the kernels, and so their captures, unchanged."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_sha() -> str:
     h = hashlib.sha256()
     for name in ("grouped_gemm.cu", "ptx.cuh", "moe_internal.h"):
-        with open(os.path.join(ROOT, "moe_routed_expert_routing_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "moe_routed_expert_routing_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()
 
 

@@ -40,7 +40,8 @@
 //
 // Outputs: the gate-up GEMM stores h in bf16 (the rounding the MLP defines);
 // the down GEMM stores y in fp32, so the only rounding between the fp32
-// accumulators and the combine's fp32 sum is the final one to bf16.
+// accumulators and the combine's fp32 sum is the final one to bf16 (on the
+// tiled paths moe_forward asks for fp16 y instead, rounded once, saturating).
 #include <cuda_bf16.h>
 
 #include "moe_internal.h"
