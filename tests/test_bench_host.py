@@ -87,3 +87,12 @@ def test_reference_arm_other_ranks_exit_quietly(capsys, monkeypatch):
     monkeypatch.setenv("RANK", "1")
     assert bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "0"]) == 0
     assert capsys.readouterr().out.strip() == ""
+
+
+def test_traffic_key_ignores_comments_not_code():
+    """The ncu traffic captures stay keyed to the kernel code: comments and
+    layout do not change the key, a changed token does."""
+    src = "int a = 1; // note\n/* block\n comment */  int b =  2;\n"
+    assert bench.code_only(src) == bench.code_only("int a = 1;\n   int b = 2; // other note\n")
+    assert bench.code_only(src) != bench.code_only("int a = 1; int b = 3;")
+    assert bench.kernel_sha() == bench.kernel_sha()
