@@ -131,8 +131,9 @@ def test_mxfp8_forward_equals_bf16_forward_on_dequantized(B, case):
 
 def test_mxfp8_forward_scale_extremes(B):
     """Blocks at the ends of the scale range the expansion handles: maxima >= 2^16
-    (scale exponent e > 7, expanded with two bf16 multiplies), a block at 2^-90
-    (e = -98), blocks whose small entries quantize to E4M3 subnormal codes, a zero
+    (scale exponent e > 7, expanded with two bf16 multiplies), a block at 2^-110
+    (e = -118, the smallest the format note allows), blocks whose small entries
+    quantize to E4M3 subnormal codes, a zero
     block and signed zeros; in both GEMMs of touched experts. The forward on the
     MXFP8 weights equals the bf16 forward on the dequantized weights bit for bit."""
     T, E, k, H, I = 8, 8, 2, 512, 256
@@ -146,14 +147,16 @@ def test_mxfp8_forward_scale_extremes(B):
     W13[0, 3, :32] *= 2.0 ** 24                     # gate row: max ~2^19, e = 11
     W13[1, I + 9, 64:96] *= 2.0 ** 17               # up row: e around 4..5, and one block pushed above 2^16
     W13[1, I + 9, 64] = 70000.0
-    W13[2, 5, 32:64] = 2.0 ** -90                   # tiny block: e = -98
+    # e = -118; 2^-126 and 2^-127 quantize to E4M3 subnormal codes whose values are a
+    # bf16 normal and a bf16 subnormal
+    W13[2, 5, 32:64] = torch.tensor([2.0 ** -110, -(2.0 ** -113), 2.0 ** -126, -(2.0 ** -127)] + [2.0 ** -118] * 28)
     W13[0, 7, 96:128] = torch.tensor([1.0, -1e-5, 3e-6, -2e-6] + [0.0] * 14 + [-0.0] * 14)   # subnormal codes
     W2[0, 11, :32] *= 2.0 ** 24                     # down GEMM: e > 7 as well
     W2[1, 2, 32:64] = torch.tensor([-0.5, 1e-5] + [0.0] * 30)
     W2[2, 4, :32] = 0
     p_mx = B.Problem.make(T, E, k, H, I, weight_layout=B.MOE_WEIGHTS_MXFP8)
     W13_mx, W2_mx, (q13, s13), (q2, s2) = quantized(B, p_mx, W13, W2)
-    assert s13.max() > 127 + 7 and s2.max() > 127 + 7 and s13.min() < 127 - 90
+    assert s13.max() > 127 + 7 and s2.max() > 127 + 7 and s13.min() == 127 - 118
     assert np.any((q13 & 0x78) == 0) and np.any(((q13 & 0x78) == 0) & ((q13 & 0x07) != 0))   # subnormal codes
     W13_d = dequantized_device(q13, s13, W13.shape)
     W2_d = dequantized_device(q2, s2, W2.shape)
