@@ -65,12 +65,12 @@ GRAPH_STEPS = 10
 # traffic reports null. Commands and raw
 # figures: profiles/traffic_dominant_kernels.md.
 NCU_TRAFFIC = {
-    "kernel_sha256": "81ca1e992f936f144c15be6ef721b899c395a39c9003253edb7f4074fab62beb",
-    "fused_small": {"case": "decode T=8 shape with E=24", "traffic": 2.644432e+09, "algorithmic": 2.644378e+09},
-    "fused_small_mxfp8": {"case": "decode T=8 shape with E=24, MXFP8 weights", "traffic": 1.364374e+09, "algorithmic": 1.364460e+09},
-    "gate_up_small_m": {"case": "Zipf small batch with E=128", "traffic": 6.938417e+09, "algorithmic": 6.947865e+09},
-    "gate_up_tiled": {"case": "prefill shape with T=256, E=48", "traffic": 4.260360e+09, "algorithmic": 4.259316e+09},
-    "gate_up_pair": {"case": "large shape with T=4096, E=64", "traffic": 2.309426e+09, "algorithmic": 1.979711e+09},
+    "kernel_sha256": "1e0eeef253463b3b5f17374a38394bc5cac51e7801a93f502ffb550356918cce",
+    "fused_small": {"case": "decode T=8 shape with E=24", "traffic": 2.644566e+09, "algorithmic": 2.644378e+09},
+    "fused_small_mxfp8": {"case": "decode T=8 shape with E=24, MXFP8 weights", "traffic": 1.364430e+09, "algorithmic": 1.364460e+09},
+    "gate_up_small_m": {"case": "Zipf small batch with E=128", "traffic": 6.939009e+09, "algorithmic": 6.947865e+09},
+    "gate_up_tiled": {"case": "prefill shape with T=256, E=48", "traffic": 4.260369e+09, "algorithmic": 4.259316e+09},
+    "gate_up_pair": {"case": "large shape with T=4096, E=64", "traffic": 2.329624e+09, "algorithmic": 1.979711e+09},
 }
 
 

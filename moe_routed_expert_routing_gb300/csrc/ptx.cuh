@@ -48,10 +48,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Test the phase; while it is incomplete the thread may sleep for up to 1 us
+// (suspend-time hint) instead of spinning, which leaves issue slots and power
+// to the working warps. Measured in one process against the plain try_wait:
+// the large shape -5.3% per call (power-capped), MXFP8 decode T=8 -2.5%, bf16
+// decode T=8 -0.7%, outputs bit-identical; a 100 us hint did no better.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
                  : "r"(bar), "r"(parity)
