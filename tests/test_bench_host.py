@@ -96,3 +96,39 @@ def test_traffic_key_ignores_comments_not_code():
     assert bench.code_only(src) == bench.code_only("int a = 1;\n   int b = 2; // other note\n")
     assert bench.code_only(src) != bench.code_only("int a = 1; int b = 3;")
     assert bench.kernel_sha() == bench.kernel_sha()
+
+
+def test_traffic_key_selection():
+    """Each workload's dominant kernel maps to its own capture."""
+    def inp(path):
+        return {"path": (path, 128)}
+    assert bench.traffic_key([inp(2), inp(2)], "bf16", True) == "fused_small"
+    assert bench.traffic_key([inp(2)], "mxfp8", True) == "fused_small_mxfp8"
+    assert bench.traffic_key([inp(2)], "bf16", False) == "gate_up_small_m"
+    assert bench.traffic_key([inp(3)], "bf16", False) == "gate_up_tiled"
+    assert bench.traffic_key([inp(1)], "bf16", False) == "gate_up_pair"
+    assert bench.traffic_key([inp(1), inp(3)], "bf16", False) is None
+    for key in ("fused_small", "fused_small_mxfp8", "gate_up_small_m", "gate_up_tiled", "gate_up_pair"):
+        cap = bench.NCU_TRAFFIC[key]
+        assert cap["traffic"] > 0 and 0.9 < cap["traffic"] / cap["algorithmic"] < 1.3
+
+
+@pytest.mark.gpu
+def test_gpu_arm_json_line_on_tiny(capsys, monkeypatch):
+    """The GPU arm's one JSON line carries every key of the measurement
+    contract (tiny workload, a few steps)."""
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    assert bench.main(["--workload", "tiny", "--steps", "20", "--warmup", "3", "--e2e-steps", "5",
+                       "--cpu-seconds", "0.5"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
+                "gpu_launches", "clocks"):
+        assert key in line, key
+    assert line["value"] > 0 and line["n_gpus"] == 1 and line["gpu_launches"] > 0
+    r = line["roofline"]
+    assert r["bound"] in ("hbm", "tensor") and r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+    assert line["e2e"]["h2d_bytes_per_step"] > 0 and line["e2e"]["d2h_bytes_per_step"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(line["clocks"])
