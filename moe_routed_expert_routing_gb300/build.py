@@ -9,6 +9,7 @@ shared CUDA runtime (the same libcudart.so.13 PyTorch loads).
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -44,8 +45,16 @@ def _stale(out: str, deps) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    """Compile what is stale and link. Several processes (one per rank) may call
+    this at once: a file lock lets the first build and the others find it done."""
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        return _build_locked(nvcc, force, verbose, extra_flags)
+
+
+def _build_locked(nvcc: str, force: bool, verbose: bool, extra_flags) -> str:
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "moe.h")]
     common = ["-std=c++17", "-O3", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
               "--expt-relaxed-constexpr", *extra_flags]
