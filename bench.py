@@ -686,13 +686,19 @@ def run_compare_forms(args, world, rank, local):
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
     forms = {"separate": B.MOE_FORWARD_SEPARATE, "one_kernel": B.MOE_FORWARD_ONE_KERNEL}
+    layout = B.MOE_WEIGHTS_MXFP8 if args.weights == "mxfp8" else B.MOE_WEIGHTS_ROW_MAJOR
     rows = []
     for name in WORKLOAD_SETS[args.workload]:
         d = make_inputs([name], device, args.experts, args.tokens)[0]
         wl = d["wl"]
+        if layout == B.MOE_WEIGHTS_MXFP8:
+            q = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path, weight_layout=layout)
+            d["W13"], d["W2"] = B.moe_quantize_weights(q, d["W13"], d["W2"])
+            torch.cuda.synchronize(device)
+            torch.cuda.empty_cache()
         graphs, bufs = {}, {}
         for f, code in forms.items():
-            p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path, forward_form=code)
+            p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path, forward_form=code, weight_layout=layout)
             bufs[f] = B.Buffers(p, device)
 
             def fwd(p=p, b=bufs[f]):
@@ -728,8 +734,10 @@ def run_compare_forms(args, world, rank, local):
         same = torch.equal(bufs["separate"].out.view(torch.int16), bufs["one_kernel"].out.view(torch.int16))
         rows.append({"workload": wl.describe(), "us_per_call": {f: float(np.median(v)) for f, v in us.items()},
                      "rounds_us": {f: [round(x, 2) for x in v] for f, v in us.items()},
-                     "bit_identical": bool(same), "auto_picks": "one_kernel" if B.moe_resolve_profile(
-                         B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path))["megakernel"] else "separate"})
+                     "bit_identical": bool(same), "weights": args.weights,
+                     "auto_picks": "one_kernel" if B.moe_resolve_profile(
+                         B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=args.path, weight_layout=layout))[
+                             "megakernel"] else "separate"})
         del graphs, bufs, d
         torch.cuda.empty_cache()
     return {"compare": "moe_forward forms (separate kernels vs one kernel)", "rows": rows}

@@ -97,7 +97,7 @@ def test_quantizer_matches_oracle_decode_shape_sampled(B):
         assert np.array_equal(s2[rows], os_)
 
 
-# (T, E, k, H, I, form): tile 16 with split down GEMM (AUTO one kernel), tile 16
+# (T, E, k, H, I, form): tile 16 with split down GEMM (AUTO: three kernels), tile 16
 # unsplit, tile 16 unsplit as one kernel, tile 32, tile 64
 CASES = [(1, 64, 4, 512, 256, 0), (8, 64, 4, 4096, 256, 0), (8, 64, 4, 4096, 256, 2),
          (64, 32, 4, 512, 384, 0), (100, 32, 4, 512, 256, 0)]
