@@ -157,6 +157,10 @@ def test_launch_profile_table(B):
     assert dec8 == dict(path=2, tile_rows=16, down_split_k=1, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1,
                         megakernel=0, kernel_launches=3)
     assert B.moe_resolve_profile(P(8, 384, 6, 7168, 3072, forward_form=B.MOE_FORWARD_ONE_KERNEL))["megakernel"] == 1
+    # MXFP8 weights: AUTO keeps three kernels at T=1 (measured faster); one kernel on request
+    assert B.moe_resolve_profile(P(1, 384, 6, 7168, 3072, weight_layout=B.MOE_WEIGHTS_MXFP8))["megakernel"] == 0
+    assert B.moe_resolve_profile(P(1, 384, 6, 7168, 3072, weight_layout=B.MOE_WEIGHTS_MXFP8,
+                                   forward_form=B.MOE_FORWARD_ONE_KERNEL))["megakernel"] == 1
     assert B.moe_resolve_profile(P(1, 384, 6, 7168, 3072, forward_form=B.MOE_FORWARD_SEPARATE))["megakernel"] == 0
     with pytest.raises(B.MoeError) as ei:      # not decode-size: one kernel is refused, not ignored
         B.moe_resolve_profile(P(128, 256, 8, 7168, 2048, forward_form=B.MOE_FORWARD_ONE_KERNEL))
