@@ -22,7 +22,9 @@
                        nearest-code search (ties to the even mantissa,
                        saturation at 448); the scale rule as the bound
                        256 <= max|V| / X < 512; grid values round-tripping
-                       exactly; a block of zeros.
+                       exactly; a block of zeros; the block format the
+                       FlashInfer page prints (32 elements, E8M0 scale), read
+                       from ``tests/golden/mx_block_format.txt``.
 
 ``test_planted_mistakes`` then builds mutated copies of ``moe_oracle.c``
 (a dropped term, a swapped operand, a wrong sign, a wrong index ...) and
@@ -414,9 +416,59 @@ def pin_mx_round_trip(o: Oracle):
     assert np.array_equal(o.mx_dequantize(q, sc), bits)
 
 
+def read_golden(name: str) -> dict:
+    """``key = value`` lines of a fixture under ``tests/golden/`` ('#' starts a comment)."""
+    out = {}
+    with open(os.path.join(HERE, "golden", name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                key, value = (part.strip() for part in line.split("=", 1))
+                out[key] = value
+    return out
+
+
+def pin_mx_block_format(o: Oracle):
+    """The block format the FlashInfer page prints for MXFP8 (32 E4M3 elements
+    sharing one E8M0 scale; ``tests/golden/mx_block_format.txt``): every one
+    of a block's elements, and none outside it, sets that block's scale, and
+    each element decodes as E4M3 value times 2^(s - bias)."""
+    fmt = read_golden("mx_block_format.txt")
+    B, bias = int(fmt["block_elements"]), int(fmt["scale_bias"])
+    assert (fmt["element"], fmt["scale"]) == ("e4m3", "e8m0")
+    nb = 4
+    base = np.full((1, nb * B), 1.0, np.float32)            # every block: max 1 -> s = bias - 8
+    q0, s0 = o.mx_quantize(torch_bf16_bits(base))
+    assert s0.shape == (1, nb) and np.all(s0.astype(int) == bias - 8)
+    for b in range(nb):
+        for i in range(B):
+            w = base.copy()
+            w[0, b * B + i] = 64.0                          # lifts only block b's maximum, by 2^6
+            _, s = o.mx_quantize(torch_bf16_bits(w))
+            want = s0.astype(int).copy()
+            want[0, b] += 6
+            assert np.array_equal(s.astype(int), want), (b, i)
+    # decode: the E4M3 value of each code times 2^(s - bias), on random blocks
+    rng = np.random.default_rng(14)
+    w = rng.standard_normal((8, nb * B)).astype(np.float32) * np.ldexp(1.0, rng.integers(-12, 12, (8, 1)))
+    q, s = o.mx_quantize(torch_bf16_bits(w))
+    table = o.e4m3_values().astype(np.float64)
+    scale = np.repeat(np.ldexp(1.0, s.astype(np.int64) - bias), B, axis=1)
+    wb = bf16_bits_to_f32(torch_bf16_bits(w)).astype(np.float64)
+    # E4M3 keeps 3 mantissa bits: a normal element is within 2^-4 relative,
+    # one below the block's smallest normal within half a subnormal step; the
+    # scale leaves the block maximum in [256, 512) X, so elements above 448 X
+    # saturate to 448 X.
+    kept = np.minimum(np.abs(wb), 448.0 * scale)
+    err = np.abs(table[q] * scale - wb)
+    assert np.all(err <= (np.abs(wb) - kept) + np.maximum(kept * 2.0 ** -4, scale * 2.0 ** -10))
+    assert np.array_equal(np.sign(table[q]) * (wb != 0), np.sign(wb))
+
+
 PINS = [pin_round_bf16, pin_dispatch_hand, pin_dispatch_brute, pin_dense_mlp,
         pin_identity_expert, pin_naive_fp64, pin_streamed_equals_tokens,
-        pin_e4m3_values, pin_e4m3_rounding_brute, pin_mx_scale_rule, pin_mx_round_trip]
+        pin_e4m3_values, pin_e4m3_rounding_brute, pin_mx_scale_rule, pin_mx_round_trip,
+        pin_mx_block_format]
 
 
 # ----------------------------------------------------------------------------- tests
@@ -459,6 +511,8 @@ MUTATIONS = [
     ("e4m3_saturate_to_nan", "if (a >= 448.0f)\n        return sign | 0x7E;", "if (a >= 448.0f)\n        return sign | 0x7F;"),
     ("e4m3_value_bias", "mag = ldexpf(1.0f + (float)man / 8.0f, ex - 7);", "mag = ldexpf(1.0f + (float)man / 8.0f, ex - 8);"),
     ("mx_dequant_scale_bias", "int e = (int)s[r * nb + k / 32] - 127;", "int e = (int)s[r * nb + k / 32] - 126;"),
+    ("mx_amax_half_block", "for (int i = 0; i < 32; ++i) {\n                float a",
+     "for (int i = 0; i < 16; ++i) {\n                float a"),
     ("mx_block_stride", "const uint16_t *v = w + r * K + (int64_t)b * 32;", "const uint16_t *v = w + r * K + (int64_t)b * 31;"),
     ("invalid_id_kept", "if (e >= 0 && e < E)\n            counts[e] += 1;", "if (e >= 0 && e < E + 1 && e != E)\n            counts[e] += 1;\n        if (e == E) counts[0] += 1;"),
 ]

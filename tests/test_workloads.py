@@ -1,4 +1,6 @@
 """The seeded workload generators draw what their docstring promises (host only)."""
+import os
+
 import numpy as np
 import pytest
 
@@ -54,3 +56,33 @@ def test_weights_small_shape():
     assert 0.015 < float(W13.float().std()) < 0.025
     x = wlm.make_x(wl)
     assert x.shape == (4, 64)
+
+
+def _page_shapes():
+    """Geometries and token counts from ``tests/golden/page_workload_shapes.txt``."""
+    geometry, tokens = {}, {}
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "page_workload_shapes.txt")
+    with open(path) as f:
+        for line in f:
+            fields = line.split("#", 1)[0].split()
+            if not fields:
+                continue
+            if fields[0] == "geometry":
+                geometry[fields[1]] = tuple(int(v) for v in fields[2:6])
+            elif fields[0] == "tokens":
+                tokens[fields[1]] = {int(v) for v in fields[2:]}
+    return geometry, tokens
+
+
+def test_shapes_follow_the_pages():
+    """The decode, prefill and Zipf small-batch workloads use the expert
+    geometries the DeepGEMM and FlashInfer pages benchmark, at token counts
+    the DeepGEMM page times. (tiny is a small parity case; large is a
+    hot-expert case at its own geometry: 128 experts, top-8, 4096 / 1536.)"""
+    geometry, tokens = _page_shapes()
+    shape = {name: (wl.E, wl.k, wl.H, wl.I) for name, wl in wlm.WORKLOADS.items()}
+    for name in ("decode1", "decode8", "prefill"):
+        assert shape[name] == geometry["deepgemm"], name
+    assert shape["small"] == geometry["flashinfer"]
+    for name in ("decode1", "decode8", "small", "prefill", "large"):
+        assert wlm.WORKLOADS[name].T in tokens["deepgemm"], name
