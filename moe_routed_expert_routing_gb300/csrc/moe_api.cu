@@ -677,7 +677,8 @@ const char *moe_status_string(moe_status_t status)
     case MOE_ERR_WORKSPACE:
         return "MOE_ERR_WORKSPACE: workspace smaller than moe_workspace_size()";
     case MOE_ERR_UNSUPPORTED:
-        return "MOE_ERR_UNSUPPORTED: device is not sm_103 (GB300)";
+        return "MOE_ERR_UNSUPPORTED: the device is not sm_103 (GB300), or the weight layout or forward form "
+               "asked for is not available for this shape";
     case MOE_ERR_CUDA:
         return "MOE_ERR_CUDA: a CUDA call failed";
     }

@@ -44,6 +44,9 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings(lib):
     for s in range(7):
         assert lib.status_string(s).startswith("MOE_")
+    # the code also covers a layout or form the shape cannot take, not only the device
+    text = lib.status_string(5)
+    assert "sm_103" in text and "layout" in text and "form" in text
 
 
 def test_workspace_size_and_path(lib):
