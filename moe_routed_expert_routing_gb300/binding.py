@@ -169,6 +169,33 @@ def _ptr(t) -> int | None:
     return t.data_ptr()
 
 
+def _need(t, name: str, dtype, numel: int):
+    """Fail closed before any launch: ``t`` must be a CUDA tensor of ``dtype``
+    with at least ``numel`` elements. The C entry points see plain pointers
+    and cannot check the extent of a buffer; a short one would be read or
+    written out of bounds on the device. (A raw int pointer is passed on
+    unchecked, as the C caller's responsibility.)"""
+    if t is None or isinstance(t, int):
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (device memory), not on {t.device}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, not {t.dtype}")
+    if t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements; the problem needs at least {numel}")
+
+
+def _need_weights(problem, W13, W2):
+    """W13 [E, 2I, H] and W2 [E, H, I] in the problem's weight layout."""
+    if problem.weight_layout == MOE_WEIGHTS_MXFP8:
+        b13, b2 = moe_weight_bytes(problem, MOE_WEIGHTS_MXFP8)
+        _need(W13, "W13", torch.uint8, b13)
+        _need(W2, "W2", torch.uint8, b2)
+    else:
+        _need(W13, "W13", torch.bfloat16, problem.E * 2 * problem.I * problem.H)
+        _need(W2, "W2", torch.bfloat16, problem.E * problem.H * problem.I)
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -202,8 +229,21 @@ def moe_resolve_profile(problem: Problem) -> dict:
     return prof.as_dict()
 
 
+def _need_routing(problem, topk_ids, expert_offsets, perm, d_num_tokens):
+    R = problem.T_max * problem.k
+    _need(topk_ids, "topk_ids", torch.int32, R)
+    _need(expert_offsets, "expert_offsets", torch.int32, problem.E + 1)
+    _need(perm, "perm", torch.int32, problem.cap)
+    _need(d_num_tokens, "d_num_tokens", torch.int32, 1)
+
+
 def moe_dispatch(problem, topk_ids, expert_offsets, perm, inv, ws, x=None, x_sorted=None, d_num_tokens=None,
                  stream=None):
+    _need_routing(problem, topk_ids, expert_offsets, perm, d_num_tokens)
+    _need(inv, "inv", torch.int32, problem.T_max * problem.k)
+    _need(ws, "ws", None, 0)
+    _need(x, "x", torch.bfloat16, problem.T_max * problem.H)
+    _need(x_sorted, "x_sorted", torch.bfloat16, problem.cap * problem.H)
     _check(load_library().moe_dispatch(ctypes.byref(problem), _ptr(topk_ids), _ptr(d_num_tokens),
                                        _ptr(expert_offsets), _ptr(perm), _ptr(inv), _ptr(x), _ptr(x_sorted),
                                        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "moe_dispatch")
@@ -212,24 +252,49 @@ def moe_dispatch(problem, topk_ids, expert_offsets, perm, inv, ws, x=None, x_sor
 def moe_dispatch_noalloc(problem, topk_ids, expert_offsets, perm, inv, x=None, x_sorted=None, d_num_tokens=None,
                          stream=None):
     """moe_dispatch with no workspace (library-owned static scratch); see include/moe.h."""
+    _need_routing(problem, topk_ids, expert_offsets, perm, d_num_tokens)
+    _need(inv, "inv", torch.int32, problem.T_max * problem.k)
+    _need(x, "x", torch.bfloat16, problem.T_max * problem.H)
+    _need(x_sorted, "x_sorted", torch.bfloat16, problem.cap * problem.H)
     _check(load_library().moe_dispatch_noalloc(ctypes.byref(problem), _ptr(topk_ids), _ptr(d_num_tokens),
                                                _ptr(expert_offsets), _ptr(perm), _ptr(inv), _ptr(x),
                                                _ptr(x_sorted), _stream(stream)), "moe_dispatch_noalloc")
 
 
 def moe_expert_compute(problem, x_sorted, expert_offsets, W13, W2, y_sorted, ws, stream=None):
+    _need(x_sorted, "x_sorted", torch.bfloat16, problem.cap * problem.H)
+    _need(expert_offsets, "expert_offsets", torch.int32, problem.E + 1)
+    if problem.weight_layout != MOE_WEIGHTS_MXFP8:   # that layout is refused by the library itself
+        _need_weights(problem, W13, W2)
+    _need(y_sorted, "y_sorted", torch.float32, problem.cap * problem.H)
+    _need(ws, "ws", None, 0)
     _check(load_library().moe_expert_compute(ctypes.byref(problem), _ptr(x_sorted), _ptr(expert_offsets), _ptr(W13),
                                              _ptr(W2), _ptr(y_sorted), _ptr(ws), ws.numel() * ws.element_size(),
                                              _stream(stream)), "moe_expert_compute")
 
 
 def moe_combine(problem, y_sorted, inv, topk_weights, out, d_num_tokens=None, stream=None):
+    _need(y_sorted, "y_sorted", torch.float32, problem.cap * problem.H)
+    _need(inv, "inv", torch.int32, problem.T_max * problem.k)
+    _need(topk_weights, "topk_weights", torch.float32, problem.T_max * problem.k)
+    _need(out, "out", torch.bfloat16, problem.T_max * problem.H)
+    _need(d_num_tokens, "d_num_tokens", torch.int32, 1)
     _check(load_library().moe_combine(ctypes.byref(problem), _ptr(y_sorted), _ptr(inv), _ptr(topk_weights),
                                       _ptr(d_num_tokens), _ptr(out), _stream(stream)), "moe_combine")
 
 
+def _need_forward(problem, x, topk_ids, topk_weights, W13, W2, expert_offsets, perm, out, ws, d_num_tokens):
+    _need(x, "x", torch.bfloat16, problem.T_max * problem.H)
+    _need_routing(problem, topk_ids, expert_offsets, perm, d_num_tokens)
+    _need(topk_weights, "topk_weights", torch.float32, problem.T_max * problem.k)
+    _need_weights(problem, W13, W2)
+    _need(out, "out", torch.bfloat16, problem.T_max * problem.H)
+    _need(ws, "ws", None, 0)
+
+
 def moe_forward(problem, x, topk_ids, topk_weights, W13, W2, expert_offsets, perm, out, ws, d_num_tokens=None,
                 stream=None):
+    _need_forward(problem, x, topk_ids, topk_weights, W13, W2, expert_offsets, perm, out, ws, d_num_tokens)
     _check(load_library().moe_forward(ctypes.byref(problem), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
                                       _ptr(d_num_tokens), _ptr(W13), _ptr(W2), _ptr(expert_offsets), _ptr(perm),
                                       _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
@@ -239,6 +304,7 @@ def moe_forward(problem, x, topk_ids, topk_weights, W13, W2, expert_offsets, per
 def moe_forward_profiled(problem, x, topk_ids, topk_weights, W13, W2, expert_offsets, perm, out, ws, events,
                          d_num_tokens=None, stream=None):
     """moe_forward plus 6 stage events (torch.cuda.Event(enable_timing=True), already recorded once)."""
+    _need_forward(problem, x, topk_ids, topk_weights, W13, W2, expert_offsets, perm, out, ws, d_num_tokens)
     arr = (_vp * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(load_library().moe_forward_profiled(ctypes.byref(problem), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
                                                _ptr(d_num_tokens), _ptr(W13), _ptr(W2), _ptr(expert_offsets),
@@ -252,6 +318,8 @@ def moe_pack_weights(problem, W13, W2, W13_packed=None, W2_packed=None, stream=N
         W13_packed = torch.empty_like(W13)
     if W2_packed is None:
         W2_packed = torch.empty_like(W2)
+    for name, t in (("W13", W13), ("W2", W2), ("W13_packed", W13_packed), ("W2_packed", W2_packed)):
+        _need(t, name, torch.bfloat16, problem.E * (2 if "13" in name else 1) * problem.I * problem.H)
     _check(load_library().moe_pack_weights(ctypes.byref(problem), _ptr(W13), _ptr(W2), _ptr(W13_packed),
                                            _ptr(W2_packed), _stream(stream)), "moe_pack_weights")
     return W13_packed, W2_packed
@@ -272,12 +340,17 @@ def moe_quantize_weights(problem, W13, W2, W13_mx=None, W2_mx=None, stream=None)
         W13_mx = torch.empty(b13, dtype=torch.uint8, device=W13.device)
     if W2_mx is None:
         W2_mx = torch.empty(b2, dtype=torch.uint8, device=W2.device)
+    _need(W13, "W13", torch.bfloat16, problem.E * 2 * problem.I * problem.H)
+    _need(W2, "W2", torch.bfloat16, problem.E * problem.H * problem.I)
+    _need(W13_mx, "W13_mx", torch.uint8, b13)
+    _need(W2_mx, "W2_mx", torch.uint8, b2)
     _check(load_library().moe_quantize_weights(ctypes.byref(problem), _ptr(W13), _ptr(W2), _ptr(W13_mx),
                                                _ptr(W2_mx), _stream(stream)), "moe_quantize_weights")
     return W13_mx, W2_mx
 
 
 def moe_last_device_error(ws, stream=None) -> int:
+    _need(ws, "ws", None, 4)
     code = ctypes.c_int32(0)
     _check(load_library().moe_last_device_error(_ptr(ws), _stream(stream), ctypes.byref(code)),
            "moe_last_device_error")
@@ -285,6 +358,7 @@ def moe_last_device_error(ws, stream=None) -> int:
 
 
 def moe_clear_device_error(ws, stream=None):
+    _need(ws, "ws", None, 0)
     _check(load_library().moe_clear_device_error(_ptr(ws), _stream(stream)), "moe_clear_device_error")
 
 

@@ -120,3 +120,47 @@ def test_weight_bytes_pure_host(lib):
     with pytest.raises(lib.MoeError) as ei:
         lib.moe_weight_bytes(p, 7)
     assert ei.value.status == 2
+
+
+class _DeviceStandIn:
+    """Stands in for a CUDA tensor (device, dtype, element count) so that the
+    binding's extent and dtype checks can be exercised without a GPU."""
+    is_cuda = True
+
+    def __init__(self, dtype, n):
+        self.dtype, self._n = dtype, n
+
+    def numel(self):
+        return self._n
+
+
+def test_binding_checks_fail_closed_before_the_library(lib, monkeypatch):
+    import torch
+    P = lib.Problem.make(16, 8, 2, 256, 128)
+    # dtype and extent, per argument
+    lib._need(_DeviceStandIn(torch.int32, 32), "topk_ids", torch.int32, 32)
+    with pytest.raises(ValueError, match="int32"):
+        lib._need(_DeviceStandIn(torch.int64, 32), "topk_ids", torch.int32, 32)
+    with pytest.raises(ValueError, match="at least 32"):
+        lib._need(_DeviceStandIn(torch.int32, 31), "topk_ids", torch.int32, 32)
+    lib._need(1 << 40, "raw pointer", torch.int32, 32)          # a raw address is the caller's to vouch for
+    with pytest.raises(ValueError, match="W13"):
+        lib._need_weights(P, _DeviceStandIn(torch.bfloat16, 8 * 2 * 128 * 256 - 1),
+                          _DeviceStandIn(torch.bfloat16, 8 * 256 * 128))
+    Q = lib.Problem.make(16, 8, 2, 256, 128, weight_layout=lib.MOE_WEIGHTS_MXFP8)
+    b13, b2 = lib.moe_weight_bytes(Q, lib.MOE_WEIGHTS_MXFP8)
+    lib._need_weights(Q, _DeviceStandIn(torch.uint8, b13), _DeviceStandIn(torch.uint8, b2))
+    with pytest.raises(ValueError, match="W2"):
+        lib._need_weights(Q, _DeviceStandIn(torch.uint8, b13), _DeviceStandIn(torch.uint8, b2 - 1))
+
+    # host tensors never reach the C entry points
+    def no_library(*a, **k):
+        raise AssertionError("the library was called")
+    monkeypatch.setattr(lib, "load_library", no_library)
+    x = torch.zeros((16, 256), dtype=torch.bfloat16)
+    ids = torch.zeros((16, 2), dtype=torch.int32)
+    w = torch.ones((16, 2), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lib.moe_forward(P, x, ids, w, 1 << 40, 1 << 40, 1 << 40, 1 << 40, 1 << 40, 1 << 40)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lib.moe_combine(P, 1 << 40, 1 << 40, w, 1 << 40)

@@ -142,3 +142,33 @@ def test_fp16_intermediate_y_range_is_reported(B):
         err = B.moe_last_device_error(bufs.ws)
         assert bool(err & B.MOE_DEVERR_Y_RANGE) == flagged, err
         assert torch.isfinite(bufs.out[:T].float()).all()
+
+
+def test_binding_rejects_wrong_dtype_and_short_buffers(B):
+    """The binding fails closed on CUDA tensors of the wrong dtype or extent,
+    before any launch, and the buffers stay as they were."""
+    p = B.Problem.make(16, 8, 2, 256, 128)
+    wl = wlm.custom("bad", 16, 8, 2, 256, 128, seed=3)
+    x = wlm.make_x(wl, "cuda")
+    W13, W2 = wlm.make_weights(wl, "cuda")
+    ids_np, w_np = wlm.make_routing(wl)
+    ids = torch.from_numpy(ids_np).cuda()
+    w = torch.from_numpy(w_np).cuda()
+    bufs = B.Buffers(p)
+    bufs.out.fill_(5.0)
+    cases = [
+        dict(topk_ids=ids.long()),                     # int64 ids
+        dict(topk_weights=w.double()),                 # fp64 weights
+        dict(x=x[:15]),                                # one token short
+        dict(W2=W2[:7]),                               # one expert short
+        dict(perm=bufs.perm[:-1]),                     # perm shorter than the capacity
+    ]
+    for bad in cases:
+        args = dict(x=x, topk_ids=ids, topk_weights=w, W13=W13, W2=W2, expert_offsets=bufs.expert_offsets,
+                    perm=bufs.perm, out=bufs.out, ws=bufs.ws)
+        args.update(bad)
+        with pytest.raises(ValueError):
+            B.moe_forward(p, **args)
+    torch.cuda.synchronize()
+    assert torch.all(bufs.out == 5.0)
+    assert B.moe_last_device_error(bufs.ws) == 0
