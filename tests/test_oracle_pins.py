@@ -483,6 +483,30 @@ def test_pin(orc, pin):
     pin(orc)
 
 
+def test_dispatch_matches_brute_force_on_random_routings(orc):
+    """Property form of the dispatch pin: on random shapes and ids (dropped
+    -1 slots and out-of-range ids included), the oracle's dispatch equals the
+    O(R * E) restatement, and the bad-id flag is set exactly when an id lies
+    outside [-1, E)."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    @hyp.settings(max_examples=200, deadline=None, derandomize=True)
+    @hyp.given(T=st.integers(0, 40), k=st.integers(1, 6), E=st.integers(1, 12), data=st.data())
+    def check(T, k, E, data):
+        flat = data.draw(st.lists(st.integers(-2, E + 1), min_size=T * k, max_size=T * k))
+        ids = np.array(flat, dtype=np.int32).reshape(T, k)
+        counts, offsets, perm, inv, bad = orc.dispatch(ids, E)
+        b_off, b_perm, b_inv = brute_dispatch(ids.reshape(-1), E)
+        assert offsets.tolist() == b_off
+        assert perm[:b_off[-1]].tolist() == b_perm and np.all(perm[b_off[-1]:] == -1)
+        assert inv.tolist() == b_inv
+        assert counts.tolist() == np.diff(b_off).tolist()
+        assert bool(bad) == any(v < -1 or v >= E for v in flat)
+
+    check()
+
+
 # Each entry: (name, text in moe_oracle.c, replacement). Every mutation is a
 # plausible slip: a dropped term, a swapped or transposed operand, a wrong
 # sign, a wrong index or stride, a missing rounding, an unstable scatter.
