@@ -9,6 +9,16 @@
 // FP4 weight packets", Motivation: for sparse small-token work, mark one-use
 // routed weight loads EVICT_FIRST.
 //
+// Three kernels live here:
+//  * grouped_gemm_kernel -- one GEMM (gate-up or down) per launch, on a
+//    single CTA per tile; the template below, in two operand placements;
+//  * fused_small_kernel -- both GEMMs of the M-small path in one persistent
+//    launch (16-row token tiles), optionally the whole forward (dispatch and
+//    combine inside), and an MXFP8 mode whose converter warps expand E4M3
+//    weights to bf16 in TMEM;
+//  * grouped_gemm_pair_kernel -- the tiled placement on 2-CTA clusters,
+//    tcgen05.mma.cta_group::2 of M=256 x N=256, for the largest batches.
+//
 // One kernel template, two placements of the operands:
 //
 //  * tiled (large batches): A = 128 activation rows, B = 256 weight rows
@@ -33,6 +43,9 @@
 // accumulators so the epilogue of one unit overlaps the main loop of the
 // next. Every wait is bounded: on give-up the CTA raises an abort flag,
 // drains what it has in flight, frees TMEM and sets MOE_DEVERR_WAIT_TIMEOUT.
+// mbarrier waits suspend up to 1 us per test (try_wait with a time hint)
+// instead of re-testing in a loop, which leaves shared memory to the TMA
+// writes and the MMA operand reads.
 //
 // Rows of a tile past the end of its expert belong to the next expert (or
 // are zero-filled by TMA past the capacity): they are computed and never
