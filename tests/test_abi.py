@@ -164,3 +164,13 @@ def test_binding_checks_fail_closed_before_the_library(lib, monkeypatch):
         lib.moe_forward(P, x, ids, w, 1 << 40, 1 << 40, 1 << 40, 1 << 40, 1 << 40, 1 << 40)
     with pytest.raises(ValueError, match="CUDA tensor"):
         lib.moe_combine(P, 1 << 40, 1 << 40, w, 1 << 40)
+
+
+def test_missing_library_fails_loudly(lib, tmp_path, monkeypatch):
+    """Without libmoe.so the binding raises; nothing falls back to a CPU path."""
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        lib.load_library(str(tmp_path / "libmoe.so"))
+    monkeypatch.setattr(lib, "_lib", None)
+    monkeypatch.setattr(lib, "lib_path", lambda: str(tmp_path / "absent" / "libmoe.so"))
+    with pytest.raises(RuntimeError, match="not found"):
+        lib.moe_workspace_size(lib.Problem.make(16, 8, 2, 256, 128))
