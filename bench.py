@@ -2,22 +2,26 @@
 """Benchmark of routed-MoE expert execution on one GB300 (or N replicas).
 
 One step = one pass of the whole path (dispatch -> gate-up GEMM with fused
-SiLU*up -> down GEMM -> combine) over each batch of the chosen workload; the
-default workload is the decode configuration: a T=1 batch and a T=8 batch
-(E=384, k=6, H=7168, I=3072), back to back. Weights, routing and activations
-are synthetic (seeded generators in workloads.py) and resident in HBM.
+SiLU*up -> down GEMM -> combine) over each batch of the chosen workload. The
+default workload is the largest single-GPU configuration: T=8192 tokens,
+E=128 experts, top-8, H=4096, I=1536, a quarter of the tokens forced onto
+expert 0 (the tensor-bound case). Weights, routing and activations are
+synthetic (seeded generators in workloads.py) and resident in HBM.
 
-Timing: the step is captured in a CUDA graph (10 steps per graph, each
-forward recording 6 stage events as external graph nodes); W warm-up steps,
-then K steps between two CUDA events, barrier + synchronize on both sides,
-max over ranks. The touched expert weights of one step (~6.8 GB for decode)
-are far larger than the 129 MB L2, so no flush is needed between steps.
+Timing: one step is captured in a CUDA graph. Warm-up is exactly W steps
+(one eager forward, which also sets the kernels' function attributes, then
+W-1 replays); then exactly K replays between two CUDA events, barrier +
+synchronize on both sides, max over ranks. The touched expert weights and
+sorted batches of one step (~5.5 GB for the default workload) are far larger
+than the 129 MB L2, so no flush is needed between steps.
 
-Printed: one JSON line (rank 0) with the throughput (TFLOP/s), us/call, the
-roofline of the dominant kernel (the gate-up GEMM) from its event-timed
-duration, an end-to-end number through the public C-ABI call with pinned host
-buffers, SM clocks sampled during the timed region and the CPU oracle's
-throughput on a bounded sample.
+Printed: one JSON line (rank 0) with the throughput (TFLOP/s), the roofline
+of the dominant kernel (its share of a profiled step, from CUDA events
+between the stages, applied to the timed step), an end-to-end number through
+the public C-ABI call with pinned host buffers, SM clocks sampled during the
+timed region, the CPU oracle's throughput on a bounded sample, and, under
+`per_config`, us/call, TFLOP/s and call-roofline fraction of the prefill,
+Zipf small-batch and decode workloads, each timed on its own.
 
 ``--impl reference`` times the CPU oracle instead (rank 0 only).
 """
@@ -62,8 +66,7 @@ GRAPH_STEPS = 10
 # ratio times its own algorithmic bytes: the units (touched experts, row tiles)
 # grow and the bytes with them. Keyed to the sha256 of the GEMM sources at
 # capture time, comments and layout left out: after any change to the code,
-# traffic reports null. Commands and raw
-# figures: profiles/traffic_dominant_kernels.md.
+# traffic reports null.
 NCU_TRAFFIC = {
     "kernel_sha256": "1e0eeef253463b3b5f17374a38394bc5cac51e7801a93f502ffb550356918cce",
     "fused_small": {"case": "decode T=8 shape with E=24", "traffic": 2.644566e+09, "algorithmic": 2.644378e+09},
@@ -309,15 +312,8 @@ def make_inputs(names, device, experts=0, tokens=0):
     return out
 
 
-def run_ours(args, world, rank, local):
-    from moe_routed_expert_routing_gb300.build import build
-    build()
-    from moe_routed_expert_routing_gb300 import binding as B
-
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    init_dist(world, local)
-    names = WORKLOAD_SETS[args.workload]
+def prepare(B, names, device, args):
+    """Device inputs, problems and caller buffers of the named batches."""
     inputs = make_inputs(names, device, args.experts, args.tokens)
     layout = (B.MOE_WEIGHTS_MXFP8 if args.weights == "mxfp8" else
               B.MOE_WEIGHTS_PACKED if args.packed else B.MOE_WEIGHTS_ROW_MAJOR)
@@ -337,109 +333,93 @@ def run_ours(args, world, rank, local):
         d["bufs"] = B.Buffers(d["problem"], device)
         d["path"] = B.moe_resolve_path(d["problem"])
         d["profile"] = B.moe_resolve_profile(d["problem"])
-    stream = torch.cuda.Stream(device)
+    return inputs
 
-    def new_events():
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-        for e in evs:
-            e.record(stream)   # creates the underlying cudaEvent_t
-        return evs
 
-    # first calls outside capture (function attributes), then capture GRAPH_STEPS steps
-    with torch.cuda.stream(stream):
-        for d in inputs:
-            B.moe_forward(d["problem"], d["x"], d["ids"], d["w"], d["W13"], d["W2"], d["bufs"].expert_offsets,
-                          d["bufs"].perm, d["bufs"].out, d["bufs"].ws, stream=stream)
-    stream.synchronize()
-    for d in inputs:
-        err = B.moe_last_device_error(d["bufs"].ws, stream)
-        if err:
-            raise RuntimeError(f"device error word {err} on {d['wl'].name}")
-
-    G = GRAPH_STEPS if args.steps % GRAPH_STEPS == 0 else 1
-    events = [[new_events() for _ in inputs] for _ in range(G)]
-    stream.synchronize()
-    # headline graph: G steps of plain moe_forward (kernels back to back, so
-    # programmatic dependent launch overlaps each kernel's prologue with the
-    # previous kernel's tail); profiled graph: the same steps with stage events
-    # (event nodes sit between the kernels and cut that overlap)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            for g in range(G):
-                for d in inputs:
-                    B.moe_forward(d["problem"], d["x"], d["ids"], d["w"], d["W13"], d["W2"],
-                                  d["bufs"].expert_offsets, d["bufs"].perm, d["bufs"].out, d["bufs"].ws,
-                                  stream=stream)
-    graph_prof = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph_prof, stream=stream):
-            for g in range(G):
-                for i, d in enumerate(inputs):
-                    B.moe_forward_profiled(d["problem"], d["x"], d["ids"], d["w"], d["W13"], d["W2"],
-                                           d["bufs"].expert_offsets, d["bufs"].perm, d["bufs"].out, d["bufs"].ws,
-                                           events[g][i], stream=stream)
-    n_replays = args.steps // G
-    warm_replays = max(1, math.ceil(args.warmup / G))
-    with torch.cuda.stream(stream):
-        for _ in range(warm_replays):
-            graph.replay()
-            graph_prof.replay()
-    stream.synchronize()
-
-    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
-                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    barrier(world, device)
-    torch.cuda.synchronize(device)
-    clocks.start()
-    time.sleep(0.25)
-    with torch.cuda.stream(stream):
-        t_start.record(stream)
-        for _ in range(n_replays):
-            graph.replay()
-        t_end.record(stream)
-    torch.cuda.synchronize(device)
-    clk = clocks.stop()
-    barrier(world, device)
-    local_ms = t_start.elapsed_time(t_end)
-    max_ms = max_over_ranks(local_ms, world, device)
-    K = n_replays * G
-
-    # kernel durations: the profiled graph over its own timed region (same
-    # steps, stage events between the kernels); the last G steps are read back
-    prof_replays = max(1, min(n_replays, 20))
-    p_start = torch.cuda.Event(enable_timing=True)
-    p_end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        p_start.record(stream)
-        for _ in range(prof_replays):
-            graph_prof.replay()
-        p_end.record(stream)
-    torch.cuda.synchronize(device)
-    prof_ms_per_step = p_start.elapsed_time(p_end) / (prof_replays * G)
-
-    # per-stage times of the last G steps of the profiled region
-    stage_us = []
+def forward_step(B, inputs, stream, events=None):
+    """One step: moe_forward over every batch of the workload (with stage events if given)."""
     for i, d in enumerate(inputs):
-        per = np.array([[events[g][i][s].elapsed_time(events[g][i][s + 1]) * 1e3 for s in range(5)]
-                        for g in range(G)])
-        stage_us.append(per.mean(axis=0))
+        b = d["bufs"]
+        if events is None:
+            B.moe_forward(d["problem"], d["x"], d["ids"], d["w"], d["W13"], d["W2"], b.expert_offsets, b.perm,
+                          b.out, b.ws, stream=stream)
+        else:
+            B.moe_forward_profiled(d["problem"], d["x"], d["ids"], d["w"], d["W13"], d["W2"], b.expert_offsets,
+                                   b.perm, b.out, b.ws, events[i], stream=stream)
+
+
+def check_device_errors(B, inputs, stream):
     for d in inputs:
         err = B.moe_last_device_error(d["bufs"].ws, stream)
         if err:
             raise RuntimeError(f"device error word {err} on {d['wl'].name}")
 
-    flops_step = sum(d["acct"]["flops"] for d in inputs)
-    bytes_step = sum(d["acct"]["bytes"] for d in inputs)
-    ms_per_step = max_ms / K
-    value = world * flops_step * K / (max_ms * 1e-3) / 1e12
-    peaks = load_peaks()
 
-    # dominant kernel: the gate-up GEMM (2/3 of the FLOPs and weight bytes); on
-    # the M-small path both GEMMs run as one persistent kernel, timed as one;
-    # for decode batches that kernel is the whole call (all stage marks after it)
+def capture(stream, fn, steps: int):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(steps):
+                fn(s)
+    return g
+
+
+def replay_timed(stream, graph, reps: int) -> float:
+    """Milliseconds of `reps` back-to-back replays between two CUDA events on `stream`."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def stage_profile(B, inputs, stream, steps: int = 4, reps: int = 2):
+    """Stage times from a graph of `steps` steps of moe_forward_profiled (six
+    events per forward, external event nodes between the kernels), replayed
+    `reps` times; the stage times are those of the last replay. Returns
+    (per-batch mean stage times in us, profiled step time in us)."""
+    events = []
+    for _ in range(steps):
+        row = []
+        for _ in inputs:
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            for e in evs:
+                e.record(stream)   # creates the underlying cudaEvent_t
+            row.append(evs)
+        events.append(row)
+    stream.synchronize()
+    g = capture(stream, lambda s: forward_step(B, inputs, stream, events[s]), steps)
+    for _ in range(reps - 1):
+        replay_timed(stream, g, 1)
+    ms = replay_timed(stream, g, 1)
+    stage_us = []
+    for i in range(len(inputs)):
+        per = np.array([[events[s][i][j].elapsed_time(events[s][i][j + 1]) * 1e3 for j in range(5)]
+                        for s in range(steps)])
+        stage_us.append(per.mean(axis=0))
+    del g
+    return stage_us, ms * 1e3 / steps
+
+
+def tensor_peak(peaks: dict, region_s: float):
+    """The measured bf16 peak that applies to a kernel timed over `region_s`
+    seconds: the sustained figure (seconds-long loop under the power cap) for
+    regions of a second or more, else the burst figure."""
+    if region_s >= 1.0:
+        return peaks["bf16_tflops_sustained"], f"bf16 dense, sustained ({peaks['source']}): timed region {region_s:.2f} s"
+    return peaks["bf16_tflops"], f"bf16 dense, burst ({peaks['source']}): timed region {region_s * 1e3:.0f} ms < 1 s"
+
+
+def dominant_kernel(inputs, stage_us, weights: str):
+    """Which kernel dominates the step, its profiled time per step (us) and
+    its algorithmic FLOPs and bytes per step. The gate-up GEMM holds 2/3 of
+    the FLOPs and weight bytes; where both GEMMs run as one persistent kernel
+    (M-small path) that kernel is timed as one, and where the whole forward is
+    one kernel (decode-size batches) its stage marks all fall after it."""
     fused = all(d["profile"]["fused_mlp"] for d in inputs)
     mega = [d["profile"]["megakernel"] for d in inputs]
 
@@ -448,39 +428,131 @@ def run_ours(args, world, rank, local):
             return float(sum(s))
         return float(s[2]) + (float(s[3]) if fused else 0.0)
 
-    g1_us = sum(kernel_us(d, s) for d, s in zip(inputs, stage_us))
-    g1_flops = sum(d["acct"]["gemm1_flops"] * (1.5 if fused else 1.0) for d in inputs)
-    g1_bytes = sum(d["acct"]["gemm1_bytes"] + (d["acct"]["gemm2_bytes"] if fused else 0.0) for d in inputs)
-    t_tensor = g1_flops / (peaks["bf16_tflops_sustained"] * 1e12)
-    t_hbm = g1_bytes / (peaks["hbm_gbs"] * 1e9)
-    if t_tensor > t_hbm:
-        achieved = g1_flops / (g1_us * 1e-6) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "peak_kind": f"bf16 dense, sustained, {peaks['source']}"}
+    us = sum(kernel_us(d, s) for d, s in zip(inputs, stage_us))
+    flops = sum(d["acct"]["gemm1_flops"] * (1.5 if fused else 1.0) for d in inputs)
+    nbytes = sum(d["acct"]["gemm1_bytes"] + (d["acct"]["gemm2_bytes"] if fused else 0.0) for d in inputs)
+    if fused:
+        name = ("fused_small_kernel (gate-up + down in one persistent launch"
+                + ("; the whole forward for " + ", ".join(d["wl"].name for d, m in zip(inputs, mega) if m)
+                   if any(mega) else "") + ")")
     else:
-        achieved = g1_bytes / (g1_us * 1e-6) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "peak_kind": f"HBM copy, {peaks['source']}"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = ("fused_small_kernel (gate-up + down in one persistent launch"
-                      + ("; the whole forward for " + ", ".join(d["wl"].name for d, m in zip(inputs, mega) if m)
-                         if any(mega) else "") + ")"
-                      if fused else "grouped_gemm_kernel (gate-up, SiLU*up epilogue)")
-    roof["algorithmic_per_step"] = g1_flops if roof["bound"] == "tensor" else g1_bytes
-    roof["algorithmic_per_launch"] = roof["algorithmic_per_step"] / len(inputs)
-    roof["algorithmic_bytes_per_launch"] = g1_bytes / len(inputs)
+        paths = {d["path"][0] for d in inputs}
+        name = ("grouped_gemm_pair_kernel (gate-up, CTA pairs, SiLU*up epilogue)" if paths == {1} else
+                "grouped_gemm_kernel (gate-up, SiLU*up epilogue)")
+    return {"name": name, "profiled_us": us, "flops": flops, "bytes": nbytes, "fused": fused,
+            "key": traffic_key(inputs, weights, fused)}
+
+
+def roofline_entry(kern: dict, kernel_us: float, peaks: dict, region_s: float, launches: int) -> dict:
+    """roofline of the dominant kernel: algorithmic work per launch / its time per launch."""
+    t_peak, t_kind = tensor_peak(peaks, region_s)
+    t_tensor = kern["flops"] / (t_peak * 1e12)
+    t_hbm = kern["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    per_launch_us = kernel_us / launches
+    if t_tensor > t_hbm:
+        alg = kern["flops"] / launches
+        r = {"bound": "tensor", "achieved": alg / (per_launch_us * 1e-6) / 1e12, "peak": t_peak,
+             "unit": "TFLOP/s", "peak_kind": t_kind}
+        other = (peaks["bf16_tflops_sustained"] if t_peak == peaks["bf16_tflops"] else peaks["bf16_tflops"])
+        r["frac_vs_other_bf16_peak"] = {"peak": other, "frac": r["achieved"] / other}
+    else:
+        alg = kern["bytes"] / launches
+        r = {"bound": "hbm", "achieved": alg / (per_launch_us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"],
+             "unit": "GB/s", "peak_kind": f"HBM copy ({peaks['source']})"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["kernel"] = kern["name"]
+    r["algorithmic_per_launch"] = alg
+    r["algorithmic_bytes_per_launch"] = kern["bytes"] / launches
+    r["kernel_us_per_launch"] = per_launch_us
+    return r
+
+
+def call_roofline(inputs, ms_per_step: float, peaks: dict, region_s: float) -> dict:
+    """Whole-call roofline: per batch the slower of its FLOPs at the tensor
+    peak and its touched bytes at the copy bandwidth, summed over the step."""
+    t_peak, t_kind = tensor_peak(peaks, region_s)
+    t_roof = 0.0
+    bound = set()
+    for d in inputs:
+        tf = d["acct"]["flops"] / (t_peak * 1e12)
+        tb = d["acct"]["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        t_roof += max(tf, tb)
+        bound.add("tensor" if tf > tb else "hbm")
+    return {"t_roof_us": t_roof * 1e6, "t_step_us": ms_per_step * 1e3, "frac": t_roof * 1e3 / ms_per_step,
+            "bound": "+".join(sorted(bound)), "tensor_peak": t_peak, "tensor_peak_kind": t_kind,
+            "hbm_peak_gbs": peaks["hbm_gbs"]}
+
+
+def stage_dict(d, s):
+    if d["profile"]["megakernel"]:
+        return {"forward_one_kernel": float(sum(s))}
+    return {k: float(v) for k, v in zip(STAGES, s)}
+
+
+def run_ours(args, world, rank, local):
+    from moe_routed_expert_routing_gb300.build import build
+    build()
+    from moe_routed_expert_routing_gb300 import binding as B
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, local)
+    inputs = prepare(B, WORKLOAD_SETS[args.workload], device, args)
+    stream = torch.cuda.Stream(device)
+    peaks = load_peaks()
+
+    # warm-up: W steps in all. The first runs eagerly, outside capture (it sets
+    # the kernels' function attributes); the rest replay the one-step graph
+    # that the timed region replays, so its upload is warm too.
+    with torch.cuda.stream(stream):
+        forward_step(B, inputs, stream)
+    stream.synchronize()
+    check_device_errors(B, inputs, stream)
+    graph = capture(stream, lambda s: forward_step(B, inputs, stream), 1)
+    warmup = max(1, args.warmup)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup - 1):
+            graph.replay()
+    stream.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    clocks.start()
+    time.sleep(0.25)
+    local_ms = replay_timed(stream, graph, args.steps)   # exactly K steps, one graph replay each
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    barrier(world, device)
+    max_ms = max_over_ranks(local_ms, world, device)
+    K = args.steps
+    ms_per_step = max_ms / K
+    check_device_errors(B, inputs, stream)
+
+    # stage shares from the profiled graph (same steps, event nodes between
+    # the kernels); the dominant kernel's time per step is its share of the
+    # profiled step applied to the timed step, so it can never exceed it
+    stage_us, prof_step_us = stage_profile(B, inputs, stream)
+    kern = dominant_kernel(inputs, stage_us, args.weights)
+    share = min(1.0, kern["profiled_us"] / prof_step_us)
+    kernel_us = share * ms_per_step * 1e3
+    region_s = max_ms * 1e-3
+    roof = roofline_entry(kern, kernel_us, peaks, region_s, len(inputs))
+    roof["kernel_time"] = (f"share {share:.4f} of the profiled step ({kern['profiled_us']:.1f} of "
+                           f"{prof_step_us:.1f} us, CUDA events between the stages) times the timed step "
+                           f"({ms_per_step * 1e3:.1f} us)")
+    cap = NCU_TRAFFIC.get(kern["key"]) if kern["key"] else None
     traffic = None
-    key = traffic_key(inputs, args.weights, fused)
-    cap = NCU_TRAFFIC.get(key) if key else None
     if cap and NCU_TRAFFIC["kernel_sha256"] == kernel_sha():
         traffic = cap["traffic"] / cap["algorithmic"] * roof["algorithmic_bytes_per_launch"]
     roof["traffic"] = traffic
     roof["traffic_note"] = (f"ncu dram read+write bytes per launch of {cap['case']}, scaled by algorithmic bytes"
                             if traffic is not None else "no capture for this kernel version/workload")
-    # whole-call roofline: slower of FLOPs at tensor peak and touched bytes at HBM bandwidth
-    t_roof = sum(max(d["acct"]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12),
-                     d["acct"]["bytes"] / (peaks["hbm_gbs"] * 1e9)) for d in inputs)
 
+    flops_step = sum(d["acct"]["flops"] for d in inputs)
+    bytes_step = sum(d["acct"]["bytes"] for d in inputs)
+    value = world * flops_step * K / (max_ms * 1e-3) / 1e12
     e2e = run_e2e(B, inputs, stream, device, args, world)
 
     result = {
@@ -489,7 +561,7 @@ def run_ours(args, world, rank, local):
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": K,
-        "warmup": warm_replays * G,
+        "warmup": warmup,
         "ms_per_step": ms_per_step,
         "higher_is_better": True,
         "scaling": "weak",
@@ -502,41 +574,103 @@ def run_ours(args, world, rank, local):
             "paths": {d["wl"].name: {"path": {1: "tiled (CTA pairs)", 2: "small_m", 3: "tiled (1 CTA)"}[d["path"][0]],
                                      "tile_rows": d["path"][1]} for d in inputs},
             "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB of touched weights+activations per step",
-            "timing": (f"CUDA graph of {G} step(s) replayed {n_replays}x between CUDA events; kernel and stage "
-                       f"times from a second graph of the same steps with stage events, replayed {prof_replays}x"),
+            "timing": (f"one-step CUDA graph replayed {K}x between CUDA events (warm-up: 1 eager step + "
+                       f"{warmup - 1} replays); stage times from a second graph of the same steps with stage "
+                       f"events"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "weights": ("MXFP8 (E4M3 codes + E8M0 scale per 32, expanded to bf16 on chip)"
                         if args.weights == "mxfp8" else "packed (access-ordered)" if args.packed else "row-major"),
         },
-        "us_per_call": {d["wl"].name: float(sum(s)) for d, s in zip(inputs, stage_us)},
-        "profiled_ms_per_step": prof_ms_per_step,
-        "stages_us": {d["wl"].name: ({"forward_one_kernel": float(sum(s))} if d["profile"]["megakernel"]
-                                     else {k: float(v) for k, v in zip(STAGES, s)})
-                      for d, s in zip(inputs, stage_us)},
-        "tflops_per_call": {d["wl"].name: d["acct"]["flops"] / (float(sum(s)) * 1e-6) / 1e12
-                            for d, s in zip(inputs, stage_us)},
-        "call_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": ms_per_step * 1e3,
-                          "frac": t_roof * 1e3 / ms_per_step,
-                          "touched_expert_weights_gb": {d["wl"].name: d["acct"]["touched_experts"] * 3 * d["wl"].H
-                                                        * d["wl"].I * (33 / 32 if args.weights == "mxfp8" else 2)
-                                                        / 1e9 for d in inputs}},
+        "us_per_call": {d["wl"].name: float(sum(s)) * ms_per_step * 1e3 / prof_step_us
+                        for d, s in zip(inputs, stage_us)},
+        "us_per_call_note": "each batch's share of the profiled step applied to the timed step",
+        "profiled_ms_per_step": prof_step_us * 1e-3,
+        "stages_us_profiled": {d["wl"].name: stage_dict(d, s) for d, s in zip(inputs, stage_us)},
+        "tflops_per_step": flops_step / (ms_per_step * 1e-3) / 1e12,
+        "call_roofline": call_roofline(inputs, ms_per_step, peaks, region_s),
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": sum(d["profile"]["kernel_launches"] for d in inputs) * K,
         "clocks": clk,
     }
+    result["call_roofline"]["touched_expert_weights_gb"] = {
+        d["wl"].name: d["acct"]["touched_experts"] * 3 * d["wl"].H * d["wl"].I
+        * (33 / 32 if args.weights == "mxfp8" else 2) / 1e9 for d in inputs}
     if args.weights == "mxfp8":
         result["dtype"] = "bf16 (weights mxfp8)"
+    cpu_inputs = inputs
     if rank == 0 and (args.packed or args.weights == "mxfp8"):
         result["cpu_baseline"] = None
         result["cpu_baseline_note"] = "not run with --packed / --weights mxfp8 (see the row-major bf16 line)"
     elif rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = time_oracle(inputs, args.cpu_seconds,
+        result["cpu_baseline"] = time_oracle(cpu_inputs, args.cpu_seconds,
                                              tokens_cap=args.cpu_tokens if args.cpu_tokens > 0 else None)
         result["cpu_baseline"]["value_note"] = "oracle FLOP rate on the sample; a baseline, not the target"
     elif rank == 0:
         result["cpu_baseline"] = None
+    # the other workloads of the same family, each timed on its own (one GPU only)
+    if world == 1 and args.per_config:
+        del inputs, cpu_inputs, graph
+        torch.cuda.synchronize(device)
+        torch.cuda.empty_cache()
+        result["per_config"] = run_per_config(B, args, device, stream, peaks)
     return result
+
+
+PER_CONFIG = ["prefill", "small", "decode"]
+
+
+def run_per_config(B, args, device, stream, peaks) -> dict:
+    """us/call, TFLOP/s and the call-roofline fraction of each other workload:
+    a graph of G steps (G * step >= ~10 ms) replayed so that ~args.config_ms of
+    work is timed between CUDA events, after two warm replays."""
+    out = {}
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0]))
+    clocks.start()
+    for name in PER_CONFIG:
+        if name == args.workload:
+            continue
+        inputs = prepare(B, WORKLOAD_SETS[name], device, args)
+        with torch.cuda.stream(stream):
+            forward_step(B, inputs, stream)
+        stream.synchronize()
+        check_device_errors(B, inputs, stream)
+        one = capture(stream, lambda s: forward_step(B, inputs, stream), 1)
+        replay_timed(stream, one, 2)
+        est_ms = replay_timed(stream, one, 3) / 3
+        G = max(1, min(20, int(math.ceil(10.0 / max(est_ms, 1e-3)))))
+        g = capture(stream, lambda s: forward_step(B, inputs, stream), G)
+        reps = max(2, int(math.ceil(args.config_ms / (G * est_ms))))
+        replay_timed(stream, g, 2)
+        ms = replay_timed(stream, g, reps)
+        check_device_errors(B, inputs, stream)
+        steps = reps * G
+        ms_per_step = ms / steps
+        stage_us, prof_step_us = stage_profile(B, inputs, stream)
+        kern = dominant_kernel(inputs, stage_us, args.weights)
+        share = min(1.0, kern["profiled_us"] / prof_step_us)
+        region_s = ms * 1e-3
+        roof = roofline_entry(kern, share * ms_per_step * 1e3, peaks, region_s, len(inputs))
+        flops = sum(d["acct"]["flops"] for d in inputs)
+        out[name] = {
+            "workload": " + ".join(d["wl"].describe() for d in inputs),
+            "steps": steps, "graph_steps": G,
+            "ms_per_step": ms_per_step,
+            "us_per_call": {d["wl"].name: float(sum(s)) * ms_per_step * 1e3 / prof_step_us
+                            for d, s in zip(inputs, stage_us)},
+            "tflops": flops / (ms_per_step * 1e-3) / 1e12,
+            "call_roofline": call_roofline(inputs, ms_per_step, peaks, region_s),
+            "dominant_kernel": {k: roof[k] for k in ("kernel", "bound", "achieved", "peak", "unit", "frac",
+                                                       "kernel_us_per_launch")},
+            "stages_us_profiled": {d["wl"].name: stage_dict(d, s) for d, s in zip(inputs, stage_us)},
+            "paths": {d["wl"].name: d["profile"] for d in inputs},
+        }
+        del inputs, one, g
+        torch.cuda.synchronize(device)
+        torch.cuda.empty_cache()
+    out["clocks"] = clocks.stop()
+    return out
 
 
 def run_e2e(B, inputs, stream, device, args, world):
@@ -794,7 +928,11 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOAD_SETS), default="decode")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_SETS), default="large")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip the per-config block (prefill, small, decode timed on their own)")
+    ap.add_argument("--config-ms", type=float, default=150.0,
+                    help="milliseconds of work timed per entry of the per-config block")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens per batch in the CPU sample (0 = auto)")

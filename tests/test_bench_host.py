@@ -69,7 +69,9 @@ def test_call_accounting():
 
 def test_defaults():
     a = bench.parse_args([])
-    assert a.gpus == 1 and a.impl == "ours" and a.workload == "decode" and a.warmup >= 3
+    # the headline is the largest single-GPU configuration (T=8192, E=128, k=8, H=4096, I=1536)
+    assert a.gpus == 1 and a.impl == "ours" and a.workload == "large" and a.warmup >= 3
+    assert a.per_config
 
 
 def test_reference_arm_line_on_tiny(capsys, monkeypatch):
@@ -120,7 +122,7 @@ def test_gpu_arm_json_line_on_tiny(capsys, monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "1")
     monkeypatch.setenv("RANK", "0")
     assert bench.main(["--workload", "tiny", "--steps", "20", "--warmup", "3", "--e2e-steps", "5",
-                       "--cpu-seconds", "0.5"]) == 0
+                       "--cpu-seconds", "0.5", "--no-per-config"]) == 0
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
                 "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
@@ -132,3 +134,25 @@ def test_gpu_arm_json_line_on_tiny(capsys, monkeypatch):
     assert line["e2e"]["h2d_bytes_per_step"] > 0 and line["e2e"]["d2h_bytes_per_step"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(line["clocks"])
+    # warm-up is honoured exactly, and the dominant kernel's time per step
+    # cannot exceed the step
+    assert line["warmup"] == 3 and line["steps"] == 20
+    assert r["kernel_us_per_launch"] * len(line["config"]["batches_per_step"]) <= line["ms_per_step"] * 1e3 + 1e-6
+    assert r["algorithmic_per_launch"] / (r["kernel_us_per_launch"] * 1e-6) / (1e12 if r["unit"] == "TFLOP/s"
+                                                                             else 1e9) == pytest.approx(r["achieved"])
+
+
+@pytest.mark.gpu
+def test_gpu_arm_per_config_block(capsys, monkeypatch):
+    """The per-config block times prefill, the Zipf small batch and decode on
+    their own (shrunk here to E=8, T=16 so that the test is quick)."""
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    assert bench.main(["--workload", "tiny", "--steps", "5", "--warmup", "3", "--e2e-steps", "2",
+                       "--no-cpu-baseline", "--experts", "8", "--tokens", "16", "--config-ms", "5"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    pc = line["per_config"]
+    for name in ("prefill", "small", "decode"):
+        e = pc[name]
+        assert e["ms_per_step"] > 0 and e["tflops"] > 0 and 0 < e["call_roofline"]["frac"]
+        assert e["dominant_kernel"]["kernel_us_per_launch"] <= e["ms_per_step"] * 1e3 + 1e-6
