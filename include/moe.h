@@ -56,7 +56,9 @@ typedef enum moe_status {
     MOE_OK = 0,
     MOE_ERR_NULL = 1,        /* a required pointer is NULL */
     MOE_ERR_SHAPE = 2,       /* a size is out of range or inconsistent */
-    MOE_ERR_ALIGN = 3,       /* H or I not a multiple of the tile, or a misaligned buffer */
+    MOE_ERR_ALIGN = 3,       /* H or I not a multiple of 64 (of 128 for the PACKED and MXFP8 weight
+                                layouts, moe_pack_weights and moe_quantize_weights), or a misaligned
+                                buffer */
     MOE_ERR_WORKSPACE = 4,   /* ws_bytes smaller than moe_workspace_size() */
     MOE_ERR_UNSUPPORTED = 5, /* no GB300-class device, or a path this build lacks */
     MOE_ERR_CUDA = 6         /* a CUDA call failed */
@@ -82,8 +84,8 @@ typedef struct moe_problem {
     int32_t T_max;    /* maximum tokens of one call, >= 1 (static) */
     int32_t E;        /* experts, 1..1024 */
     int32_t k;        /* experts per token, 1..E */
-    int32_t H;        /* hidden size, multiple of 256 */
-    int32_t I;        /* intermediate size, multiple of 128 */
+    int32_t H;        /* hidden size, multiple of 64 (of 128 for PACKED and MXFP8 weights) */
+    int32_t I;        /* intermediate size, multiple of 64 (of 128 for PACKED and MXFP8 weights) */
     int32_t capacity; /* rows of the sorted batch; 0 means T_max*k; else >= T_max*k */
     int32_t path;     /* moe_path_t */
     int32_t weight_layout; /* moe_weight_layout_t of W13 and W2 */
@@ -277,7 +279,9 @@ moe_status_t moe_forward_profiled(const moe_problem_t *problem, const void *x, c
  *  - Returns MOE_ERR_WORKSPACE, before touching the device, when the problem
  *    needs more than the static array: 64 + 2 * ceil(T_max*k / 1024) * E ints.
  *  - The first call on a device looks up the array's device address with
- *    that device current; make that first call before any stream capture.
+ *    that device current, and looks it up again when the device's current
+ *    context has changed since (cudaDeviceReset, a new primary context);
+ *    make the first call in each context before any stream capture.
  *  - All calls share the one array, which keeps the previous call's contents
  *    (each call rewrites what it reads). Calls that overlap on the GPU --
  *    different streams without ordering between them -- race on it: order

@@ -8,7 +8,9 @@
 // code cannot use the array's name as a device address (in host code it
 // names a host-side stand-in), so the address is looked up once per device
 // with cudaGetSymbolAddress, with that device current, and handed to the
-// same kernels moe_dispatch launches.
+// same kernels moe_dispatch launches. The address is kept with the CUDA
+// context it was looked up in and looked up again when the device's current
+// context is another one (after cudaDeviceReset, say).
 #include <mutex>
 
 #include "moe_internal.h"
@@ -22,19 +24,49 @@ constexpr int kMaxDevices = 64;
 
 std::mutex g_setup_mutex;
 int32_t *g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device (set up on first use).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+// The driver's cuCtxGetCurrent, through the runtime's entry-point query (the
+// library links the runtime only).
+CtxGetCurrentFn ctx_get_current_fn()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    }
+    return fn;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up on the
+// first call in each CUDA context of that device.
 moe_status_t scratch_for_current_device(int32_t **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return MOE_ERR_CUDA;
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    if (!get_ctx)
+        return MOE_ERR_CUDA;
+    // no context yet on this thread: the symbol lookup below sets up the
+    // device's primary context, which is then read again
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS)
+        return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+    if (!ctx || !g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
             return MOE_ERR_CUDA;
+        if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx)
+            return MOE_ERR_CUDA;
         g_scratch_ptr[dev] = static_cast<int32_t *>(p);
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return MOE_OK;
@@ -56,8 +88,7 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_problem_t *problem, const
         return MOE_ERR_NULL;
     if (x && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(x_sorted)) & 15u))
         return MOE_ERR_ALIGN;
-    const long long R = static_cast<long long>(p.T_max) * p.k;
-    const long long n_blocks = (R + moe::kDispatchSlotsPerBlock - 1) / moe::kDispatchSlotsPerBlock;
+    const long long n_blocks = moe::dispatch_blocks(p);
     const long long need = kErrWordInts + 2 * n_blocks * p.E;
     if (need > MOE_NOALLOC_SCRATCH_INTS)
         return MOE_ERR_WORKSPACE;
@@ -79,9 +110,8 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_problem_t *problem, const
         return MOE_ERR_CUDA;
     if (!x)
         return MOE_OK;
-    const int cap = p.capacity ? p.capacity : p.T_max * p.k;
-    if (moe::launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, cap, x_sorted, moe::device_sm_count(), s,
-                                moe::use_pdl(p)) != cudaSuccess)
+    if (moe::launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, moe::capacity_of(p), x_sorted,
+                                moe::device_sm_count(), s, moe::use_pdl(p)) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

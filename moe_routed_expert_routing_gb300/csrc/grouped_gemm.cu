@@ -225,10 +225,13 @@ template <bool kGated>
 __device__ __forceinline__ void tiled_epilogue(uint32_t t_row, const GemmArgs &args, int row, bool valid, int n0,
                                                float *scratch)
 {
+    // output columns of this unit inside n_out: a multiple of 64 (n_out and
+    // n0 are), so every column chunk below lies wholly inside or outside
+    const int cols = args.n_out - n0;
     if (kGated) {
         __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(args.out) + static_cast<size_t>(row) * args.n_out + n0;
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
+        for (int c = 0; c < 128 && c < cols; c += 32) {
             uint32_t g[32], v[32];
             tmem_ld_32x32b_x32(t_row + c, g);
             tmem_ld_32x32b_x32(t_row + 128 + c, v);
@@ -259,7 +262,7 @@ __device__ __forceinline__ void tiled_epilogue(uint32_t t_row, const GemmArgs &a
         __half *const y = static_cast<__half *>(args.out);
         bool clipped = false;
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 64) {
+        for (int c = 0; c < 256 && c < cols; c += 64) {
             uint32_t d[64];
             tmem_ld_32x32b_x32(t_row + c, *reinterpret_cast<uint32_t(*)[32]>(d));
             tmem_ld_32x32b_x32(t_row + c + 32, *reinterpret_cast<uint32_t(*)[32]>(d + 32));
@@ -296,7 +299,7 @@ __device__ __forceinline__ void tiled_epilogue(uint32_t t_row, const GemmArgs &a
         float4 *const mine = reinterpret_cast<float4 *>(scratch + lane * 36);
         float *const y = static_cast<float *>(args.out);
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
+        for (int c = 0; c < 256 && c < cols; c += 32) {
             uint32_t d[32];
             tmem_ld_32x32b_x32(t_row + c, d);
             tmem_wait_ld();
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
 
     const uint32_t tmem_base = s_tmem_base;
-    const int NT = args.n_out / C::kOutCols;
+    const int NT = (args.n_out + C::kOutCols - 1) / C::kOutCols;   // the last tile may be partly past n_out
     const int total_units = s_tp[E] * NT * kSplitK;
     const int k_blocks = args.K / kBK / kSplitK;   // K blocks of one unit
 
@@ -540,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 16; ++i) {
                         const int rr = c + i;
                         const int row = t.row0 + rr;
-                        if (rr < t.rows && row >= 0 && row < args.cap) {
+                        if (rr < t.rows && row >= 0 && row < args.cap && col < args.n_out) {
                             const size_t o = static_cast<size_t>(row) * args.n_out + col;
                             if (kGated)
                                 static_cast<__nv_bfloat16 *>(args.out)[o] =
@@ -898,8 +901,8 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
     tc_fence_after();
 
     const uint32_t tmem_base = s_tmem_base;
-    const int NT1 = A1.n_out / 128;                 // gate-up column tiles (I / 128)
-    const int NT2 = A2.n_out / 128;                 // down column tiles (H / 128)
+    const int NT1 = (A1.n_out + 127) / 128;         // gate-up column tiles (ceil(I / 128))
+    const int NT2 = (A2.n_out + 127) / 128;         // down column tiles (ceil(H / 128))
     const int units1 = s_tp[E] * NT1;
     const int total_units = units1 + s_tp[E] * NT2 * kSplitDown;
     const int kb1 = A1.K / C::kWK;
@@ -1217,7 +1220,7 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                 for (int i = 0; i < 16; ++i) {
                     const int rr = c + i;
                     const int row = t.row0 + rr;
-                    if (rr < t.rows && row >= 0 && row < A1.cap) {
+                    if (rr < t.rows && row >= 0 && row < A1.cap && col < (up ? A1.n_out : A2.n_out)) {
                         if (up) {
                             static_cast<__nv_bfloat16 *>(A1.out)[static_cast<size_t>(row) * A1.n_out + col] =
                                 __float2bfloat16_rn(silu_mul(__uint_as_float(g[i]), __uint_as_float(w[i])));
@@ -1369,7 +1372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
 
     const uint32_t tmem_base = s_tmem_base;
-    const int NT = args.n_out / C::kOutCols;
+    const int NT = (args.n_out + C::kOutCols - 1) / C::kOutCols;
     const int cluster_id = blockIdx.x >> 1;
     const int n_clusters = gridDim.x >> 1;
     const int total_units = s_tp[E] * NT;
@@ -1584,7 +1587,7 @@ cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
     a.out_f16 = p.out_f16 ? 1 : 0;
     // Upper bound of the units any routing can produce; no more CTAs than that.
     const long long max_row_tiles = (static_cast<long long>(p.cap) + kTileRows - 1) / kTileRows + p.E;
-    const long long max_units = max_row_tiles * (p.n_out / C::kOutCols) * kSplitK;
+    const long long max_units = max_row_tiles * ((p.n_out + C::kOutCols - 1) / C::kOutCols) * kSplitK;
     const int grid = static_cast<int>(max_units < num_sms ? (max_units < 1 ? 1 : max_units) : num_sms);
     return launch_k(kern, dim3(grid), dim3(kThreads), C::kDynSmem, stream, p.pdl, tm_act, tm_w, a);
 }
@@ -1643,7 +1646,8 @@ cudaError_t run_pair(const GemmProblem &p, int num_sms, cudaStream_t stream)
     a.up_row_offset = p.up_row_offset;
     a.w_packed = p.w_packed ? 1 : 0;
     a.out_f16 = p.out_f16 ? 1 : 0;
-    const long long max_units = ((static_cast<long long>(p.cap) + 255) / 256 + p.E) * (p.n_out / C::kOutCols);
+    const long long max_units =
+        ((static_cast<long long>(p.cap) + 255) / 256 + p.E) * ((p.n_out + C::kOutCols - 1) / C::kOutCols);
     long long clusters = max_units < max_clusters ? max_units : max_clusters;
     if (clusters < 1)
         clusters = 1;
@@ -1775,12 +1779,14 @@ cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *r
         fa.out = static_cast<__nv_bfloat16 *>(mega->out);
         fa.done = counters;
     }
-    // one CTA per SM: every CTA must be resident for the down units' waits
+    // one CTA per SM, all resident at once (the down units and the combine
+    // wait on counts other CTAs publish): a cooperative launch, sized against
+    // the device's occupancy for this kernel
     const long long tiles = (static_cast<long long>(up.cap) + kTileRows - 1) / kTileRows + up.E;
-    const long long max_units = tiles * (up.n_out / 128 + (down.n_out / 128) * kSplitDown);
-    const int grid = static_cast<int>(max_units < num_sms ? (max_units < 1 ? 1 : max_units) : num_sms);
-    return launch_k(kern, dim3(grid), dim3(C::kThreadsCta), dyn_smem, stream, up.pdl, tm_x, tm_w13, tm_h, tm_w2,
-                    fa);
+    const long long max_units = tiles * ((up.n_out + 127) / 128 + ((down.n_out + 127) / 128) * kSplitDown);
+    const long long want = max_units < num_sms ? (max_units < 1 ? 1 : max_units) : num_sms;
+    return launch_k_coresident(kern, want, dim3(C::kThreadsCta), dyn_smem, stream, up.pdl, num_sms, tm_x, tm_w13,
+                               tm_h, tm_w2, fa);
 }
 
 }  // namespace

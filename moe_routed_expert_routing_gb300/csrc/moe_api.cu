@@ -21,8 +21,6 @@ struct Layout {
     size_t err, ready, counters, block_counts, block_base, h, x_sorted, y_sorted, inv, total;
 };
 
-int capacity_of(const moe_problem_t &p) { return p.capacity ? p.capacity : p.T_max * p.k; }
-
 // Workspace header, at fixed offsets so that moe_clear_device_error can clear
 // it without the problem: the error word, then the fused decode kernel's
 // per-expert readiness counts and its two GPU-wide counters. The kernels leave
@@ -46,7 +44,7 @@ Layout layout_of(const moe_problem_t &p)
 {
     const size_t cap = static_cast<size_t>(capacity_of(p));
     const size_t R = static_cast<size_t>(p.T_max) * p.k;
-    const size_t n_blocks = (R + kDispatchSlotsPerBlock - 1) / kDispatchSlotsPerBlock;
+    const size_t n_blocks = static_cast<size_t>(dispatch_blocks(p));
     Layout L;
     L.err = 0;
     L.ready = kReadyOffset;
@@ -67,6 +65,9 @@ Layout layout_of(const moe_problem_t &p)
     L.total = o;
     return L;
 }
+
+// H and I are whole 128-row weight tiles (and 128-wide K blocks)
+bool tiles_of_128(const moe_problem_t &p) { return p.H % 128 == 0 && p.I % 128 == 0; }
 
 moe_status_t check_problem(const moe_problem_t *p)
 {
@@ -89,7 +90,12 @@ moe_status_t check_problem(const moe_problem_t *p)
         return MOE_ERR_SHAPE;
     if (static_cast<long long>(p->E) * 2 * p->I > (1LL << 31) || static_cast<long long>(p->E) * p->H > (1LL << 31))
         return MOE_ERR_SHAPE;
-    if (p->H % 256 != 0 || p->I % 128 != 0)
+    // 64-element K blocks (one 128-byte swizzle row) and 64-column output
+    // granularity; the PACKED and MXFP8 layouts are built of 128-row weight
+    // tiles (and, for MXFP8, 128-wide K blocks), so they need multiples of 128
+    if (p->H % 64 != 0 || p->I % 64 != 0)
+        return MOE_ERR_ALIGN;
+    if (p->weight_layout != MOE_WEIGHTS_ROW_MAJOR && !tiles_of_128(*p))
         return MOE_ERR_ALIGN;
     return MOE_OK;
 }
@@ -171,7 +177,7 @@ bool down_split_k(const moe_problem_t &p, int path, int tile_rows, int sms)
         return false;
     const long long R_max = static_cast<long long>(p.T_max) * p.k;
     const long long max_experts = R_max < p.E ? R_max : p.E;
-    return max_experts * (p.H / 128) < 4LL * sms;
+    return max_experts * ((p.H + 127) / 128) < 4LL * sms;
 }
 
 // Enqueue both GEMMs. With y_zeroed false and a split down GEMM, y is
@@ -336,6 +342,14 @@ int device_sm_count()
 }
 
 moe_status_t validate_problem(const moe_problem_t *problem) { return check_problem(problem); }
+
+int capacity_of(const moe_problem_t &p) { return p.capacity ? p.capacity : p.T_max * p.k; }
+
+long long dispatch_blocks(const moe_problem_t &p)
+{
+    const long long R = static_cast<long long>(p.T_max) * p.k;
+    return (R + kDispatchSlotsPerBlock - 1) / kDispatchSlotsPerBlock;
+}
 
 moe_status_t validate_device() { return check_device(); }
 
@@ -593,7 +607,7 @@ moe_status_t moe_pack_weights(const moe_problem_t *problem, const void *W13, con
     const moe_problem_t &p = *problem;
     if (!W13 || !W2 || !W13_packed || !W2_packed)
         return MOE_ERR_NULL;
-    if (!aligned16(W13) || !aligned16(W2) || !aligned16(W13_packed) || !aligned16(W2_packed))
+    if (!tiles_of_128(p) || !aligned16(W13) || !aligned16(W2) || !aligned16(W13_packed) || !aligned16(W2_packed))
         return MOE_ERR_ALIGN;
     if ((st = check_device()) != MOE_OK)
         return st;
@@ -631,7 +645,7 @@ moe_status_t moe_quantize_weights(const moe_problem_t *problem, const void *W13,
     const moe_problem_t &p = *problem;
     if (!W13 || !W2 || !W13_mx || !W2_mx)
         return MOE_ERR_NULL;
-    if (!aligned16(W13) || !aligned16(W2) || !aligned16(W13_mx) || !aligned16(W2_mx))
+    if (!tiles_of_128(p) || !aligned16(W13) || !aligned16(W2) || !aligned16(W13_mx) || !aligned16(W2_mx))
         return MOE_ERR_ALIGN;
     if ((st = check_device()) != MOE_OK)
         return st;
@@ -673,7 +687,8 @@ const char *moe_status_string(moe_status_t status)
     case MOE_ERR_SHAPE:
         return "MOE_ERR_SHAPE: a size is out of range or inconsistent";
     case MOE_ERR_ALIGN:
-        return "MOE_ERR_ALIGN: H % 256, I % 128 or buffer alignment violated";
+        return "MOE_ERR_ALIGN: H or I not a multiple of 64 (of 128 for the PACKED and MXFP8 weight layouts), "
+               "or a misaligned buffer";
     case MOE_ERR_WORKSPACE:
         return "MOE_ERR_WORKSPACE: workspace smaller than moe_workspace_size()";
     case MOE_ERR_UNSUPPORTED:

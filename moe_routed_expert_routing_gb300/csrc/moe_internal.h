@@ -54,6 +54,49 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// ---- kernels whose CTAs wait on one another ----
+// Such a kernel is correct only if every CTA of its grid is resident at
+// once. The launch asks for that guarantee (cudaLaunchAttributeCooperative:
+// the grid starts only when all of its CTAs fit, and a grid that could never
+// fit is refused), and the host first sizes the grid against the occupancy
+// the device reports for the kernel. Pure host arithmetic: the grid to
+// launch for `want` CTAs when `per_sm` CTAs fit on one of `sms` SMs, or 0
+// when none fits (the launch is then refused before it is made).
+inline int coresident_grid(long long want, int per_sm, int sms)
+{
+    if (want < 1 || per_sm < 1 || sms < 1)
+        return 0;
+    const long long most = static_cast<long long>(per_sm) * sms;
+    return static_cast<int>(want < most ? want : most);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k_coresident(void (*kernel)(KArgs...), long long want_ctas, dim3 block, size_t smem,
+                                cudaStream_t stream, bool pdl, int sms, Args &&...args)
+{
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, static_cast<int>(block.x),
+                                                                  smem);
+    if (e != cudaSuccess)
+        return e;
+    const int grid = coresident_grid(want_ctas, per_sm, sms);
+    if (grid < 1)
+        return cudaErrorCooperativeLaunchTooLarge;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ---- dispatch (dispatch.cu) ----
 cudaError_t launch_dispatch(const int32_t *topk_ids, const int32_t *d_num_tokens, int T_max, int k, int E,
                             int32_t *block_counts, int32_t *block_base, int32_t *expert_offsets,
@@ -137,6 +180,10 @@ int device_sm_count();
 
 // host validation shared by the entry points (moe_api.cu)
 moe_status_t validate_problem(const moe_problem_t *problem);
+// rows of the sorted batch: the problem's capacity, or T_max * k when it is 0
+int capacity_of(const moe_problem_t &problem);
+// blocks of the multi-block dispatch: one per kDispatchSlotsPerBlock routed slots
+long long dispatch_blocks(const moe_problem_t &problem);
 moe_status_t validate_device();
 // whether launches for this problem use programmatic dependent launch (M-small path)
 bool use_pdl(const moe_problem_t &problem);

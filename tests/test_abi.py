@@ -174,3 +174,28 @@ def test_missing_library_fails_loudly(lib, tmp_path, monkeypatch):
     monkeypatch.setattr(lib, "lib_path", lambda: str(tmp_path / "absent" / "libmoe.so"))
     with pytest.raises(RuntimeError, match="not found"):
         lib.moe_workspace_size(lib.Problem.make(16, 8, 2, 256, 128))
+
+
+def test_hidden_and_intermediate_multiples_of_64(lib):
+    """H and I need only be multiples of 64 (FlashInfer moe_ep page, Shape
+    Coverage & Guardrails: hidden and intermediate sizes that are multiples
+    of 64, e.g. 2880); the PACKED and MXFP8 layouts, built of 128-row weight
+    tiles, keep multiples of 128 and are refused otherwise, before any CUDA call."""
+    P = lib.Problem.make
+    for H, I in [(448, 192), (2880, 2880), (64, 64), (7168, 3072)]:
+        assert lib.moe_workspace_size(P(64, 8, 2, H, I)) > 0
+    for H, I in [(480, 192), (448, 160), (32, 64)]:
+        with pytest.raises(lib.MoeError) as ei:
+            lib.moe_workspace_size(P(64, 8, 2, H, I))
+        assert ei.value.status == 3
+    for layout in (lib.MOE_WEIGHTS_PACKED, lib.MOE_WEIGHTS_MXFP8):
+        for H, I in [(448, 256), (512, 192)]:
+            with pytest.raises(lib.MoeError) as ei:
+                lib.moe_workspace_size(P(64, 8, 2, H, I, weight_layout=layout))
+            assert ei.value.status == 3
+        assert lib.moe_workspace_size(P(64, 8, 2, 512, 256, weight_layout=layout)) > 0
+    so = lib.load_library()
+    q = P(64, 8, 2, 448, 192)
+    fake = 1 << 40   # never dereferenced: refused before the device is touched
+    assert so.moe_pack_weights(ctypes.byref(q), fake, fake, fake, fake, None) == 3
+    assert so.moe_quantize_weights(ctypes.byref(q), fake, fake, fake, fake, None) == 3

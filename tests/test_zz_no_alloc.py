@@ -3,8 +3,9 @@ allocate device memory (a runtime whose device memory is fixed at start-up,
 or code under stream capture, where cudaMalloc is illegal). It keeps its
 scratch in a static device array inside libmoe.so instead of a caller
 workspace. Its results must equal moe_dispatch's, call after call, since all
-calls share that one array. Collected last so that a failure here does not
-stop the rest of a run early; it also passes alone in a fresh process.
+calls share that one array, and the oracle's dispatch bit for bit. Collected
+last so that a failure here does not stop the rest of a run early; it also
+passes alone in a fresh process.
 """
 from __future__ import annotations
 
@@ -12,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wlm
 
 pytestmark = pytest.mark.gpu
@@ -88,3 +90,26 @@ def test_noalloc_dispatch_rejects_problems_beyond_its_static_scratch(B):
     with pytest.raises(B.MoeError) as ei:
         B.moe_dispatch_noalloc(p, fake, fake, fake, fake)
     assert ei.value.status == 4
+
+
+def test_noalloc_dispatch_matches_oracle(B):
+    """Bit-exact against the oracle's stable dispatch on its own, at the
+    prefill shape (12 dispatch blocks), with a dropped slot and experts 0..4
+    given 1000 more slots each across two blocks (slot 5 of those tokens may
+    repeat one of them: duplicates are two rows, as in the oracle)."""
+    wl = wlm.WORKLOADS["prefill"]
+    ids_np, _ = wlm.make_routing(wl)
+    ids_np[7, 2] = -1
+    ids_np[100:1100, :5] = np.arange(5, dtype=np.int32)   # experts 0..4 each hold 1000 more slots in a row
+    ids = torch.from_numpy(ids_np).cuda()
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I)
+    for _ in range(2):
+        got = _outputs(p)
+        B.moe_dispatch_noalloc(p, ids, got[0], got[1], got[2])
+        torch.cuda.synchronize()
+        _, o_off, o_perm, o_inv, n_bad = oracle.dispatch(ids_np, wl.E)
+        n_rows = int(o_off[-1])
+        assert n_bad == 0 and n_rows == wl.R - 1
+        assert np.array_equal(got[0].cpu().numpy(), o_off)
+        assert np.array_equal(got[1].cpu().numpy()[:n_rows], o_perm[:n_rows])
+        assert np.array_equal(got[2].cpu().numpy(), o_inv)
