@@ -1303,6 +1303,22 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
 // CTA 0's full barrier (2 arrivals + both CTAs' bytes); CTA 0's commits are
 // multicast to both CTAs' empty / TMEM-full barriers; both epilogues release
 // the accumulator on CTA 0's TMEM-empty barrier.
+//
+// Swapped last tiles. The last row tile of an expert holds count % 256 rows;
+// on a 256-row tile those past the count are padding the tensor cores still
+// multiply (11% of the MMAs of the large-batch shape, where a quarter of the
+// experts hold just over 512 rows). A last tile of at most 128 rows runs
+// swapped instead: the weights go on the MMA's M side (128 weight rows per
+// CTA) and the tile's rows on N, rounded up to 64 (N/2 per CTA, loaded with a
+// 32-row box), so the MMAs and the activation loads shrink with the rows.
+// Each CTA's TMEM then holds its 128 weight rows x N rows; the epilogue
+// stores it transposed (lane = output column). Down: the CTA's 128 W2 rows
+// are its 128 output columns. Gate-up: the CTA's 128 weight rows are 64 gate
+// rows and the matching 64 up rows (two 64-row boxes), so SiLU(gate)*up pairs
+// TMEM lane i with lane i + 64: epilogue warps 6 and 7 hand their up values to
+// warps 4 and 5 through shared memory, 16 rows at a time, on a pair of
+// mbarriers (bounded waits). Row-major weights only (the PACKED images are
+// whole 128-row tiles).
 template <bool kGated, int kStages>
 struct PairCfg {
     static constexpr int kHalfBytes = 128 * 128;                 // 128 rows x 64 bf16
@@ -1312,14 +1328,27 @@ struct PairCfg {
     static constexpr int kAccCols = 256;
     static constexpr int kTmemCols = 512;
     static constexpr uint32_t kIdesc = idesc_bf16_f32(256, 256);
-    static constexpr int kEpiScratch = kGated ? 0 : 4 * 32 * 36 * 4;   // fp32 output: transpose scratch
+    static constexpr int kSwapRows = 128;     // last tiles with at most this many rows run swapped
+    static constexpr int kSwapBox = 32;       // activation rows of one TMA box of a swapped unit
+    static constexpr int kXchStride = 17;     // gate-up exchange: floats per lane (16 rows + 1 against bank conflicts)
+    // down: fp32 transpose scratch; gate-up: the up values of two warps, 32 lanes x 16 rows each
+    static constexpr int kEpiScratch = kGated ? 2 * 32 * kXchStride * 4 : 4 * 32 * 36 * 4;
     static constexpr int kDynSmem = 1024 + kStages * kStageBytes + kEpiScratch;
 };
+
+// Rows on the MMA's N side of a swapped unit (a multiple of 64: each CTA
+// loads whole 32-row boxes), or 0 for a unit that runs as usual.
+template <int kSwapRows>
+__device__ __forceinline__ int swap_tokens(const Unit &t, bool swap_ok)
+{
+    return (swap_ok && t.rows <= kSwapRows) ? ((t.rows + 63) & ~63) : 0;
+}
 
 template <bool kGated, int kStages>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
-                             const GemmArgs args)
+                             const __grid_constant__ CUtensorMap tm_act_swap,
+                             const __grid_constant__ CUtensorMap tm_w_swap, const GemmArgs args)
 {
     using C = PairCfg<kGated, kStages>;
     extern __shared__ uint8_t smem_raw[];
@@ -1328,6 +1357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(8) uint64_t bar_tfull[2];
     __shared__ __align__(8) uint64_t bar_tempty[2];       // used in CTA 0
     __shared__ __align__(8) uint64_t bar_drain;           // used in CTA 0
+    __shared__ __align__(8) uint64_t bar_xfull[2];        // gate-up, swapped units: up values handed over
+    __shared__ __align__(8) uint64_t bar_xempty[2];       // ... and taken
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
     __shared__ int s_off[kMaxExperts + 1];
@@ -1348,6 +1379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bar_tfull[b]), 1);
             mbar_init(smem_u32(&bar_tempty[b]), 8);   // 4 epilogue warps x 2 CTAs
+            mbar_init(smem_u32(&bar_xfull[b]), 1);
+            mbar_init(smem_u32(&bar_xempty[b]), 1);
         }
         mbar_init(smem_u32(&bar_drain), 1);
         s_abort = 0;
@@ -1356,6 +1389,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_act);
         tma_prefetch_desc(&tm_w);
+        if (!args.w_packed) {
+            tma_prefetch_desc(&tm_act_swap);
+            tma_prefetch_desc(&tm_w_swap);
+        }
     }
     if (warp == 2) {
         tmem_alloc_pair(smem_u32(&s_tmem_base), C::kTmemCols);
@@ -1377,6 +1414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_clusters = gridDim.x >> 1;
     const int total_units = s_tp[E] * NT;
     const int k_blocks = args.K / kBK;
+    const bool swap_ok = !args.w_packed;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -1387,9 +1425,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int u = cluster_id; ok && u < total_units; u += n_clusters) {
             const Unit t = decode_unit<false, C::kPairRows, C::kOutCols>(u, s_off, s_tp, E, NT);
+            const int n_swap = swap_tokens<C::kSwapRows>(t, swap_ok);
             const int a_row = t.row0 + 128 * static_cast<int>(rank);
             const int w_row = kGated ? t.e * args.w_rows_per_expert + (rank ? args.up_row_offset : 0) + t.n0
                                      : t.e * args.w_rows_per_expert + t.n0 + 128 * static_cast<int>(rank);
+            // swapped: this CTA's 128 weight rows (gate-up: 64 gate + the 64 matching up rows) in the A half,
+            // its n_swap / 2 activation rows in the B half
+            const int half = n_swap >> 1;
+            const int sw_row = kGated ? t.e * args.w_rows_per_expert + t.n0 + 64 * static_cast<int>(rank)
+                                      : w_row;
+            const int sa_row = t.row0 + half * static_cast<int>(rank);
             if (lane == 0) {
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, abort_flag, args.wait_limit_ns)) {
@@ -1400,10 +1445,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_dst = smem_u32(smem + stage * C::kStageBytes);
                     const uint32_t b_dst = a_dst + C::kHalfBytes;
                     const int kc = kb * kBK;
-                    mbar_arrive_expect_tx_cluster(full0, C::kStageBytes);
-                    tma_load_2d_pair(a_dst, &tm_act, full0, kc, a_row, pol_a);
-                    const int2 wc = weight_coords(args, kGated, w_row, kb);
-                    tma_load_2d_pair(b_dst, &tm_w, full0, wc.x, wc.y, pol_w);
+                    if (n_swap == 0) {
+                        mbar_arrive_expect_tx_cluster(full0, C::kStageBytes);
+                        tma_load_2d_pair(a_dst, &tm_act, full0, kc, a_row, pol_a);
+                        const int2 wc = weight_coords(args, kGated, w_row, kb);
+                        tma_load_2d_pair(b_dst, &tm_w, full0, wc.x, wc.y, pol_w);
+                    } else {
+                        mbar_arrive_expect_tx_cluster(full0, C::kHalfBytes + half * 128);
+                        if (kGated) {
+                            tma_load_2d_pair(a_dst, &tm_w_swap, full0, kc, sw_row, pol_w);
+                            tma_load_2d_pair(a_dst + 64 * 128, &tm_w_swap, full0, kc, sw_row + args.up_row_offset,
+                                             pol_w);
+                        } else {
+                            tma_load_2d_pair(a_dst, &tm_w, full0, kc, sw_row, pol_w);
+                        }
+                        for (int j = 0; j < half; j += C::kSwapBox)
+                            tma_load_2d_pair(b_dst + j * 128, &tm_act_swap, full0, kc, sa_row + j, pol_a);
+                    }
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -1423,6 +1481,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = cluster_id; ok && u < total_units; u += n_clusters, ++local) {
                 const int buf = local & 1;
                 const uint32_t use = (local >> 1) & 1;
+                const int n_swap =
+                    swap_tokens<C::kSwapRows>(decode_unit<false, C::kPairRows, C::kOutCols>(u, s_off, s_tp, E, NT),
+                                              swap_ok);
+                const uint32_t idesc = n_swap ? idesc_bf16_f32(256, n_swap) : C::kIdesc;
                 if (!mbar_wait_bounded(smem_u32(&bar_tempty[buf]), use ^ 1u, abort_flag, args.wait_limit_ns)) {
                     ok = false;
                     break;
@@ -1441,7 +1503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
                         const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                         umma_bf16_pair(d_tmem, smem_desc_kmajor_sw128(a_addr + kk * 32),
-                                       smem_desc_kmajor_sw128(b_addr + kk * 32), C::kIdesc, acc);
+                                       smem_desc_kmajor_sw128(b_addr + kk * 32), idesc, acc);
                     }
                     umma_commit_pair(smem_u32(&bar_empty[stage]), 0x3);
                     if (++stage == kStages) {
@@ -1461,9 +1523,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp - 4;
+        float *const scratch = reinterpret_cast<float *>(smem + kStages * C::kStageBytes);
+        uint32_t xk = 0;   // gate-up exchanges of this warp so far (their mbarrier phases)
         int local = 0;
         for (int u = cluster_id; u < total_units; u += n_clusters, ++local) {
             const Unit t = decode_unit<false, C::kPairRows, C::kOutCols>(u, s_off, s_tp, E, NT);
+            const int n_swap = swap_tokens<C::kSwapRows>(t, swap_ok);
             const int buf = local & 1;
             const uint32_t use = (local >> 1) & 1;
             int ok = 0;
@@ -1474,10 +1539,91 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + buf * C::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
-            const int r = 128 * static_cast<int>(rank) + q * 32 + lane;   // row within the 256-row pair tile
-            const int row = t.row0 + r;
-            tiled_epilogue<kGated>(t_row, args, row, r < t.rows && row >= 0 && row < args.cap, t.n0,
-                                   reinterpret_cast<float *>(smem + kStages * C::kStageBytes) + q * 32 * 36);
+            if (n_swap == 0) {
+                const int r = 128 * static_cast<int>(rank) + q * 32 + lane;   // row within the 256-row pair tile
+                const int row = t.row0 + r;
+                tiled_epilogue<kGated>(t_row, args, row, r < t.rows && row >= 0 && row < args.cap, t.n0,
+                                       scratch + q * 32 * 36);
+            } else if (!kGated) {
+                // lane = W2 row = output column; TMEM columns = the unit's rows
+                const int col = t.n0 + 128 * static_cast<int>(rank) + q * 32 + lane;
+                const bool col_ok = col < args.n_out;
+                bool clipped = false;
+#pragma unroll 1
+                for (int c = 0; c < n_swap && c < t.rows; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(t_row + c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (!col_ok || c + i >= t.rows)
+                            continue;
+                        const size_t o = static_cast<size_t>(t.row0 + c + i) * args.n_out + col;
+                        const float y = __uint_as_float(v[i]);
+                        if (args.out_f16) {
+                            // the rounding of the unswapped epilogue: to nearest, saturating at +-65504
+                            clipped |= fabsf(y) > 65504.f;
+                            uint32_t h2;
+                            asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(0.f), "f"(y));
+                            static_cast<uint16_t *>(args.out)[o] = static_cast<uint16_t>(h2 & 0xffffu);
+                        } else {
+                            static_cast<float *>(args.out)[o] = y;
+                        }
+                    }
+                }
+                if (__any_sync(kFull, clipped) && lane == 0)
+                    atomicOr(args.err, MOE_DEVERR_Y_RANGE);
+            } else {
+                // lanes 0..63: gate rows, lanes 64..127: the matching up rows, of this CTA's 64 output
+                // columns; warp q + 2 hands its up values to warp q, 16 rows at a time
+                const int pair = q & 1;
+                float *const xch = scratch + pair * 32 * C::kXchStride;
+                const uint32_t xfull = smem_u32(&bar_xfull[pair]);
+                const uint32_t xempty = smem_u32(&bar_xempty[pair]);
+                const int col = t.n0 + 64 * static_cast<int>(rank) + pair * 32 + lane;
+                const bool col_ok = col < args.n_out;
+                bool good = true;
+#pragma unroll 1
+                for (int c = 0; c < n_swap && c < t.rows; c += 16, ++xk) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(t_row + c, v);
+                    tmem_wait_ld();
+                    int w_ok = 0;
+                    if (lane == 0)
+                        w_ok = mbar_wait_bounded(q >= 2 ? xempty : xfull, q >= 2 ? ((xk & 1u) ^ 1u) : (xk & 1u),
+                                                 abort_flag, args.wait_limit_ns)
+                                   ? 1
+                                   : 0;
+                    if (!__shfl_sync(kFull, w_ok, 0)) {
+                        good = false;
+                        break;
+                    }
+                    if (q >= 2) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            xch[lane * C::kXchStride + i] = __uint_as_float(v[i]);
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(xfull);
+                    } else {
+                        float up[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            up[i] = xch[lane * C::kXchStride + i];
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(xempty);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (col_ok && c + i < t.rows)
+                                static_cast<__nv_bfloat16 *>(args.out)[static_cast<size_t>(t.row0 + c + i) *
+                                                                           args.n_out + col] =
+                                    __float2bfloat16_rn(silu_mul(__uint_as_float(v[i]), up[i]));
+                    }
+                }
+                if (!good)
+                    break;
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
@@ -1627,9 +1773,19 @@ cudaError_t run_pair(const GemmProblem &p, int num_sms, cudaStream_t stream)
         max_clusters = n > 0 ? n : 1;
         attr_done_for_device = dev;
     }
-    CUtensorMap tm_act, tm_w;
+    CUtensorMap tm_act, tm_w, tm_act_swap, tm_w_swap;
     if (!make_map(&tm_act, p.act, static_cast<uint64_t>(p.act_rows), static_cast<uint64_t>(p.K), 128) ||
         !make_weight_map(&tm_w, p))
+        return cudaErrorInvalidValue;
+    // swapped last tiles (row-major weights): activation rows in 32-row boxes;
+    // gate-up weights in 64-row boxes (64 gate + 64 up rows per CTA)
+    tm_act_swap = tm_act;
+    tm_w_swap = tm_w;
+    if (!p.w_packed &&
+        (!make_map(&tm_act_swap, p.act, static_cast<uint64_t>(p.act_rows), static_cast<uint64_t>(p.K),
+                   C::kSwapBox) ||
+         (kGated && !make_map(&tm_w_swap, p.w, static_cast<uint64_t>(p.E) * p.w_rows_per_expert,
+                              static_cast<uint64_t>(p.K), 64))))
         return cudaErrorInvalidValue;
     GemmArgs a;
     a.expert_offsets = p.expert_offsets;
@@ -1652,7 +1808,7 @@ cudaError_t run_pair(const GemmProblem &p, int num_sms, cudaStream_t stream)
     if (clusters < 1)
         clusters = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-    return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, a);
+    return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, tm_act_swap, tm_w_swap, a);
 }
 
 
