@@ -609,7 +609,7 @@ def run_ours(args, world, rank, local):
     elif rank == 0:
         result["cpu_baseline"] = None
     # the other workloads of the same family, each timed on its own (one GPU only)
-    if world == 1 and args.per_config:
+    if world == 1 and args.per_config and args.weights == "bf16":
         del inputs, cpu_inputs, graph
         torch.cuda.synchronize(device)
         torch.cuda.empty_cache()
