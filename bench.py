@@ -674,10 +674,14 @@ def run_per_config(B, args, device, stream, peaks) -> dict:
 
 
 def run_e2e(B, inputs, stream, device, args, world):
-    """Same metric through the public call with pinned host inputs/outputs
-    copied every step. A step's inputs of all batches (x, ids, weights) sit in
-    one pinned staging buffer and go over in one copy, and the outputs come
-    back in one copy, as a caller batching a step's traffic would do."""
+    """Same metric through the public call, with every step's inputs copied
+    from pinned host memory to the device and its outputs back, inside the
+    timed region. A step's inputs of all batches (x, ids, weights) sit in one
+    pinned staging buffer and go over in one copy; the outputs come back in
+    one copy. The copies run on a stream of their own, double-buffered, as a
+    serving loop overlaps them: step i+1's inputs go over while step i
+    computes, and step i's outputs come back while step i+1 computes. The
+    region ends when the last step's outputs are on the host."""
     def aligned(n):
         return (n + 255) // 256 * 256
 
@@ -691,49 +695,79 @@ def run_e2e(B, inputs, stream, device, args, world):
         out_parts.append((d, o_out))
         o_out += aligned(d["bufs"].out.numel() * d["bufs"].out.element_size())
     host_in = torch.empty(o_in, dtype=torch.uint8).pin_memory()
-    dev_in = torch.empty(o_in, dtype=torch.uint8, device=device)
     host_out = torch.empty(o_out, dtype=torch.uint8).pin_memory()
-    dev_out = torch.empty(o_out, dtype=torch.uint8, device=device)
-    views = {}
+    dev_in = [torch.empty(o_in, dtype=torch.uint8, device=device) for _ in range(2)]
+    dev_out = [torch.empty(o_out, dtype=torch.uint8, device=device) for _ in range(2)]
+    views = [{}, {}]
     for d, name, off, t in in_parts:
         nbytes = t.numel() * t.element_size()
         host_in[off:off + nbytes].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
-        views[(id(d), name)] = dev_in[off:off + nbytes].view(t.dtype).view(t.shape)
+        for b in range(2):
+            views[b][(id(d), name)] = dev_in[b][off:off + nbytes].view(t.dtype).view(t.shape)
     for d, off in out_parts:
         o = d["bufs"].out
-        views[(id(d), "out")] = dev_out[off:off + o.numel() * o.element_size()].view(o.dtype).view(o.shape)
+        for b in range(2):
+            views[b][(id(d), "out")] = dev_out[b][off:off + o.numel() * o.element_size()].view(o.dtype).view(o.shape)
     steps = max(1, min(args.steps, args.e2e_steps))
     h2d, d2h = o_in, o_out
+    copy = torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
 
-    def one_step():
-        dev_in.copy_(host_in, non_blocking=True)
-        for d in inputs:
-            v = lambda name: views[(id(d), name)]
-            B.moe_forward(d["problem"], v("x"), v("ids"), v("w"), d["W13"], d["W2"], d["bufs"].expert_offsets,
-                          d["bufs"].perm, v("out"), d["bufs"].ws, stream=stream)
-        host_out.copy_(dev_out, non_blocking=True)
+    def h2d_copy(b):
+        with torch.cuda.stream(copy):
+            dev_in[b].copy_(host_in, non_blocking=True)
+            ev_in[b].record(copy)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            one_step()
-    stream.synchronize()
+    def compute(b):
+        stream.wait_event(ev_in[b])
+        with torch.cuda.stream(stream):
+            for d in inputs:
+                v = views[b]
+                B.moe_forward(d["problem"], v[(id(d), "x")], v[(id(d), "ids")], v[(id(d), "w")], d["W13"], d["W2"],
+                              d["bufs"].expert_offsets, d["bufs"].perm, v[(id(d), "out")], d["bufs"].ws,
+                              stream=stream)
+            ev_done[b].record(stream)
+
+    def d2h_copy(b):
+        copy.wait_event(ev_done[b])
+        with torch.cuda.stream(copy):
+            host_out.copy_(dev_out[b], non_blocking=True)
+
+    def run(n):
+        # copy stream order: in(0); in(1), out(0); in(2), out(1); ... so that in(i+1)
+        # follows out(i-1), which follows step i-1's compute: buffer i+1 % 2 is free
+        h2d_copy(0)
+        for i in range(n):
+            compute(i % 2)
+            if i + 1 < n:
+                h2d_copy((i + 1) % 2)
+            d2h_copy(i % 2)
+
+    run(3)
+    torch.cuda.synchronize(device)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     barrier(world, device)
     torch.cuda.synchronize(device)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(steps):
-            one_step()
-        t1.record(stream)
+    t0.record(copy)
+    run(steps)
+    t1.record(copy)
     torch.cuda.synchronize(device)
     ms = max_over_ranks(t0.elapsed_time(t1), world, device)
+    # the last step's outputs, as the host received them, equal the timed graph's
+    for d, off in out_parts:
+        o = d["bufs"].out
+        got = host_out[off:off + o.numel() * o.element_size()]
+        if not torch.equal(got, o.contiguous().view(-1).view(torch.uint8).cpu()):
+            raise RuntimeError(f"e2e output of {d['wl'].name} differs from the graph's")
     flops_step = sum(d["acct"]["flops"] for d in inputs)
     return {"value": world * flops_step * steps / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": ms / steps,
-            "api": "moe_forward (eager, C ABI); each step one pinned host->device copy of all inputs and one "
-                   "device->host copy of all outputs"}
+            "api": "moe_forward (eager, C ABI); each step one pinned host->device copy of all its inputs and one "
+                   "device->host copy of all its outputs, on a copy stream double-buffered against the compute "
+                   "stream (step i+1's inputs and step i-1's outputs move while step i computes)"}
 
 
 # ----------------------------------------------------------------------------- token sweep
