@@ -78,28 +78,62 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Y *__res
         const int32_t *inv_t = inv + static_cast<size_t>(t) * k;
         const float *w_t = w + static_cast<size_t>(t) * k;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        // loads of up to four routed rows are issued together, then summed in
-        // ascending j, so the sum is the same sequence of roundings as a plain loop
-        for (int j0 = 0; j0 < k; j0 += 4) {
-            float f[4][8];
-            int row[4];
-            float wj[4];
+        if constexpr (sizeof(Y) == 2) {
+            // fp16 y: the loads of up to eight routed rows are issued together
+            // and kept as raw 16-byte vectors (4 registers a row, where widened
+            // rows would take 8), so twice the bytes are in flight for the same
+            // registers; then widened and summed in ascending j as below
+            for (int j0 = 0; j0 < k; j0 += 8) {
+                uint4 raw[8];
+                int row[8];
+                float wj[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                row[q] = (j0 + q < k) ? __ldg(inv_t + j0 + q) : -1;
-                wj[q] = (j0 + q < k) ? __ldg(w_t + j0 + q) : 0.f;
+                for (int q = 0; q < 8; ++q) {
+                    row[q] = (j0 + q < k) ? __ldg(inv_t + j0 + q) : -1;
+                    wj[q] = (j0 + q < k) ? __ldg(w_t + j0 + q) : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (row[q] >= 0)
+                        raw[q] = __ldg(reinterpret_cast<const uint4 *>(y_sorted + (static_cast<size_t>(row[q]) *
+                                                                                    vec_per_row + c) * 8));
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (row[q] < 0)
+                        continue;
+                    const uint32_t u[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[i]));
+                        acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(wj[q], f.x));
+                        acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(wj[q], f.y));
+                    }
+                }
             }
+        } else {
+            // loads of up to four routed rows are issued together, then summed in
+            // ascending j, so the sum is the same sequence of roundings as a plain loop
+            for (int j0 = 0; j0 < k; j0 += 4) {
+                float f[4][8];
+                int row[4];
+                float wj[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (row[q] >= 0)
-                    load8(y_sorted, (static_cast<size_t>(row[q]) * vec_per_row + c) * 8, f[q]);
+                for (int q = 0; q < 4; ++q) {
+                    row[q] = (j0 + q < k) ? __ldg(inv_t + j0 + q) : -1;
+                    wj[q] = (j0 + q < k) ? __ldg(w_t + j0 + q) : 0.f;
+                }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (row[q] < 0)
-                    continue;
+                for (int q = 0; q < 4; ++q)
+                    if (row[q] >= 0)
+                        load8(y_sorted, (static_cast<size_t>(row[q]) * vec_per_row + c) * 8, f[q]);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    acc[i] = __fadd_rn(acc[i], __fmul_rn(wj[q], f[q][i]));
+                for (int q = 0; q < 4; ++q) {
+                    if (row[q] < 0)
+                        continue;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        acc[i] = __fadd_rn(acc[i], __fmul_rn(wj[q], f[q][i]));
+                }
             }
         }
         uint4 o;
