@@ -33,7 +33,10 @@ constexpr int kCombineThreads = 128;
 constexpr int kColsPerItem = kCombineThreads * 8;   // one work item = one token x 1024 columns
 
 // Eight consecutive columns of one y row as fp32: two 16-byte loads (fp32 y)
-// or one (fp16 y, widened exactly).
+// or one (fp16 y, widened exactly). A down GEMM that split K leaves fp32 y
+// as `parts` partial rows, `part_stride` elements apart: the row is their
+// sum, taken in part order (((p0 + p1) + p2) + p3), the order in which
+// moe_expert_compute reduces its parts, so every route gives the same bits.
 __device__ __forceinline__ void load8(const float *y, size_t i, float (&f)[8])
 {
     const float4 a = __ldg(reinterpret_cast<const float4 *>(y + i));
@@ -54,12 +57,13 @@ __device__ __forceinline__ void load8(const __half *y, size_t i, float (&f)[8])
     }
 }
 
-template <typename Y>
+template <typename Y, int kParts>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Y *__restrict__ y_sorted,
                                                                   const int32_t *__restrict__ inv,
                                                                   const float *__restrict__ w,
                                                                   const int32_t *d_num_tokens, int T_max, int k,
-                                                                  int vec_per_row, uint4 *__restrict__ out)
+                                                                  int vec_per_row, uint4 *__restrict__ out,
+                                                                  size_t part_stride)
 {
     pdl_wait();
     pdl_trigger();
@@ -110,6 +114,47 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Y *__res
                     }
                 }
             }
+        } else if (kParts > 1) {
+            // fp32 y in K parts: two routed rows at a time, the 16-byte loads of
+            // all their parts (at most 4) issued together; each row is the sum of
+            // its parts in part order, then weighted and summed in ascending j
+            for (int j0 = 0; j0 < k; j0 += 2) {
+                float4 lo[2][kParts], hi[2][kParts];
+                int row[2];
+                float wj[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    row[q] = (j0 + q < k) ? __ldg(inv_t + j0 + q) : -1;
+                    wj[q] = (j0 + q < k) ? __ldg(w_t + j0 + q) : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+#pragma unroll
+                    for (int pp = 0; pp < kParts; ++pp)
+                        if (row[q] >= 0) {
+                            const float4 *src = reinterpret_cast<const float4 *>(
+                                y_sorted + pp * part_stride + (static_cast<size_t>(row[q]) * vec_per_row + c) * 8);
+                            lo[q][pp] = __ldg(src);
+                            hi[q][pp] = __ldg(src + 1);
+                        }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    if (row[q] < 0)
+                        continue;
+                    float f[8] = {lo[q][0].x, lo[q][0].y, lo[q][0].z, lo[q][0].w,
+                                  hi[q][0].x, hi[q][0].y, hi[q][0].z, hi[q][0].w};
+#pragma unroll
+                    for (int pp = 1; pp < kParts; ++pp) {
+                        f[0] = __fadd_rn(f[0], lo[q][pp].x); f[1] = __fadd_rn(f[1], lo[q][pp].y);
+                        f[2] = __fadd_rn(f[2], lo[q][pp].z); f[3] = __fadd_rn(f[3], lo[q][pp].w);
+                        f[4] = __fadd_rn(f[4], hi[q][pp].x); f[5] = __fadd_rn(f[5], hi[q][pp].y);
+                        f[6] = __fadd_rn(f[6], hi[q][pp].z); f[7] = __fadd_rn(f[7], hi[q][pp].w);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        acc[i] = __fadd_rn(acc[i], __fmul_rn(wj[q], f[i]));
+                }
+            }
         } else {
             // loads of up to four routed rows are issued together, then summed in
             // ascending j, so the sum is the same sequence of roundings as a plain loop
@@ -145,24 +190,66 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Y *__res
     }
 }
 
+// y[r, :] = ((p0 + p1) + p2) + p3 over the `parts` partial rows of a down
+// GEMM that split K, for r < expert_offsets[E] (rows past it are not
+// written): four columns per thread, grid-stride over rows x H/4.
+__global__ void __launch_bounds__(256) reduce_parts_kernel(const float4 *__restrict__ part0, int parts,
+                                                           size_t part_stride4, const int32_t *__restrict__ offsets,
+                                                           int E, int vec4_per_row, int cap, float4 *__restrict__ y)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int n_rows = min(offsets[E], cap);
+    const size_t n = static_cast<size_t>(n_rows) * vec4_per_row;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        float4 a = __ldg(part0 + i);
+        for (int q = 1; q < parts; ++q) {
+            const float4 b = __ldg(part0 + q * part_stride4 + i);
+            a.x = __fadd_rn(a.x, b.x);
+            a.y = __fadd_rn(a.y, b.y);
+            a.z = __fadd_rn(a.z, b.z);
+            a.w = __fadd_rn(a.w, b.w);
+        }
+        y[i] = a;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_reduce_parts(const float *parts_base, int parts, const int32_t *expert_offsets, int E, int H,
+                                int cap, float *y_sorted, int num_sms, cudaStream_t stream, bool pdl)
+{
+    const size_t rows_vec4 = static_cast<size_t>(cap) * (H / 4);
+    long long blocks = static_cast<long long>((rows_vec4 + 255) / 256);
+    blocks = blocks < num_sms * 8LL ? blocks : num_sms * 8LL;
+    if (blocks < 1)
+        blocks = 1;
+    return launch_k(reduce_parts_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, pdl,
+                    reinterpret_cast<const float4 *>(parts_base), parts, rows_vec4, expert_offsets, E, H / 4, cap,
+                    reinterpret_cast<float4 *>(y_sorted));
+}
 
 cudaError_t launch_combine(const void *y_sorted, bool y_f16, const int32_t *inv, const float *topk_weights,
                            const int32_t *d_num_tokens, int T_max, int k, int H, void *out, int num_sms,
-                           cudaStream_t stream, bool pdl)
+                           cudaStream_t stream, bool pdl, int parts, size_t part_stride)
 {
+    if (y_f16 && parts != 1)   // fp16 y comes from the tiled paths, whose down GEMM never splits K
+        return cudaErrorInvalidValue;
     const long long groups = (static_cast<long long>(H) + kColsPerItem - 1) / kColsPerItem;
     const long long items = static_cast<long long>(T_max) * groups;
     int blocks = static_cast<int>(items < num_sms * 16LL ? items : num_sms * 16LL);
     if (blocks < 1)
         blocks = 1;
     if (y_f16)
-        return launch_k(combine_kernel<__half>, dim3(blocks), dim3(kCombineThreads), 0, stream, pdl,
+        return launch_k(combine_kernel<__half, 1>, dim3(blocks), dim3(kCombineThreads), 0, stream, pdl,
                         static_cast<const __half *>(y_sorted), inv, topk_weights, d_num_tokens, T_max, k, H / 8,
-                        static_cast<uint4 *>(out));
-    return launch_k(combine_kernel<float>, dim3(blocks), dim3(kCombineThreads), 0, stream, pdl,
-                    static_cast<const float *>(y_sorted), inv, topk_weights, d_num_tokens, T_max, k, H / 8,
-                    static_cast<uint4 *>(out));
+                        static_cast<uint4 *>(out), size_t(0));
+    auto kern = parts == 4 ? combine_kernel<float, 4> : parts == 2 ? combine_kernel<float, 2> : combine_kernel<float, 1>;
+    if (parts != 1 && parts != 2 && parts != 4)
+        return cudaErrorInvalidValue;
+    return launch_k(kern, dim3(blocks), dim3(kCombineThreads), 0, stream, pdl, static_cast<const float *>(y_sorted),
+                    inv, topk_weights, d_num_tokens, T_max, k, H / 8, static_cast<uint4 *>(out), part_stride);
 }
 
 }  // namespace moe

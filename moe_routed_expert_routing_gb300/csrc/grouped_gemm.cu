@@ -128,7 +128,8 @@ struct Cfg {
     static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0, "tiles must keep 1024-byte alignment");
     static_assert(kTmemCols <= 512, "TMEM has 512 columns");
     static_assert(!kSmallM || (kTileRows % 16 == 0 && kTileRows >= 16 && kTileRows <= 256), "MMA N");
-    static_assert(kSplitK == 1 || (kSplitK == 2 && kSmallM && !kGated), "split-K: M-small down GEMM only");
+    static_assert(kSplitK == 1 || ((kSplitK == 2 || kSplitK == 4) && kSmallM && !kGated),
+                  "split-K: M-small down GEMM only");
 };
 
 struct Unit {
@@ -548,10 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (kGated)
                                 static_cast<__nv_bfloat16 *>(args.out)[o] =
                                     __float2bfloat16_rn(silu_mul(__uint_as_float(g[i]), __uint_as_float(v[i])));
-                            else if (kSplitK == 1)
-                                static_cast<float *>(args.out)[o] = __uint_as_float(g[i]);
-                            else  // two K halves into a zeroed output: 0 + a + b == 0 + b + a exactly
-                                atomicAdd(static_cast<float *>(args.out) + o, __uint_as_float(g[i]));
+                            else   // K part u % kSplitK to its own buffer (summed in part order later)
+                                static_cast<float *>(args.out)[static_cast<size_t>(u % kSplitK) * args.cap *
+                                                                   args.n_out + o] = __uint_as_float(g[i]);
                         }
                     }
                 }
@@ -597,14 +597,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // CTA first runs the local dispatch of the call's few routed slots itself
 // (histogram, scan, stable scatter into shared memory; CTA 0 also writes
 // expert_offsets and perm for the caller), so no other kernel precedes the
-// GEMMs. Down units publish their y rows on a GPU-wide count; when it is
-// full every CTA combines its share of tokens x 1024 columns. The last CTA
+// GEMMs. Each CTA, once through with its GEMM units, counts itself on a
+// GPU-wide count (one add per CTA, not one per unit: the polls and adds on
+// that one address stay few); when every CTA has, each combines its share of
+// tokens x 1024 columns. The last CTA
 // to leave returns every counter to zero (FlashInfer moe_ep page, launch-path
 // notes: workspaces are allocated zeroed and the kernel cleans its
 // counters and flags at its tail), also after a timed-out wait, so repeated
-// calls need no memset. The split down GEMM writes its two K halves to two
-// fp32 buffers that the combine adds (a + b: the same value the two-atomic
-// form produces), so y needs no zeroing either.
+// calls need no memset. A down GEMM that splits K (2 or 4 parts, in both
+// forms) writes each part to its own fp32 buffer and the combine adds them
+// in part order, so y needs no zeroing and the sum is deterministic.
 //
 // MXFP8 weights (kFp8): a weight block is 128 K elements (one 128-byte row of
 // E4M3 codes) plus its 4 scale bytes per row; a stage holds two such 16 KB
@@ -652,7 +654,7 @@ struct FusedArgs {
     int32_t *expert_offsets_out;   // [E + 1] for the caller
     int32_t *perm_out;             // [cap] for the caller
     __nv_bfloat16 *out;            // [T_max, H]
-    int32_t *done;                 // epilogue warps that finished a down unit, zero at launch and at exit
+    int32_t *done;                 // CTAs through with their GEMM units, zero at launch and at exit
 };
 
 // Local dispatch of all routed slots inside one CTA (every CTA of the
@@ -767,7 +769,7 @@ __device__ void cta_combine(const FusedArgs &fa, const int *s_inv, int T)
     const int vec = H / 4;
     const int groups = (vec + kThreads - 1) / kThreads;
     const float4 *y0 = static_cast<const float4 *>(fa.down.out);
-    const float4 *y1 = y0 + static_cast<size_t>(fa.down.cap) * vec;
+    const size_t part = static_cast<size_t>(fa.down.cap) * vec;   // float4s between K parts
     const long long items = static_cast<long long>(T) * groups;
     for (long long item = blockIdx.x; item < items; item += gridDim.x) {
         const int t = static_cast<int>(item / groups);
@@ -787,10 +789,12 @@ __device__ void cta_combine(const FusedArgs &fa, const int *s_inv, int T)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (row[q] >= 0) {
+                    // the row is the sum of its K parts in part order, as moe_expert_compute reduces them
                     const size_t i = static_cast<size_t>(row[q]) * vec + c;
                     a[q] = __ldcg(y0 + i);
-                    if (kSplitDown == 2) {
-                        const float4 b = __ldcg(y1 + i);
+#pragma unroll
+                    for (int pp = 1; pp < kSplitDown; ++pp) {
+                        const float4 b = __ldcg(y0 + pp * part + i);
                         a[q].x = __fadd_rn(a[q].x, b.x);
                         a[q].y = __fadd_rn(a[q].y, b.y);
                         a[q].z = __fadd_rn(a[q].z, b.z);
@@ -1207,8 +1211,9 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
             tc_fence_after();
             const uint32_t t_row = tmem_base + buf * C::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
             const int col = t.n0 + q * 32 + lane;
+            // a down unit's K part goes to its own buffer (summed in part order by the combine)
             float *const y_out = static_cast<float *>(A2.out) +
-                                 ((kMega && !up) ? static_cast<size_t>(v % kSplitDown) * A2.cap * A2.n_out : 0);
+                                 (!up ? static_cast<size_t>(v % kSplitDown) * A2.cap * A2.n_out : 0);
 #pragma unroll 1
             for (int c = 0; c < kTileRows; c += 16) {
                 uint32_t g[16], w[16];
@@ -1225,27 +1230,27 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                             static_cast<__nv_bfloat16 *>(A1.out)[static_cast<size_t>(row) * A1.n_out + col] =
                                 __float2bfloat16_rn(silu_mul(__uint_as_float(g[i]), __uint_as_float(w[i])));
                         } else {
-                            float *y = y_out + static_cast<size_t>(row) * A2.n_out + col;
-                            if (kSplitDown == 1 || kMega)
-                                *y = __uint_as_float(g[i]);
-                            else  // two K halves into a zeroed output: exact and order-free
-                                atomicAdd(y, __uint_as_float(g[i]));
+                            y_out[static_cast<size_t>(row) * A2.n_out + col] = __uint_as_float(g[i]);
                         }
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_tempty[buf]));
-            if (up || kMega) {
-                // publish this warp's h (or y) rows: every storing lane fences,
-                // then one lane releases the count (4 warps per unit; no
+            if (up) {
+                // publish this warp's h rows: every storing lane fences, then
+                // one lane releases the expert's count (4 warps per unit; no
                 // cross-warp wait)
                 __threadfence();
                 __syncwarp();
                 if (lane == 0)
-                    red_release_gpu_add(up ? fa.ready + t.e : fa.done, 1);
+                    red_release_gpu_add(fa.ready + t.e, 1);
             }
         }
+        // whole-forward form: this thread's y stores before the CTA's one count
+        // on `done` (after the CTA barrier below)
+        if (kMega)
+            __threadfence();
     }
 
     tc_fence_before();
@@ -1255,8 +1260,13 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
         tmem_dealloc(tmem_base, C::kTmemCols);
     }
     if (kMega) {
-        // combine once every down unit of the call has published its rows
-        const int need = 4 * s_tp[E] * NT2 * kSplitDown;
+        // every CTA counts itself once on `done`, after all its units (its
+        // epilogue threads fenced their y stores before the barrier above;
+        // also after giving up, so that the others need not wait the limit);
+        // the combine starts once every CTA has counted itself
+        if (threadIdx.x == 0)
+            red_release_gpu_add(fa.done, 1);
+        const int need = static_cast<int>(gridDim.x);
         if (threadIdx.x == 0 && !s_abort) {
             const uint64_t t0 = global_timer_ns();
             while (ld_acquire_gpu(fa.done) < need) {
@@ -1849,12 +1859,14 @@ long long mega_table_budget()
         return -1;
     if (dev != cached_dev) {
         int optin = 0;
-        cudaFuncAttributes fa1 = {}, fa2 = {};
+        cudaFuncAttributes fa1 = {}, fa2 = {}, fa4 = {};
         if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
             cudaFuncGetAttributes(&fa1, fused_small_kernel<kTileRows, kStages, 1, true, kFp8>) != cudaSuccess ||
-            cudaFuncGetAttributes(&fa2, fused_small_kernel<kTileRows, kStages, 2, true, kFp8>) != cudaSuccess)
+            cudaFuncGetAttributes(&fa2, fused_small_kernel<kTileRows, kStages, 2, true, kFp8>) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa4, fused_small_kernel<kTileRows, kStages, 4, true, kFp8>) != cudaSuccess)
             return -1;
-        const size_t st = fa1.sharedSizeBytes > fa2.sharedSizeBytes ? fa1.sharedSizeBytes : fa2.sharedSizeBytes;
+        size_t st = fa1.sharedSizeBytes > fa2.sharedSizeBytes ? fa1.sharedSizeBytes : fa2.sharedSizeBytes;
+        st = st > fa4.sharedSizeBytes ? st : fa4.sharedSizeBytes;
         cached = static_cast<long long>(optin) - static_cast<long long>(st) -
                  FusedCfg<kTileRows, kStages, kFp8>::kDynSmem;
         cached_dev = dev;
@@ -1953,7 +1965,8 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t 
         return cudaErrorInvalidValue;
     if (p.out_f16 && (p.small_m || p.gated))   // fp16 y: tiled down GEMM only
         return cudaErrorInvalidValue;
-    if (p.split_k != 1 && (p.split_k != 2 || !p.small_m || p.gated || p.tile_rows != 16 || (p.K / kBK) % 2 != 0))
+    if (p.split_k != 1 && ((p.split_k != 2 && p.split_k != 4) || !p.small_m || p.gated || p.tile_rows != 16 ||
+                           (p.K / kBK) % p.split_k != 0))
         return cudaErrorInvalidValue;
     if (p.gather && (!p.gated || !p.perm || p.k < 1))
         return cudaErrorInvalidValue;
@@ -1970,6 +1983,8 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t 
     case 16:
         if (!p.gated && p.split_k == 2)
             return run<true, false, 16, 10, 2>(p, num_sms, stream);
+        if (!p.gated && p.split_k == 4)
+            return run<true, false, 16, 10, 4>(p, num_sms, stream);
         if (p.gated)
             return p.gather ? run<true, true, 16, 6, 1, true>(p, num_sms, stream) : run<true, true, 16, 6>(p, num_sms, stream);
         return run<true, false, 16, 10>(p, num_sms, stream);
@@ -1990,7 +2005,7 @@ cudaError_t launch_fused_small(const GemmProblem &up, const GemmProblem &down, i
                                int num_sms, cudaStream_t stream, const MegaParams *mega)
 {
     if (!up.small_m || !down.small_m || !up.gated || down.gated || !up.gather || up.tile_rows != down.tile_rows ||
-        !ready || !counters || (down.split_k != 1 && down.split_k != 2))
+        !ready || !counters || (down.split_k != 1 && down.split_k != 2 && down.split_k != 4))
         return cudaErrorInvalidValue;
     if (mega ? (!mega->ids || !mega->topk_w || !mega->expert_offsets_out || !mega->perm_out || !mega->out ||
                 mega->T_max < 1)
@@ -2000,19 +2015,19 @@ cudaError_t launch_fused_small(const GemmProblem &up, const GemmProblem &down, i
         return cudaErrorInvalidValue;
     if (up.w_mxfp8) {
         // MXFP8 weights: every M-small tile height (this kernel is their only GEMM)
-        if (up.K % 128 != 0 || down.K % 128 != 0 || (down.split_k == 2 && (down.K / 128) % 2 != 0))
+        if (up.K % 128 != 0 || down.K % 128 != 0 || (down.K / 128) % down.split_k != 0)
             return cudaErrorInvalidValue;
         if (mega && (up.tile_rows != 16))
             return cudaErrorInvalidValue;
         switch (up.tile_rows) {
         case 16:
             if (mega)
-                return down.split_k == 2
-                           ? run_fused<16, 5, 2, true, true>(up, down, ready, counters, num_sms, stream, mega)
-                           : run_fused<16, 5, 1, true, true>(up, down, ready, counters, num_sms, stream, mega);
-            return down.split_k == 2
-                       ? run_fused<16, 5, 2, false, true>(up, down, ready, counters, num_sms, stream, nullptr)
-                       : run_fused<16, 5, 1, false, true>(up, down, ready, counters, num_sms, stream, nullptr);
+                return down.split_k == 4   ? run_fused<16, 5, 4, true, true>(up, down, ready, counters, num_sms, stream, mega)
+                       : down.split_k == 2 ? run_fused<16, 5, 2, true, true>(up, down, ready, counters, num_sms, stream, mega)
+                                           : run_fused<16, 5, 1, true, true>(up, down, ready, counters, num_sms, stream, mega);
+            return down.split_k == 4   ? run_fused<16, 5, 4, false, true>(up, down, ready, counters, num_sms, stream, nullptr)
+                   : down.split_k == 2 ? run_fused<16, 5, 2, false, true>(up, down, ready, counters, num_sms, stream, nullptr)
+                                       : run_fused<16, 5, 1, false, true>(up, down, ready, counters, num_sms, stream, nullptr);
         case 32:
             return down.split_k == 1
                        ? run_fused<32, 4, 1, false, true>(up, down, ready, counters, num_sms, stream, nullptr)
@@ -2029,11 +2044,15 @@ cudaError_t launch_fused_small(const GemmProblem &up, const GemmProblem &down, i
     // with 32-row tiles (the Zipf small batch) two launches measured 2% faster
     if (up.tile_rows != 16)
         return cudaErrorInvalidValue;
+    if ((down.K / kBK) % down.split_k != 0)
+        return cudaErrorInvalidValue;
     if (mega)
-        return down.split_k == 2 ? run_fused<16, 6, 2, true, false>(up, down, ready, counters, num_sms, stream, mega)
-                                 : run_fused<16, 6, 1, true, false>(up, down, ready, counters, num_sms, stream, mega);
-    return down.split_k == 2 ? run_fused<16, 6, 2, false, false>(up, down, ready, counters, num_sms, stream, nullptr)
-                             : run_fused<16, 6, 1, false, false>(up, down, ready, counters, num_sms, stream, nullptr);
+        return down.split_k == 4   ? run_fused<16, 6, 4, true, false>(up, down, ready, counters, num_sms, stream, mega)
+               : down.split_k == 2 ? run_fused<16, 6, 2, true, false>(up, down, ready, counters, num_sms, stream, mega)
+                                   : run_fused<16, 6, 1, true, false>(up, down, ready, counters, num_sms, stream, mega);
+    return down.split_k == 4   ? run_fused<16, 6, 4, false, false>(up, down, ready, counters, num_sms, stream, nullptr)
+           : down.split_k == 2 ? run_fused<16, 6, 2, false, false>(up, down, ready, counters, num_sms, stream, nullptr)
+                               : run_fused<16, 6, 1, false, false>(up, down, ready, counters, num_sms, stream, nullptr);
 }
 
 bool fused_mega_fits(int E, long long slots, bool mxfp8)

@@ -31,13 +31,21 @@ constexpr size_t kHeaderBytes = (kCountersOffset + 2 * sizeof(int32_t) + kAlign 
 
 void resolve(const moe_problem_t &p, int *path, int *tile_rows);
 
-// A split down GEMM is possible (the SM count decides): the fused kernel then
-// needs two fp32 y buffers.
-bool split_possible(const moe_problem_t &p)
+// 128-wide K blocks of the down GEMM, the unit its K parts are made of (for
+// every weight layout alike, so that MXFP8 and bf16 weights split the same
+// way and stay bit-identical); 1 when I is not a multiple of 128 (no split).
+int down_k_blocks(const moe_problem_t &p) { return p.I % 128 == 0 ? p.I / 128 : 1; }
+
+// The most K parts the down GEMM may split into for this problem (the SM
+// count decides how many it does): its fp32 y then takes that many buffers.
+int split_parts_max(const moe_problem_t &p)
 {
     int path = 0, tile_rows = 0;
     resolve(p, &path, &tile_rows);
-    return path == MOE_PATH_SMALL_M && tile_rows == 16 && (p.I / 64) % 2 == 0;
+    if (path != MOE_PATH_SMALL_M || tile_rows != 16)
+        return 1;
+    const int kb = down_k_blocks(p);
+    return kb % 4 == 0 ? 4 : (kb % 2 == 0 ? 2 : 1);
 }
 
 Layout layout_of(const moe_problem_t &p)
@@ -59,7 +67,7 @@ Layout layout_of(const moe_problem_t &p)
     L.x_sorted = o;
     o = align_up(o + 2 * cap * p.H);
     L.y_sorted = o;
-    o = align_up(o + 4 * cap * p.H * (split_possible(p) ? 2 : 1));
+    o = align_up(o + 4 * cap * p.H * static_cast<size_t>(split_parts_max(p)));
     L.inv = o;
     o = align_up(o + sizeof(int32_t) * R);
     L.total = o;
@@ -166,28 +174,47 @@ moe_status_t record_stage(void *const *stage_events, int i, cudaStream_t s)
         cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), s, cudaEventRecordExternal));
 }
 
-// Split the M-small down GEMM's K in two when it would otherwise have too few
-// units to fill the GPU (decode: a handful of experts x H/128 weight tiles):
-// the two halves are added into a zeroed fp32 y, which is exact and
-// order-independent for two terms. Decided from static shapes only.
-bool down_split_k(const moe_problem_t &p, int path, int tile_rows, int sms)
+// K parts of the M-small down GEMM (1, 2 or 4), from static shapes only.
+// Decode batches touch a handful of experts, so the down GEMM has few units
+// (experts x H/128 weight tiles) for the SMs, and the last wave of units runs
+// on a fraction of them: splitting K gives more, smaller units. The choice
+// is the one with the fewest waves of full-K work, ceil(units * S / sms) / S,
+// ties going to fewer parts. Each part goes to its own fp32 y buffer; the
+// combine (or moe_expert_compute's reduction) adds them in part order, so
+// the result is deterministic whatever the split. More parts must save at
+// least 5% of the waves: each unit costs its readiness wait and epilogue.
+// At one token, E=384, H=7168, I=3072 (336 units of full K): 2 parts give
+// 672 units, 5 on 64 SMs and 4 on 88; 4 parts give 1344, 9 and 8.
+int down_split_k(const moe_problem_t &p, int path, int tile_rows, int sms)
 {
-    const int k_block = p.weight_layout == MOE_WEIGHTS_MXFP8 ? 128 : 64;   // K of one weight block
-    if (path != MOE_PATH_SMALL_M || tile_rows != 16 || (p.I / k_block) % 2 != 0)
-        return false;
+    if (path != MOE_PATH_SMALL_M || tile_rows != 16 || sms <= 0)
+        return 1;
+    const int kb = down_k_blocks(p);
     const long long R_max = static_cast<long long>(p.T_max) * p.k;
-    const long long max_experts = R_max < p.E ? R_max : p.E;
-    return max_experts * ((p.H + 127) / 128) < 4LL * sms;
+    const long long units = (R_max < p.E ? R_max : p.E) * ((p.H + 127) / 128);
+    int best = 1;
+    double best_waves = static_cast<double>((units + sms - 1) / sms);
+    for (int parts = 2; parts <= 4; parts *= 2) {
+        if (kb % parts != 0)
+            continue;
+        const double waves = static_cast<double>((units * parts + sms - 1) / sms) / parts;
+        if (waves < 0.95 * best_waves) {
+            best = parts;
+            best_waves = waves;
+        }
+    }
+    return best;
 }
 
-// Enqueue both GEMMs. With y_zeroed false and a split down GEMM, y is
-// cleared here first (moe_forward clears it at its start instead, so that the
-// kernels of the call stay back to back on the stream). With gather_perm set,
-// `act` is x[T_max, H] itself and the gate-up GEMM fetches each sorted row
-// x[perm[row] / k] straight into shared memory (no x_sorted round trip).
+// Enqueue both GEMMs. With gather_perm set, `act` is x[T_max, H] itself and
+// the gate-up GEMM fetches each sorted row x[perm[row] / k] straight into
+// shared memory (no x_sorted round trip). A down GEMM that splits K writes
+// its parts to the workspace's y buffers; with reduce_into set (the caller's
+// y of moe_expert_compute) they are then summed into it in part order,
+// otherwise (moe_forward) y_sorted is those buffers and the combine sums them.
 moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, const int32_t *expert_offsets,
                                     const void *W13, const void *W2, float *y_sorted, void *ws, cudaStream_t s,
-                                    void *const *stage_events = nullptr, bool y_zeroed = false,
+                                    void *const *stage_events = nullptr, float *reduce_into = nullptr,
                                     const int32_t *gather_perm = nullptr, bool fused = false,
                                     const MegaParams *mega = nullptr, bool y_f16 = false)
 {
@@ -197,10 +224,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
     const int sms = device_sm_count();
     if (sms <= 0)
         return MOE_ERR_CUDA;
-    const bool split = down_split_k(p, path, tile_rows, sms);
-    if (split && !y_zeroed && !mega &&
-        cudaMemsetAsync(y_sorted, 0, sizeof(float) * static_cast<size_t>(capacity_of(p)) * p.H, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    const int parts = down_split_k(p, path, tile_rows, sms);
     GemmProblem g;
     g.expert_offsets = expert_offsets;
     g.err = at<int32_t>(ws, L.err);
@@ -249,9 +273,17 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
     g.w_rows_per_expert = p.H;
     g.up_row_offset = 0;
     g.gated = false;
-    g.split_k = split ? 2 : 1;
-    if (!fused)
-        return cuda_status(launch_grouped_gemm(g, sms, s));
+    g.split_k = parts;
+    if (!fused) {
+        if (parts == 1 || !reduce_into)
+            return cuda_status(launch_grouped_gemm(g, sms, s));
+        g.out = at<float>(ws, L.y_sorted);   // the parts, then their sum into the caller's y
+        st = cuda_status(launch_grouped_gemm(g, sms, s));
+        if (st != MOE_OK)
+            return st;
+        return cuda_status(launch_reduce_parts(at<float>(ws, L.y_sorted), parts, expert_offsets, p.E, p.H, g.cap,
+                                               reduce_into, sms, s, g.pdl));
+    }
     // both GEMMs in one persistent launch; its stage marks share one instant
     st = cuda_status(launch_fused_small(up, g, at<int32_t>(ws, L.ready), at<int32_t>(ws, L.counters), sms, s, mega));
     if (st != MOE_OK)
@@ -300,7 +332,7 @@ bool use_megakernel(const moe_problem_t &p)
         return false;
     int path = 0, tile_rows = 0;
     resolve(p, &path, &tile_rows);
-    return down_split_k(p, path, tile_rows, device_sm_count());
+    return down_split_k(p, path, tile_rows, device_sm_count()) > 1;
 }
 
 moe_status_t check_form(const moe_problem_t &p)
@@ -408,7 +440,7 @@ moe_status_t moe_resolve_profile(const moe_problem_t *problem, moe_profile_t *pr
     std::memset(profile, 0, sizeof *profile);
     profile->path = path;
     profile->tile_rows = tile_rows;
-    profile->down_split_k = down_split_k(*problem, path, tile_rows, sms) ? 2 : 1;
+    profile->down_split_k = down_split_k(*problem, path, tile_rows, sms);
     profile->pdl = use_pdl(*problem) ? 1 : 0;
     profile->fused_gather = path == MOE_PATH_SMALL_M ? 1 : 0;
     profile->cta_pair = path == MOE_PATH_TILED ? 1 : 0;
@@ -466,7 +498,7 @@ moe_status_t moe_expert_compute(const moe_problem_t *problem, const void *x_sort
     if ((st = check_device()) != MOE_OK)
         return st;
     return enqueue_expert_compute(p, x_sorted, expert_offsets, W13, W2, y_sorted, ws,
-                                  static_cast<cudaStream_t>(stream));
+                                  static_cast<cudaStream_t>(stream), nullptr, y_sorted);
 }
 
 moe_status_t moe_combine(const moe_problem_t *problem, const float *y_sorted, const int32_t *inv,
@@ -529,15 +561,14 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
         mp.out = out;
         if ((st = mark(0)) != MOE_OK)
             return st;
-        st = enqueue_expert_compute(p, x, nullptr, W13, W2, y_sorted, ws, s, nullptr, true, nullptr, true, &mp);
+        st = enqueue_expert_compute(p, x, nullptr, W13, W2, y_sorted, ws, s, nullptr, nullptr, nullptr, true, &mp);
         for (int i = 1; st == MOE_OK && i < 6; ++i)
             st = mark(i);
         return st;
     }
-    const bool split = down_split_k(p, path, tile_rows, sms);
-    if (split && cudaMemsetAsync(y_sorted, 0, sizeof(float) * static_cast<size_t>(capacity_of(p)) * p.H, s) !=
-                     cudaSuccess)
-        return MOE_ERR_CUDA;
+    // a down GEMM that splits K leaves its parts in the workspace's y buffers;
+    // the combine sums them in part order
+    const int parts = down_split_k(p, path, tile_rows, sms);
     // decode-size batches (M-small, 16-row token tiles): both GEMMs run as one
     // persistent kernel whose down units wait on per-expert counts (zero at
     // every launch: the kernel clears them at its tail). Measured in one
@@ -566,11 +597,11 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
     // M-small path keeps fp32 (its y is small).
     const bool y_f16 = path != MOE_PATH_SMALL_M;
     st = enqueue_expert_compute(p, fused_gather ? x : x_sorted, expert_offsets, W13, W2, y_sorted, ws, s,
-                                stage_events, true, fused_gather ? perm : nullptr, fused_mlp, nullptr, y_f16);
+                                stage_events, nullptr, fused_gather ? perm : nullptr, fused_mlp, nullptr, y_f16);
     if (st != MOE_OK || (st = mark(4)) != MOE_OK)
         return st;
     st = cuda_status(launch_combine(y_sorted, y_f16, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out, sms,
-                                    s, use_pdl(p)));
+                                    s, use_pdl(p), parts, static_cast<size_t>(capacity_of(p)) * p.H));
     if (st != MOE_OK)
         return st;
     return mark(5);

@@ -107,9 +107,16 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *perm, const int32_t
 
 // ---- combine (combine.cu) ----
 // y_sorted is fp32, or fp16 when y_f16 is set (moe_forward's tiled paths).
+// fp32 y may be `parts` partial buffers of a down GEMM that split K,
+// part_stride elements apart: each row is their sum in part order.
 cudaError_t launch_combine(const void *y_sorted, bool y_f16, const int32_t *inv, const float *topk_weights,
                            const int32_t *d_num_tokens, int T_max, int k, int H, void *out, int num_sms,
-                           cudaStream_t stream, bool pdl);
+                           cudaStream_t stream, bool pdl, int parts = 1, size_t part_stride = 0);
+
+// y_sorted[r] = ((p0 + p1) + p2) + p3 over the `parts` fp32 partial buffers of
+// [cap, H] starting at parts_base, for r < expert_offsets[E].
+cudaError_t launch_reduce_parts(const float *parts_base, int parts, const int32_t *expert_offsets, int E, int H,
+                                int cap, float *y_sorted, int num_sms, cudaStream_t stream, bool pdl);
 
 // ---- packed weights (weights_pack.cu) ----
 cudaError_t launch_pack_weights(const void *W13, const void *W2, void *W13_packed, void *W2_packed, int E, int H,
@@ -139,7 +146,7 @@ struct GemmProblem {
     bool gated;               // fused SiLU(gate) * up epilogue
     bool small_m;             // weights on the MMA M side (M-small path)
     int tile_rows;            // activation rows per tile: 128 (tiled) or 16/32/64 (M-small)
-    int split_k;              // 1, or 2 (M-small down GEMM only: two K halves added into a zeroed fp32 out)
+    int split_k;              // 1, 2 or 4 (M-small down GEMM only): K parts, part p of fp32 out at out + p * cap * n_out
     bool pdl;                 // programmatic dependent launch
     bool cta_pair;            // tiled path on 2-CTA clusters (tcgen05 cta_group::2)
     bool w_packed;            // `w` is in the access-ordered PACKED layout

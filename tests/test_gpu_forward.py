@@ -151,7 +151,8 @@ def test_launch_profile_table(B):
     """The static profile follows from the shape alone (a = T_max*k/E rows per expert)."""
     P = B.Problem.make
     dec1 = B.moe_resolve_profile(P(1, 384, 6, 7168, 3072))
-    assert dec1 == dict(path=2, tile_rows=16, down_split_k=2, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1,
+    # one token at E=384: 336 full-K down units; 4 K parts (1344 units) fill the waves best
+    assert dec1 == dict(path=2, tile_rows=16, down_split_k=4, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1,
                         megakernel=1, kernel_launches=1)
     dec8 = B.moe_resolve_profile(P(8, 384, 6, 7168, 3072))
     assert dec8 == dict(path=2, tile_rows=16, down_split_k=1, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1,
@@ -229,20 +230,24 @@ def _separate_entry_points(B, p, dw, d_T=None):
     return bufs
 
 
-# (T, E, k, H, I): one token (split down GEMM), a decode batch (unsplit), a wide top-k (split)
-MEGA_SHAPES = [(1, 64, 4, 512, 256), (8, 64, 4, 4096, 256), (24, 256, 16, 256, 128)]
+# (T, E, k, H, I), down GEMM K parts (made of 128-wide K blocks): one token
+# (4 parts; 2 where I holds two blocks), a decode batch (unsplit), a wide
+# top-k (2 parts), I not a multiple of 128 (unsplit)
+MEGA_SHAPES = [((1, 64, 6, 512, 512), 4), ((1, 64, 4, 512, 256), 2), ((8, 64, 4, 4096, 256), 1),
+               ((24, 256, 16, 256, 256), 2), ((1, 64, 4, 512, 192), 1)]
 
 
-@pytest.mark.parametrize("shape", MEGA_SHAPES, ids=["T1_split", "T8", "k16"])
-def test_megakernel_equals_separate_entry_points(B, shape):
+@pytest.mark.parametrize("shape,parts", MEGA_SHAPES, ids=["T1_split4", "T1_split2", "T8", "k16", "T1_i192"])
+def test_megakernel_equals_separate_entry_points(B, shape, parts):
     """The one-kernel forward gives the same bits as dispatch + expert compute +
-    combine launched separately (same GEMM arithmetic, same combine order), and
-    the same expert_offsets and perm."""
+    combine launched separately (same GEMM arithmetic, the down GEMM's K parts
+    summed in the same order, same combine order), and the same expert_offsets
+    and perm; the three-kernel forward too."""
     wl = wlm.custom("mega", *shape, seed=sum(shape))
     dw = DeviceWorkload(wl)
     p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, forward_form=B.MOE_FORWARD_ONE_KERNEL)
     prof = B.moe_resolve_profile(p)
-    assert prof["megakernel"] == 1 and prof["kernel_launches"] == 1
+    assert prof["megakernel"] == 1 and prof["kernel_launches"] == 1 and prof["down_split_k"] == parts
     got = forward(B, p, dw)
     assert B.moe_last_device_error(got.ws) == 0
     ref = _separate_entry_points(B, p, dw)
@@ -250,6 +255,8 @@ def test_megakernel_equals_separate_entry_points(B, shape):
     n = int(ref.expert_offsets[-1])
     assert torch.equal(got.perm[:n], ref.perm[:n])
     assert torch.equal(got.out.view(torch.int16), ref.out.view(torch.int16))
+    three = forward(B, B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, forward_form=B.MOE_FORWARD_SEPARATE), dw)
+    assert torch.equal(three.out.view(torch.int16), ref.out.view(torch.int16))
     ref_acc, _ = dw.oracle_out()
     assert_within_tolerance(wlm.bf16_bits(got.out), ref_acc, f"megakernel {shape}")
 

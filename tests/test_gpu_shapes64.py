@@ -57,7 +57,7 @@ def test_forward_multiple_of_64(B, case, path):
 DECODE = [
     # name, T, E, k, H, I: 16-row token tiles, both GEMMs in one persistent kernel
     ("dec_h448_i192", 8, 64, 4, 448, 192),    # I / 64 odd: the down GEMM keeps K whole
-    ("dec_h448_i384", 4, 64, 4, 448, 384),    # the down GEMM splits K in two
+    ("dec_h448_i512", 4, 64, 4, 448, 512),    # the down GEMM splits K in two
     ("dec_h2880", 1, 32, 6, 2880, 2880),
 ]
 
