@@ -167,7 +167,7 @@ moe_status_t moe_resolve_path(const moe_problem_t *problem, int32_t *path, int32
 typedef struct moe_profile {
     int32_t path;          /* moe_path_t that runs (never AUTO) */
     int32_t tile_rows;     /* activation rows of one CTA's tile */
-    int32_t down_split_k;  /* 1, or 2: the down GEMM's K halves added into a zeroed fp32 y */
+    int32_t down_split_k;  /* 1, 2 or 4: K parts of the down GEMM, in separate fp32 buffers summed in part order */
     int32_t pdl;           /* 1: kernels of a call use programmatic dependent launch */
     int32_t fused_gather;  /* 1: moe_forward's gate-up GEMM gathers rows from x (no x_sorted) */
     int32_t cta_pair;      /* 1: tiled GEMMs run on 2-CTA clusters */
