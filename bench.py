@@ -68,12 +68,12 @@ GRAPH_STEPS = 10
 # capture time, comments and layout left out: after any change to the code,
 # traffic reports null.
 NCU_TRAFFIC = {
-    "kernel_sha256": "4d8acd24b5c65b74db96ef9ad4f454917f04341595f2afa46987751714803b22",
-    "fused_small": {"case": "decode T=8 shape with E=24", "traffic": 2.644585e+09, "algorithmic": 2.644378e+09},
-    "fused_small_mxfp8": {"case": "decode T=8 shape with E=24, MXFP8 weights", "traffic": 1.364733e+09, "algorithmic": 1.364460e+09},
-    "gate_up_small_m": {"case": "Zipf small batch with E=128", "traffic": 6.938982e+09, "algorithmic": 6.947865e+09},
-    "gate_up_tiled": {"case": "prefill shape with T=256, E=48", "traffic": 4.260382e+09, "algorithmic": 4.259316e+09},
-    "gate_up_pair": {"case": "large shape with T=4096, E=64", "traffic": 2.386328e+09, "algorithmic": 1.979711e+09},
+    "kernel_sha256": "dc4e01cd1eb369b059ef6b2db3711a2addf670be58220979f9e25926b6728608",
+    "fused_small": {"case": "decode T=8 shape with E=24", "traffic": 2.644638e+09, "algorithmic": 2.644378e+09},
+    "fused_small_mxfp8": {"case": "decode T=8 shape with E=24, MXFP8 weights", "traffic": 1.364449e+09, "algorithmic": 1.364460e+09},
+    "gate_up_small_m": {"case": "Zipf small batch with E=128", "traffic": 6.939075e+09, "algorithmic": 6.947865e+09},
+    "gate_up_tiled": {"case": "prefill shape with T=256, E=48", "traffic": 4.260524e+09, "algorithmic": 4.259316e+09},
+    "gate_up_pair": {"case": "large shape with T=4096, E=64", "traffic": 2.262511e+09, "algorithmic": 1.979711e+09},
 }
 
 
@@ -184,25 +184,62 @@ def sum_over_ranks(value: float, world: int, device=None) -> float:
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples of SM clock, power and throttle reasons, every 10 ms,
+    each with its timestamp; stop() keeps the samples that fall inside the
+    window marked by mark_start() / mark_end() (the timed region), or all of
+    them, with a note, if none does."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.window = None
         self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
 
     def start(self):
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                                          "-i", str(self.gpu), "-lms", "100"], stdout=self.fh,
+                                          "-i", str(self.gpu), "-lms", "10"], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def mark_start(self):
+        self._t0 = time.time()
+
+    def mark_end(self):
+        self.window = (self._t0, time.time())
+
+    @staticmethod
+    def parse(lines, window=None):
+        """Samples of nvidia-smi's csv lines (see QUERY), restricted to `window`
+        (two epoch seconds) when given; returns the summary dict or None."""
+        import datetime
+        rows = []
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]), parts[6:10]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if window and window[0] <= r[0] <= window[1]]
+        use = inside or rows
+        reasons = sorted({n for r in use for n, v in zip(ClockSampler.REASONS, r[4]) if v.lower().startswith("active")})
+        out = {"sm_mhz": float(np.median([r[1] for r in use])), "sm_max_mhz": float(max(r[2] for r in use)),
+               "reasons": reasons, "samples": len(use), "power_w_max": float(max(r[3] for r in use))}
+        out["samples_from"] = ("the whole sampling run" if not window else "the timed region" if inside else
+                               "around the timed region (no sample fell inside it)")
+        return out
 
     def stop(self) -> dict | None:
         if self.proc is None:
@@ -213,27 +250,10 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, mx, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
-                    power.append(float(parts[3]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
+            lines = f.readlines()
         os.unlink(self.path)
-        if not sm:
-            return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": float(max(power)) if power else None}
+        return self.parse(lines, self.window)
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -521,8 +541,11 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(device)
     clocks.start()
     time.sleep(0.25)
+    clocks.mark_start()
     local_ms = replay_timed(stream, graph, args.steps)   # exactly K steps, one graph replay each
     torch.cuda.synchronize(device)
+    clocks.mark_end()
+    time.sleep(0.05)
     clk = clocks.stop()
     barrier(world, device)
     max_ms = max_over_ranks(local_ms, world, device)
