@@ -156,3 +156,24 @@ def test_gpu_arm_per_config_block(capsys, monkeypatch):
         e = pc[name]
         assert e["ms_per_step"] > 0 and e["tflops"] > 0 and 0 < e["call_roofline"]["frac"]
         assert e["dominant_kernel"]["kernel_us_per_launch"] <= e["ms_per_step"] * 1e3 + 1e-6
+
+
+def test_clock_samples_restricted_to_the_timed_region():
+    """Only nvidia-smi samples whose timestamps fall inside the timed region
+    count; with none inside, all of them count and the line says so."""
+    import datetime
+    t0 = datetime.datetime(2026, 12, 3, 6, 0, 0)
+
+    def line(ms, mhz, watts, cap="Not Active"):
+        ts = (t0 + datetime.timedelta(milliseconds=ms)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, 0, {mhz}, 2070, {watts}, 0x0, Not Active, Not Active, Not Active, {cap}\n"
+
+    lines = [line(0, 2070, 150), line(100, 1800, 1390, "Active"), line(110, 1820, 1395, "Active"), line(300, 2070, 200)]
+    base = t0.timestamp()
+    inside = bench.ClockSampler.parse(lines, (base + 0.05, base + 0.2))
+    assert inside["samples"] == 2 and inside["sm_mhz"] == 1810.0 and inside["reasons"] == ["sw_power_cap"]
+    assert inside["power_w_max"] == 1395.0 and inside["samples_from"] == "the timed region"
+    none_inside = bench.ClockSampler.parse(lines, (base + 0.5, base + 0.6))
+    assert none_inside["samples"] == 4 and none_inside["samples_from"].startswith("around")
+    assert bench.ClockSampler.parse(lines)["samples_from"] == "the whole sampling run"
+    assert bench.ClockSampler.parse(["garbage\n"]) is None
