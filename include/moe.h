@@ -98,11 +98,10 @@ typedef struct moe_problem {
  * moe_resolve_profile return MOE_ERR_UNSUPPORTED for a problem that is not
  * decode-size or whose tables do not fit that kernel's shared memory.
  * SEPARATE: dispatch, the two fused GEMMs and the combine as three kernels
- * chained by programmatic dependent launch. AUTO: ONE_KERNEL where the down
- * GEMM splits K (the smallest batches: measured 132.5 vs 133.0 us for one
- * token at E=384, H=7168, I=3072) and the weights are bf16; SEPARATE
- * otherwise (854.6 vs 860.0 us for eight tokens; with MXFP8 weights 120.5 vs
- * 123.4 us for one token). Other problems ignore the field. */
+ * chained by programmatic dependent launch. AUTO: SEPARATE (measured at one
+ * token, E=384, H=7168, I=3072, down GEMM in 4 K parts: 129.6 vs 131.5 us
+ * with bf16 weights, 117.3 vs 121.8 us with MXFP8 weights). Other problems
+ * ignore the field. */
 typedef enum moe_forward_form {
     MOE_FORWARD_AUTO = 0,
     MOE_FORWARD_SEPARATE = 1,

@@ -316,23 +316,15 @@ moe_status_t check_layout_path(const moe_problem_t &p)
     return (p.weight_layout == MOE_WEIGHTS_MXFP8 && path != MOE_PATH_SMALL_M) ? MOE_ERR_UNSUPPORTED : MOE_OK;
 }
 
-// moe_forward runs as one kernel: asked for, or (AUTO) where the down GEMM
-// splits K, the one case where one kernel measured faster than three chained
-// by programmatic dependent launch.
+// moe_forward runs as one kernel (decode-size batches whose tables fit).
 bool use_megakernel(const moe_problem_t &p)
 {
-    if (p.forward_form == MOE_FORWARD_SEPARATE || !megakernel_possible(p))
-        return false;
-    if (p.forward_form == MOE_FORWARD_ONE_KERNEL)
-        return true;
-    // AUTO: one kernel where the down GEMM splits K (the smallest batches), with
-    // bf16 weights. Measured in one process at T=1, E=384: bf16 132.5 vs 133.0 us
-    // for three kernels; MXFP8 123.4 vs 120.5 us, so MXFP8 keeps three.
-    if (p.weight_layout == MOE_WEIGHTS_MXFP8)
-        return false;
-    int path = 0, tile_rows = 0;
-    resolve(p, &path, &tile_rows);
-    return down_split_k(p, path, tile_rows, device_sm_count()) > 1;
+    // On request only. AUTO keeps three kernels chained by programmatic
+    // dependent launch: measured in one process at T=1, E=384, H=7168,
+    // I=3072 with the down GEMM in 4 K parts, bf16 129.6 vs 131.5 us for one
+    // kernel, MXFP8 117.3 vs 121.8 us (with 2 parts bf16 had been 133.0 vs
+    // 132.5 us, and AUTO took one kernel there).
+    return p.forward_form == MOE_FORWARD_ONE_KERNEL && megakernel_possible(p);
 }
 
 moe_status_t check_form(const moe_problem_t &p)

@@ -151,9 +151,11 @@ def test_launch_profile_table(B):
     """The static profile follows from the shape alone (a = T_max*k/E rows per expert)."""
     P = B.Problem.make
     dec1 = B.moe_resolve_profile(P(1, 384, 6, 7168, 3072))
-    # one token at E=384: 336 full-K down units; 4 K parts (1344 units) fill the waves best
+    # one token at E=384: 336 full-K down units; 4 K parts (1344 units) fill the waves best;
+    # AUTO keeps three kernels (measured faster than one with 4 K parts)
     assert dec1 == dict(path=2, tile_rows=16, down_split_k=4, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1,
-                        megakernel=1, kernel_launches=1)
+                        megakernel=0, kernel_launches=3)
+    assert B.moe_resolve_profile(P(1, 384, 6, 7168, 3072, forward_form=B.MOE_FORWARD_ONE_KERNEL))["megakernel"] == 1
     dec8 = B.moe_resolve_profile(P(8, 384, 6, 7168, 3072))
     assert dec8 == dict(path=2, tile_rows=16, down_split_k=1, pdl=1, fused_gather=1, cta_pair=0, fused_mlp=1,
                         megakernel=0, kernel_launches=3)

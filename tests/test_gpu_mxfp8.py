@@ -97,13 +97,15 @@ def test_quantizer_matches_oracle_decode_shape_sampled(B):
         assert np.array_equal(s2[rows], os_)
 
 
-# (T, E, k, H, I, form): tile 16 with split down GEMM (AUTO: three kernels), tile 16
-# unsplit, tile 16 unsplit as one kernel, tile 32, tile 64
-CASES = [(1, 64, 4, 512, 256, 0), (8, 64, 4, 4096, 256, 0), (8, 64, 4, 4096, 256, 2),
-         (64, 32, 4, 512, 384, 0), (100, 32, 4, 512, 256, 0)]
+# (T, E, k, H, I, form): tile 16 with the down GEMM in 2 K parts (AUTO: three
+# kernels), in 4 K parts (three kernels, then one), tile 16 unsplit, tile 16
+# unsplit as one kernel, tile 32, tile 64
+CASES = [(1, 64, 4, 512, 256, 0), (1, 64, 6, 512, 512, 0), (1, 64, 6, 512, 512, 2), (8, 64, 4, 4096, 256, 0),
+         (8, 64, 4, 4096, 256, 2), (64, 32, 4, 512, 384, 0), (100, 32, 4, 512, 256, 0)]
 
 
-@pytest.mark.parametrize("case", CASES, ids=["t16_split", "t16", "t16_one_kernel", "t32", "t64"])
+@pytest.mark.parametrize("case", CASES, ids=["t16_split2", "t16_split4", "t16_split4_one_kernel", "t16",
+                                             "t16_one_kernel", "t32", "t64"])
 def test_mxfp8_forward_equals_bf16_forward_on_dequantized(B, case):
     T, E, k, H, I, form = case
     wl = wlm.custom("mxf", T, E, k, H, I, seed=T + E + H)
@@ -114,6 +116,11 @@ def test_mxfp8_forward_equals_bf16_forward_on_dequantized(B, case):
     p_mx = B.Problem.make(T, E, k, H, I, weight_layout=B.MOE_WEIGHTS_MXFP8, forward_form=form)
     prof = B.moe_resolve_profile(p_mx)
     assert prof["path"] == 2 and prof["fused_mlp"] == 1
+    # MXFP8 and bf16 weights split the down GEMM's K alike (128-wide blocks)
+    assert prof["down_split_k"] == B.moe_resolve_profile(B.Problem.make(T, E, k, H, I, forward_form=form))[
+        "down_split_k"]
+    if I == 512 and T == 1:
+        assert prof["down_split_k"] == 4
     W13_mx, W2_mx, (q13, s13), (q2, s2) = quantized(B, p_mx, W13, W2)
     W13_d = dequantized_device(q13, s13, W13.shape)
     W2_d = dequantized_device(q2, s2, W2.shape)
