@@ -150,20 +150,25 @@ __device__ __forceinline__ int find_expert(const int *tp, int E, int u, int scal
     return lo;
 }
 
-template <bool kSmallM, int kTileRows, int kOutCols>
+// Unit u of a grouped GEMM. Two orders, both expert-major:
+// - kWeightOuter: column tile, then row tile. The row tiles of one weight tile
+//   go to neighbouring CTAs, which share it in L2 (the M-small GEMMs, and the
+//   CTA-pair gate-up GEMM: `large` gate-up 1079.1 vs 1093.4 us per call
+//   against the other order, in one process, outputs bit-identical);
+// - otherwise: row tile, then column tile. The column tiles of one row tile go
+//   to neighbouring CTAs (the tiled down GEMMs: the other order measured
+//   579.6 vs 573.0 us there).
+template <bool kSmallM, int kTileRows, int kOutCols, bool kWeightOuter = kSmallM>
 __device__ __forceinline__ Unit decode_unit(int u, const int *s_off, const int *s_tp, int E, int NT)
 {
     Unit t;
     int rt_local, nt;
-    if (!kSmallM) {
-        // row-tile major, column tiles inner: CTAs running together share A tiles
+    if (!kWeightOuter) {
         const int rt = u / NT;
         nt = u - rt * NT;
         t.e = find_expert(s_tp, E, rt, 1);
         rt_local = rt - s_tp[t.e];
     } else {
-        // expert, then column tile, then token tile: the token tiles of one
-        // weight tile are dealt to neighbouring CTAs, which share it in L2
         t.e = find_expert(s_tp, E, u, NT);
         const int local = u - s_tp[t.e] * NT;
         const int tiles = s_tp[t.e + 1] - s_tp[t.e];
@@ -1162,10 +1167,20 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                             const uint32_t sc = (codes4 >> (8 * (c >> 1))) & 0xffu;
                             const bool big = sc > 134u;
                             const uint32_t s1 = ((big ? 254u : sc + 120u) << 7) * 0x00010001u;
-                            e4m3x4_to_bf16x4(raw.x, s1, out[o + 0], out[o + 1]);
-                            e4m3x4_to_bf16x4(raw.y, s1, out[o + 2], out[o + 3]);
-                            e4m3x4_to_bf16x4(raw.z, s1, out[o + 4], out[o + 5]);
-                            e4m3x4_to_bf16x4(raw.w, s1, out[o + 6], out[o + 7]);
+                            // 16-row token tiles: the sign-extending permute (decode T=1 114.0 vs
+                            // 117.6 us, T=8 unchanged); wider tiles keep the multiply-add route (the
+                            // permute measured 3% slower on the Zipf small batch). Same bits.
+                            if constexpr (kTileRows == 16) {
+                                e4m3x4_to_bf16x4_sx(raw.x, s1, out[o + 0], out[o + 1]);
+                                e4m3x4_to_bf16x4_sx(raw.y, s1, out[o + 2], out[o + 3]);
+                                e4m3x4_to_bf16x4_sx(raw.z, s1, out[o + 4], out[o + 5]);
+                                e4m3x4_to_bf16x4_sx(raw.w, s1, out[o + 6], out[o + 7]);
+                            } else {
+                                e4m3x4_to_bf16x4(raw.x, s1, out[o + 0], out[o + 1]);
+                                e4m3x4_to_bf16x4(raw.y, s1, out[o + 2], out[o + 3]);
+                                e4m3x4_to_bf16x4(raw.z, s1, out[o + 4], out[o + 5]);
+                                e4m3x4_to_bf16x4(raw.w, s1, out[o + 6], out[o + 7]);
+                            }
                             if (big) {
                                 const uint32_t s2 = ((sc - 7u) << 7) * 0x00010001u;
 #pragma unroll
@@ -1434,7 +1449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0;
         bool ok = true;
         for (int u = cluster_id; ok && u < total_units; u += n_clusters) {
-            const Unit t = decode_unit<false, C::kPairRows, C::kOutCols>(u, s_off, s_tp, E, NT);
+            const Unit t = decode_unit<false, C::kPairRows, C::kOutCols, kGated>(u, s_off, s_tp, E, NT);
             const int n_swap = swap_tokens<C::kSwapRows>(t, swap_ok);
             const int a_row = t.row0 + 128 * static_cast<int>(rank);
             const int w_row = kGated ? t.e * args.w_rows_per_expert + (rank ? args.up_row_offset : 0) + t.n0
@@ -1492,7 +1507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int buf = local & 1;
                 const uint32_t use = (local >> 1) & 1;
                 const int n_swap =
-                    swap_tokens<C::kSwapRows>(decode_unit<false, C::kPairRows, C::kOutCols>(u, s_off, s_tp, E, NT),
+                    swap_tokens<C::kSwapRows>(decode_unit<false, C::kPairRows, C::kOutCols, kGated>(u, s_off, s_tp, E, NT),
                                               swap_ok);
                 const uint32_t idesc = n_swap ? idesc_bf16_f32(256, n_swap) : C::kIdesc;
                 if (!mbar_wait_bounded(smem_u32(&bar_tempty[buf]), use ^ 1u, abort_flag, args.wait_limit_ns)) {
@@ -1537,7 +1552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t xk = 0;   // gate-up exchanges of this warp so far (their mbarrier phases)
         int local = 0;
         for (int u = cluster_id; u < total_units; u += n_clusters, ++local) {
-            const Unit t = decode_unit<false, C::kPairRows, C::kOutCols>(u, s_off, s_tp, E, NT);
+            const Unit t = decode_unit<false, C::kPairRows, C::kOutCols, kGated>(u, s_off, s_tp, E, NT);
             const int n_swap = swap_tokens<C::kSwapRows>(t, swap_ok);
             const int buf = local & 1;
             const uint32_t use = (local >> 1) & 1;

@@ -421,4 +421,19 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t codes, uint32_t s1, ui
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(s1));
 }
 
+// The same map from a sign-extending permute: each code widened to a signed
+// 16-bit v gives the bf16 bits of 2^-120 times its value as (v & 0x087f) << 4
+// (exponent and mantissa bits moved 4 places up, a copy of the sign from bit
+// 11 to bit 15). One instruction fewer per pair of codes.
+__device__ __forceinline__ void e4m3x4_to_bf16x4_sx(uint32_t codes, uint32_t s1, uint32_t &lo, uint32_t &hi)
+{
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(codes));   // (b0, b1), each sign-extended to 16 bits
+    asm("prmt.b32 %0, %1, 0, 0xb3a2;" : "=r"(b) : "r"(codes));   // (b2, b3)
+    a = (a & 0x087f087fu) << 4;
+    b = (b & 0x087f087fu) << 4;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(s1));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(s1));
+}
+
 }  // namespace moe
