@@ -65,6 +65,7 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kUnitRing = 8;     // fused M-small kernel: unit ids in flight between its roles
 constexpr int kBK = 64;          // K elements per stage: one 128-byte swizzle row
 constexpr int kUmmaK = 16;       // K of one tcgen05.mma kind::f16
 constexpr unsigned kFull = 0xffffffffu;
@@ -582,18 +583,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // Both M-small GEMMs of moe_forward in one persistent launch. Units are the
 // gate-up units (rows gathered from x with tile::gather4, SiLU(gate)*up -> h)
-// followed by the down units (h -> y), dealt round-robin over one list, so
-// each CTA finishes its gate-up units before any of its down units. A down
+// followed by the down units (h -> y), in one list. CTA b takes unit b first;
+// every later unit comes from a GPU-wide count (unit = gridDim.x + the
+// count's old value), which the producer asks for one unit ahead so that the
+// atomic's round trip hides behind the current unit's loads. CTAs whose units
+// run faster (an SM nearer its weights' memory, fewer gate-up units) take
+// more units, and the CTAs finish within about one unit of each other; dealt
+// round-robin, they had finished up to 10 us (one token) and 80 us (eight
+// tokens) apart. Units leave the count in list order, so every gate-up unit
+// has an owner before any down unit is handed out, and each CTA finishes its
+// gate-up units before any of its down units. The producer publishes each unit
+// id on a ring of kUnitRing shared slots, which the MMA thread, the converter
+// warps and the epilogue warps read in order (one mbarrier pair per slot). A down
 // unit of expert e needs every gate-up unit of e: each epilogue warp makes
 // its h stores visible (every lane fences, then one lane does a release add
 // on ready[e]); the producer of a down unit waits with a bounded acquire loop
 // until ready[e] = 4 warps * tiles(e) * I/128, then fences the async proxy
 // before its TMA reads of h. No wait can be circular: gate-up units wait on nothing but
 // their own pipeline, and the grid is one CTA per SM, all resident once the
-// (independent) previous kernel leaves. The GPU-wide tail between the two
+// (independent) previous kernel leaves. The count and ready[] are zero when
+// the kernel starts and again when it ends. The GPU-wide tail between the two
 // GEMMs disappears: an SM moves on to down units of finished experts while
-// others still stream gate-up weights. ready[] is zero when the kernel starts
-// and again when it ends: the last CTA to leave clears it.
+// others still stream gate-up weights. The last CTA to leave clears ready[]
+// and the count.
 // A stage holds 32 KB of weights either way: the gate and up tiles of one K
 // block, or two K blocks of a down tile (with two token-tile slots), so the
 // down units keep as many weight bytes in flight as the gate-up units.
@@ -648,6 +660,7 @@ struct FusedArgs {
     GemmArgs down;     // down: act = h, out = y, K = I, n_out = H
     int32_t *ready;    // [E] finished gate-up units per expert, zero at launch and at exit
     int32_t *exits;    // CTAs at the tail, zero at launch and at exit
+    int32_t *next_unit;   // units handed out beyond each CTA's first, zero at launch and at exit
     const uint8_t *sc13;   // MXFP8: scale blocks of W13 and W2 (512 B per 128-row tile and 128-wide K block)
     const uint8_t *sc2;
     // whole-forward form only
@@ -845,6 +858,9 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ __align__(8) uint64_t bar_conv_full[kASlotsRing];    // fp8: weights expanded into a TMEM slot
     __shared__ __align__(8) uint64_t bar_conv_empty[kASlotsRing];   // fp8: the MMAs reading a slot are done
+    __shared__ int s_unit[kUnitRing];                                 // the CTA's units, in order
+    __shared__ __align__(8) uint64_t bar_ufull[kUnitRing];           // a unit id published
+    __shared__ __align__(8) uint64_t bar_uempty[kUnitRing];          // every role has read it
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
     __shared__ int s_T;
@@ -875,6 +891,10 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
             mbar_init(smem_u32(&bar_tempty[b]), 128);
         }
         mbar_init(smem_u32(&bar_drain), 1);
+        for (int i = 0; i < kUnitRing; ++i) {
+            mbar_init(smem_u32(&bar_ufull[i]), 1);
+            mbar_init(smem_u32(&bar_uempty[i]), 5 + C::kConvWarps);   // MMA thread, 4 epilogue warps, converters
+        }
         if (kFp8)
             for (int i = 0; i < kASlotsRing; ++i) {
                 mbar_init(smem_u32(&bar_conv_full[i]), C::kConvWarps);
@@ -925,7 +945,30 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        int uslot = 0;
+        uint32_t uphase = 0;
+        int u = blockIdx.x;
+        const bool dynamic = units1 > static_cast<int>(gridDim.x);
+        while (true) {
+            if (lane == 0) {
+                if (mbar_wait_bounded(smem_u32(&bar_uempty[uslot]), uphase ^ 1u, abort_flag, A1.wait_limit_ns)) {
+                    s_unit[uslot] = ok ? u : total_units;
+                    mbar_arrive(smem_u32(&bar_ufull[uslot]));
+                } else {
+                    ok = false;
+                }
+            }
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            if (++uslot == kUnitRing) {
+                uslot = 0;
+                uphase ^= 1u;
+            }
+            if (!ok || u >= total_units)
+                break;
+            // the unit after this one: asked for after the release above, read after this unit's loads
+            int nxt = u + static_cast<int>(gridDim.x);
+            if (dynamic && lane == 0)
+                nxt = static_cast<int>(gridDim.x) + atomicAdd(fa.next_unit, 1);
             const bool up = u < units1;
             const int v = up ? u : u - units1;
             const Unit t = up ? decode_unit<true, kTileRows, 128>(v, s_off, s_tp, E, NT1)
@@ -1019,6 +1062,7 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                 }
             }
             ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            u = __shfl_sync(kFull, nxt, 0);
         }
         if (!ok && lane == 0) {
             for (int s = 0; s < kStages; ++s)
@@ -1038,8 +1082,21 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
             int slot = 0;
             uint32_t slot_phase = 0;
             bool ok = true;
-            int local = 0;
-            for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++local) {
+            int uslot = 0;
+            uint32_t uphase = 0;
+            for (int local = 0; ok; ++local) {
+                if (!mbar_wait_bounded(smem_u32(&bar_ufull[uslot]), uphase, abort_flag, A1.wait_limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                const int u = s_unit[uslot];
+                mbar_arrive(smem_u32(&bar_uempty[uslot]));
+                if (++uslot == kUnitRing) {
+                    uslot = 0;
+                    uphase ^= 1u;
+                }
+                if (u >= total_units)
+                    break;
                 const bool up = u < units1;
                 const int steps = up ? kb1 : (kb2 + 1) / 2;
                 const int buf = local & 1;
@@ -1122,7 +1179,7 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
         // part p of 128 / parts codes, into TMEM lanes 32q.. of the slot:
         // lane i owns row 32q + i; each TMEM store takes 64 codes as 32
         // columns of bf16 pairs.
-        constexpr int kParts = C::kConvWarps / 8;
+        constexpr int kParts = C::kConvWarps >= 8 ? C::kConvWarps / 8 : 1;   // 1 in the bf16 instances (no converters)
         const int quarter = warp & 3;
         const int half = ((warp - 8) >> 2) & 1;
         const int kpart = (warp - 8) >> 3;
@@ -1132,7 +1189,25 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
         int slot = 0;
         uint32_t slot_phase = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        int uslot = 0;
+        uint32_t uphase = 0;
+        while (ok) {
+            int u = total_units, got = 0;
+            if (lane == 0) {
+                got = mbar_wait_bounded(smem_u32(&bar_ufull[uslot]), uphase, abort_flag, A1.wait_limit_ns) ? 1 : 0;
+                if (got) {
+                    u = s_unit[uslot];
+                    mbar_arrive(smem_u32(&bar_uempty[uslot]));
+                }
+            }
+            got = __shfl_sync(kFull, got, 0);
+            u = __shfl_sync(kFull, u, 0);
+            if (++uslot == kUnitRing) {
+                uslot = 0;
+                uphase ^= 1u;
+            }
+            if (!got || u >= total_units)
+                break;
             const bool up = u < units1;
             const int steps = up ? kb1 : (kb2 + 1) / 2;
             for (int st = 0; st < steps; ++st) {
@@ -1209,8 +1284,25 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
         const int q = warp - 4;
-        int local = 0;
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++local) {
+        int uslot = 0;
+        uint32_t uphase = 0;
+        for (int local = 0;; ++local) {
+            int u = total_units, got = 0;
+            if (lane == 0) {
+                got = mbar_wait_bounded(smem_u32(&bar_ufull[uslot]), uphase, abort_flag, A1.wait_limit_ns) ? 1 : 0;
+                if (got) {
+                    u = s_unit[uslot];
+                    mbar_arrive(smem_u32(&bar_uempty[uslot]));
+                }
+            }
+            got = __shfl_sync(kFull, got, 0);
+            u = __shfl_sync(kFull, u, 0);
+            if (++uslot == kUnitRing) {
+                uslot = 0;
+                uphase ^= 1u;
+            }
+            if (!got || u >= total_units)
+                break;
             const bool up = u < units1;
             const int v = up ? u : u - units1;
             const Unit t = up ? decode_unit<true, kTileRows, 128>(v, s_off, s_tp, E, NT1)
@@ -1307,6 +1399,7 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
         if (threadIdx.x == 0) {
             if (kMega)
                 *fa.done = 0;
+            *fa.next_unit = 0;
             *fa.exits = 0;
         }
     }
@@ -1951,6 +2044,7 @@ cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *r
         fa.sc2 = static_cast<const uint8_t *>(down.w) + rows2 * static_cast<uint64_t>(down.K);
     }
     fa.exits = counters + 1;
+    fa.next_unit = counters + 2;
     if (kMega) {
         fa.ids = mega->ids;
         fa.topk_w = mega->topk_w;

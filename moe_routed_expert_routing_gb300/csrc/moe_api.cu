@@ -23,11 +23,12 @@ struct Layout {
 
 // Workspace header, at fixed offsets so that moe_clear_device_error can clear
 // it without the problem: the error word, then the fused decode kernel's
-// per-expert readiness counts and its two GPU-wide counters. The kernels leave
+// per-expert readiness counts and its three GPU-wide counters (CTAs through
+// their GEMM units, CTAs at the tail, units handed out). The kernels leave
 // the counters at zero after every launch.
 constexpr size_t kReadyOffset = kAlign;
 constexpr size_t kCountersOffset = kReadyOffset + sizeof(int32_t) * kMaxExperts;
-constexpr size_t kHeaderBytes = (kCountersOffset + 2 * sizeof(int32_t) + kAlign - 1) / kAlign * kAlign;
+constexpr size_t kHeaderBytes = (kCountersOffset + 3 * sizeof(int32_t) + kAlign - 1) / kAlign * kAlign;
 
 void resolve(const moe_problem_t &p, int *path, int *tile_rows);
 
