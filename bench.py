@@ -606,7 +606,9 @@ def run_ours(args, world, rank, local):
         },
         "us_per_call": {d["wl"].name: float(sum(s)) * ms_per_step * 1e3 / prof_step_us
                         for d, s in zip(inputs, stage_us)},
-        "us_per_call_note": "each batch's share of the profiled step applied to the timed step",
+        "us_per_call_note": ("each batch's share of the profiled step applied to the timed step; "
+                             "us_per_call_alone: each batch timed in a graph of its own"),
+        "us_per_call_alone": time_alone(B, inputs, stream),
         "profiled_ms_per_step": prof_step_us * 1e-3,
         "stages_us_profiled": {d["wl"].name: stage_dict(d, s) for d, s in zip(inputs, stage_us)},
         "tflops_per_step": flops_step / (ms_per_step * 1e-3) / 1e12,
@@ -641,6 +643,29 @@ def run_ours(args, world, rank, local):
 
 
 PER_CONFIG = ["prefill", "small", "decode"]
+
+
+def time_alone(B, inputs, stream, target_ms: float = 60.0) -> dict:
+    """µs per call of each batch of a multi-batch step, timed on its own: a
+    graph of G calls of that batch alone (G * call >= ~5 ms), replayed so
+    that ~target_ms of work sits between CUDA events, after two warm replays.
+    (The stage shares of the profiled step overstate small batches: the event
+    nodes between their kernels cut the launch overlap the timed graph has.)"""
+    out = {}
+    if len(inputs) < 2:
+        return out
+    for d in inputs:
+        one = capture(stream, lambda s: forward_step(B, [d], stream), 1)
+        replay_timed(stream, one, 2)
+        est_ms = replay_timed(stream, one, 3) / 3
+        G = max(1, min(50, int(math.ceil(5.0 / max(est_ms, 1e-3)))))
+        g = capture(stream, lambda s: forward_step(B, [d], stream), G)
+        reps = max(2, int(math.ceil(target_ms / (G * est_ms))))
+        replay_timed(stream, g, 2)
+        out[d["wl"].name] = replay_timed(stream, g, reps) * 1e3 / (reps * G)
+        del one, g
+    check_device_errors(B, inputs, stream)
+    return out
 
 
 def run_per_config(B, args, device, stream, peaks) -> dict:
@@ -682,6 +707,7 @@ def run_per_config(B, args, device, stream, peaks) -> dict:
             "ms_per_step": ms_per_step,
             "us_per_call": {d["wl"].name: float(sum(s)) * ms_per_step * 1e3 / prof_step_us
                             for d, s in zip(inputs, stage_us)},
+            "us_per_call_alone": time_alone(B, inputs, stream),
             "tflops": flops / (ms_per_step * 1e-3) / 1e12,
             "call_roofline": call_roofline(inputs, ms_per_step, peaks, region_s),
             "dominant_kernel": {k: roof[k] for k in ("kernel", "bound", "achieved", "peak", "unit", "frac",

@@ -156,6 +156,11 @@ def test_gpu_arm_per_config_block(capsys, monkeypatch):
         e = pc[name]
         assert e["ms_per_step"] > 0 and e["tflops"] > 0 and 0 < e["call_roofline"]["frac"]
         assert e["dominant_kernel"]["kernel_us_per_launch"] <= e["ms_per_step"] * 1e3 + 1e-6
+    # decode's two batches are also timed each in a graph of its own
+    alone = pc["decode"]["us_per_call_alone"]
+    assert set(alone) == set(pc["decode"]["us_per_call"]) and len(alone) == 2
+    assert all(v > 0 for v in alone.values())
+    assert pc["prefill"]["us_per_call_alone"] == {}
 
 
 def test_clock_samples_restricted_to_the_timed_region():
