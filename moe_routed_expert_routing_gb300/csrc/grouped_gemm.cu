@@ -82,6 +82,8 @@ struct GemmArgs {
     int up_row_offset;
     int w_packed;       // weights in the PACKED layout (see include/moe.h)
     int out_f16;        // tiled down GEMM: y stored as fp16 (saturated at +-65504) instead of fp32
+    int32_t *sched;     // grouped_gemm_kernel: {units handed out, CTAs at the tail}, zero at launch and at exit;
+                        // null: units dealt round-robin
 };
 
 // TMA coordinates {column, row} of the 128-row weight tile starting at
@@ -343,6 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(8) uint64_t bar_tfull[2];
     __shared__ __align__(8) uint64_t bar_tempty[2];
     __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ int s_unit[kUnitRing];                          // the CTA's units, in order (dynamic deal)
+    __shared__ __align__(8) uint64_t bar_ufull[kUnitRing];     // a unit id published
+    __shared__ __align__(8) uint64_t bar_uempty[kUnitRing];    // the MMA thread and 4 epilogue warps read it
+    __shared__ int s_last;
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
     __shared__ int s_off[kMaxExperts + 1];
@@ -364,6 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bar_tempty[b]), 128);
         }
         mbar_init(smem_u32(&bar_drain), 1);
+        for (int i = 0; i < kUnitRing; ++i) {
+            mbar_init(smem_u32(&bar_ufull[i]), 1);
+            mbar_init(smem_u32(&bar_uempty[i]), 5);
+        }
         s_abort = 0;
         fence_barrier_init();
     }
@@ -394,6 +404,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int NT = (args.n_out + C::kOutCols - 1) / C::kOutCols;   // the last tile may be partly past n_out
     const int total_units = s_tp[E] * NT * kSplitK;
     const int k_blocks = args.K / kBK / kSplitK;   // K blocks of one unit
+    // More units than CTAs (and the counters given): units beyond each CTA's
+    // first come from a GPU-wide count, unit = gridDim.x + its old value,
+    // asked for one unit ahead; the producer publishes them on a ring of
+    // shared slots that the MMA thread and the epilogue warps read in order.
+    // CTAs whose units run faster take more of them. Otherwise every role
+    // deals itself units blockIdx.x, + gridDim.x, ... and the ring is unused.
+    // In one process, against round-robin units (two boxes): the down GEMMs
+    // -3.4% (Zipf small batch, M-small) and -0.5 to -0.7% (prefill, tiled),
+    // prefill's gate-up -0.6%. The M-small gate-up GEMM keeps round-robin
+    // units (+1.2 to 1.4% with the count): there the token tiles of one weight
+    // tile, dealt side by side, read it from L2 together.
+    const bool dynamic =
+        !(kSmallM && kGated) && args.sched != nullptr && total_units > static_cast<int>(gridDim.x);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -403,7 +426,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load in flight, and its phase parity
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        int uslot = 0;
+        uint32_t uphase = 0;
+        int u = blockIdx.x;
+        while (true) {
+            if (dynamic && lane == 0) {
+                if (mbar_wait_bounded(smem_u32(&bar_uempty[uslot]), uphase ^ 1u, abort_flag, args.wait_limit_ns)) {
+                    s_unit[uslot] = ok ? u : total_units;
+                    mbar_arrive(smem_u32(&bar_ufull[uslot]));
+                } else {
+                    ok = false;
+                }
+                if (++uslot == kUnitRing) {
+                    uslot = 0;
+                    uphase ^= 1u;
+                }
+            }
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            if (!ok || u >= total_units)
+                break;
+            // the unit after this one: asked for after the release above, read after this unit's loads
+            int nxt = u + static_cast<int>(gridDim.x);
+            if (dynamic && lane == 0)
+                nxt = static_cast<int>(gridDim.x) + atomicAdd(args.sched, 1);
             const Unit t = decode_unit<kSmallM, kTileRows, C::kOutCols>(u / kSplitK, s_off, s_tp, E, NT);
             const int kb0 = (u % kSplitK) * k_blocks;
             const int w_row0 = t.e * args.w_rows_per_expert + t.n0;
@@ -448,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;   // s_rows is rewritten only after lane 0 issued
+            u = __shfl_sync(kFull, nxt, 0);
         }
         if (!ok && lane == 0) {
             // give-up path: let every load still in flight land before the CTA exits
@@ -466,8 +512,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            int local = 0;
-            for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++local) {
+            int uslot = 0;
+            uint32_t uphase = 0;
+            for (int local = 0; ok; ++local) {
+                int u = static_cast<int>(blockIdx.x + local * gridDim.x);
+                if (dynamic) {
+                    if (!mbar_wait_bounded(smem_u32(&bar_ufull[uslot]), uphase, abort_flag, args.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    u = s_unit[uslot];
+                    mbar_arrive(smem_u32(&bar_uempty[uslot]));
+                    if (++uslot == kUnitRing) {
+                        uslot = 0;
+                        uphase ^= 1u;
+                    }
+                }
+                if (u >= total_units)
+                    break;
                 const int buf = local & 1;
                 const uint32_t use = (local >> 1) & 1;
                 if (!mbar_wait_bounded(smem_u32(&bar_tempty[buf]), use ^ 1u, abort_flag, args.wait_limit_ns)) {
@@ -518,8 +580,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
         const int q = warp - 4;  // TMEM lanes [32q, 32q + 32)
-        int local = 0;
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++local) {
+        int uslot = 0;
+        uint32_t uphase = 0;
+        for (int local = 0;; ++local) {
+            int u = static_cast<int>(blockIdx.x + local * gridDim.x);
+            if (dynamic) {
+                int got = 0;
+                if (lane == 0) {
+                    got = mbar_wait_bounded(smem_u32(&bar_ufull[uslot]), uphase, abort_flag, args.wait_limit_ns) ? 1
+                                                                                                                  : 0;
+                    if (got) {
+                        u = s_unit[uslot];
+                        mbar_arrive(smem_u32(&bar_uempty[uslot]));
+                    }
+                }
+                got = __shfl_sync(kFull, got, 0);
+                u = __shfl_sync(kFull, u, 0);
+                if (++uslot == kUnitRing) {
+                    uslot = 0;
+                    uphase ^= 1u;
+                }
+                if (!got)
+                    break;
+            }
+            if (u >= total_units)
+                break;
             const Unit t = decode_unit<kSmallM, kTileRows, C::kOutCols>(u / kSplitK, s_off, s_tp, E, NT);
             const int buf = local & 1;
             const uint32_t use = (local >> 1) & 1;
@@ -569,6 +654,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    // the last CTA out returns the count to zero (every CTA's last atomic on
+    // it precedes its own add here, in the same thread); a dependent launch
+    // reads it only after its wait on this grid
+    if (threadIdx.x == 0 && args.sched && dynamic)
+        s_last = atom_add_acq_rel_gpu(args.sched + 1, 1) == static_cast<int>(gridDim.x) - 1;
+    __syncthreads();
+    if (threadIdx.x == 0 && args.sched && dynamic && s_last) {
+        args.sched[0] = 0;
+        args.sched[1] = 0;
+    }
     pdl_trigger();
     if (warp == 2) {
         tc_fence_after();
@@ -1849,6 +1944,7 @@ cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
     a.up_row_offset = p.up_row_offset;
     a.w_packed = p.w_packed ? 1 : 0;
     a.out_f16 = p.out_f16 ? 1 : 0;
+    a.sched = p.sched;
     // Upper bound of the units any routing can produce; no more CTAs than that.
     const long long max_row_tiles = (static_cast<long long>(p.cap) + kTileRows - 1) / kTileRows + p.E;
     const long long max_units = max_row_tiles * ((p.n_out + C::kOutCols - 1) / C::kOutCols) * kSplitK;
@@ -1920,6 +2016,7 @@ cudaError_t run_pair(const GemmProblem &p, int num_sms, cudaStream_t stream)
     a.up_row_offset = p.up_row_offset;
     a.w_packed = p.w_packed ? 1 : 0;
     a.out_f16 = p.out_f16 ? 1 : 0;
+    a.sched = nullptr;
     const long long max_units =
         ((static_cast<long long>(p.cap) + 255) / 256 + p.E) * ((p.n_out + C::kOutCols - 1) / C::kOutCols);
     long long clusters = max_units < max_clusters ? max_units : max_clusters;
@@ -1947,6 +2044,7 @@ GemmArgs make_args(const GemmProblem &p)
     a.up_row_offset = p.up_row_offset;
     a.w_packed = p.w_packed ? 1 : 0;
     a.out_f16 = 0;
+    a.sched = nullptr;
     return a;
 }
 

@@ -24,11 +24,12 @@ struct Layout {
 // Workspace header, at fixed offsets so that moe_clear_device_error can clear
 // it without the problem: the error word, then the fused decode kernel's
 // per-expert readiness counts and its three GPU-wide counters (CTAs through
-// their GEMM units, CTAs at the tail, units handed out). The kernels leave
+// their GEMM units, CTAs at the tail, units handed out), then the separate
+// grouped GEMMs' two (units handed out, CTAs at the tail). The kernels leave
 // the counters at zero after every launch.
 constexpr size_t kReadyOffset = kAlign;
 constexpr size_t kCountersOffset = kReadyOffset + sizeof(int32_t) * kMaxExperts;
-constexpr size_t kHeaderBytes = (kCountersOffset + 3 * sizeof(int32_t) + kAlign - 1) / kAlign * kAlign;
+constexpr size_t kHeaderBytes = (kCountersOffset + 5 * sizeof(int32_t) + kAlign - 1) / kAlign * kAlign;
 
 void resolve(const moe_problem_t &p, int *path, int *tile_rows);
 
@@ -239,6 +240,7 @@ moe_status_t enqueue_expert_compute(const moe_problem_t &p, const void *act, con
     g.tile_rows = tile_rows;
     g.split_k = 1;
     g.pdl = path == MOE_PATH_SMALL_M;
+    g.sched = at<int32_t>(ws, L.counters) + 3;
     // gate-up with the fused SiLU(gate) * up epilogue: x_sorted[cap, H] x W13[E, 2I, H] -> h[cap, I]
     g.act = act;
     g.gather = gather_perm != nullptr || mega != nullptr;

@@ -152,6 +152,9 @@ struct GemmProblem {
     bool w_packed;            // `w` is in the access-ordered PACKED layout
     bool w_mxfp8;             // `w` is in the MXFP8 layout (codes, then scale blocks): fused kernel only
     bool out_f16;             // tiled down GEMM: y as fp16 (saturated; MOE_DEVERR_Y_RANGE if clipped)
+    int32_t *sched = nullptr; // single-CTA grouped GEMM (M-small and tiled): two workspace counters (units
+                              // handed out, CTAs at the tail), zero before the launch and left zero by it;
+                              // null: units dealt round-robin
 };
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);
