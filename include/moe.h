@@ -145,13 +145,15 @@ typedef enum moe_weight_layout {
 
 /* Bytes of workspace every entry point below needs for `problem` (pure host
  * arithmetic, no CUDA call). The same workspace serves all entry points; it
- * holds the device error word, the decode kernel's counters, dispatch
- * scratch, the activation h[cap, I] and, for moe_forward, the sorted batches.
- * A new workspace must be zero-filled (cudaMemset, or moe_clear_device_error)
- * before its first moe_forward call; every call leaves its counters at zero
- * again (FlashInfer moe_ep page, launch-path notes: workspaces allocated
- * zeroed, counters cleaned by the kernel's tail), so no per-call clearing is
- * needed. */
+ * holds the device error word, the GEMM kernels' counters (readiness counts
+ * and the GPU-wide counts their CTAs take units from), dispatch scratch, the
+ * activation h[cap, I] and, for moe_forward, the sorted batches. A new
+ * workspace must be zero-filled (cudaMemset, or moe_clear_device_error)
+ * before its first moe_forward or moe_expert_compute call: with stale
+ * counters the GEMMs would skip units. Every call leaves its counters at zero
+ * again, also after a timed-out wait (FlashInfer moe_ep page, launch-path
+ * notes: workspaces allocated zeroed, counters cleaned by the kernel's tail),
+ * so no per-call clearing is needed. */
 moe_status_t moe_workspace_size(const moe_problem_t *problem, size_t *bytes);
 
 /* Which expert-GEMM path `problem` resolves to (MOE_PATH_TILED,
@@ -213,6 +215,8 @@ moe_status_t moe_dispatch(const moe_problem_t *problem, const int32_t *topk_ids,
  *   W2[E, H, I] bf16, y_sorted[cap, H] fp32 out (rows past the valid count
  *   are not written), expert_offsets[E+1] as produced by moe_dispatch.
  * y_sorted stays fp32 so that the combine rounds to bf16 once, at the end.
+ * ws: a zero-filled workspace (see moe_workspace_size), left with its
+ * counters at zero.
  */
 moe_status_t moe_expert_compute(const moe_problem_t *problem, const void *x_sorted,
                                 const int32_t *expert_offsets, const void *W13, const void *W2,
@@ -320,8 +324,9 @@ moe_status_t moe_quantize_weights(const moe_problem_t *problem, const void *W13,
  * Synchronises `stream` (the only entry point that does). */
 moe_status_t moe_last_device_error(const void *ws, void *stream, int32_t *host_code);
 
-/* Clear the device error word and the decode kernel's counters (enqueued on
- * `stream`); also readies a workspace of unknown contents for moe_forward. */
+/* Clear the device error word and the GEMM kernels' counters (enqueued on
+ * `stream`); also readies a workspace of unknown contents for moe_forward
+ * and moe_expert_compute. */
 moe_status_t moe_clear_device_error(void *ws, void *stream);
 
 /* Human-readable name of a status. Never NULL. */
