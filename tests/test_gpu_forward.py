@@ -263,6 +263,51 @@ def test_megakernel_equals_separate_entry_points(B, shape, parts):
     assert_within_tolerance(wlm.bf16_bits(got.out), ref_acc, f"megakernel {shape}")
 
 
+# error word, per-expert readiness counts, the fused kernel's three GPU-wide
+# counters and the separate grouped GEMMs' two (units handed out, CTAs at the tail)
+HEADER_BYTES = 256 + 4 * (1024 + 5)
+
+
+@pytest.mark.parametrize("path", [1, 2, 3], ids=["pair", "small_m", "tiled_1cta"])
+def test_unit_counts_return_to_zero(B, path):
+    """GEMMs with more units than CTAs take units from GPU-wide counts in the
+    workspace header (the M-small down GEMM and the single-CTA tiled GEMMs);
+    after every call of moe_forward and of moe_expert_compute the header is
+    zero again, repeated calls are bit-identical, and the output matches the
+    oracle on a token subset."""
+    wl = wlm.custom("units", 1024, 16, 4, 1024, 1024, seed=71)
+    dw = DeviceWorkload(wl)
+    p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, path=path)
+    bufs = B.Buffers(p)
+    first = None
+    for _ in range(3):
+        forward(B, p, dw, bufs)
+        assert B.moe_last_device_error(bufs.ws) == 0
+        assert int(bufs.ws[:HEADER_BYTES].count_nonzero()) == 0
+        if first is None:
+            first = bufs.out.clone()
+        assert torch.equal(first.view(torch.int16), bufs.out.view(torch.int16))
+    tokens = wlm.token_subset(wl, 64)
+    ref_acc, _ = dw.oracle_out(tokens)
+    assert_within_tolerance(wlm.bf16_bits(first)[tokens], ref_acc, f"path {path}")
+    # moe_expert_compute on the same workspace, twice
+    cap = p.cap
+    offs = torch.empty(wl.E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(cap, dtype=torch.int32, device="cuda")
+    inv = torch.empty(wl.T * wl.k, dtype=torch.int32, device="cuda")
+    xs = torch.zeros((cap, wl.H), dtype=torch.bfloat16, device="cuda")
+    B.moe_dispatch(p, dw.ids, offs, perm, inv, bufs.ws, x=dw.x, x_sorted=xs)
+    ys = []
+    for _ in range(2):
+        y = torch.zeros((cap, wl.H), dtype=torch.float32, device="cuda")
+        B.moe_expert_compute(p, xs, offs, dw.W13, dw.W2, y, bufs.ws)
+        torch.cuda.synchronize()
+        assert B.moe_last_device_error(bufs.ws) == 0
+        assert int(bufs.ws[:HEADER_BYTES].count_nonzero()) == 0
+        ys.append(y)
+    assert torch.equal(ys[0], ys[1])
+
+
 def test_megakernel_tail_clears_its_counters(B):
     """Workspace header after every call: error word, readiness counts and the
     two GPU-wide counters all back at zero; repeated calls bit-identical. A
@@ -272,7 +317,7 @@ def test_megakernel_tail_clears_its_counters(B):
     p = B.Problem.make(wl.T, wl.E, wl.k, wl.H, wl.I, forward_form=B.MOE_FORWARD_ONE_KERNEL)
     assert B.moe_resolve_profile(p)["megakernel"] == 1
     bufs = B.Buffers(p)
-    header = 256 + 4 * (1024 + 2)
+    header = HEADER_BYTES
     first = None
     for _ in range(4):
         forward(B, p, dw, bufs)
