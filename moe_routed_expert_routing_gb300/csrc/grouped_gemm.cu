@@ -65,7 +65,7 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnitRing = 8;     // fused M-small kernel: unit ids in flight between its roles
+constexpr int kUnitRing = 8;     // persistent single-CTA GEMMs: unit ids in flight between their roles
 constexpr int kBK = 64;          // K elements per stage: one 128-byte swizzle row
 constexpr int kUmmaK = 16;       // K of one tcgen05.mma kind::f16
 constexpr unsigned kFull = 0xffffffffu;
@@ -137,6 +137,65 @@ struct Cfg {
 
 struct Unit {
     int e, row0, rows, n0;
+};
+
+// A CTA's ring of unit ids (kUnitRing shared slots, an mbarrier pair each):
+// the TMA producer publishes the units it loads, in order; the roles after it
+// (the MMA thread, converter and epilogue warps) take them in the same order.
+// Each thread keeps its own cursor; every wait is bounded.
+struct UnitRing {
+    int *ids;
+    uint64_t *full;    // a unit id published (one arrival)
+    uint64_t *empty;   // every reader has taken it
+    int slot;
+    uint32_t phase;
+
+    __device__ __forceinline__ UnitRing(int *i, uint64_t *f, uint64_t *e) : ids(i), full(f), empty(e), slot(0), phase(0)
+    {
+    }
+    __device__ __forceinline__ void advance()
+    {
+        if (++slot == kUnitRing) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+    // the producer (one thread)
+    __device__ __forceinline__ bool publish(int u, volatile int *abort, uint64_t limit_ns)
+    {
+        if (!mbar_wait_bounded(smem_u32(&empty[slot]), phase ^ 1u, abort, limit_ns))
+            return false;
+        ids[slot] = u;
+        mbar_arrive(smem_u32(&full[slot]));
+        advance();
+        return true;
+    }
+    // a reader of one thread
+    __device__ __forceinline__ bool take(int &u, volatile int *abort, uint64_t limit_ns)
+    {
+        if (!mbar_wait_bounded(smem_u32(&full[slot]), phase, abort, limit_ns))
+            return false;
+        u = ids[slot];
+        mbar_arrive(smem_u32(&empty[slot]));
+        advance();
+        return true;
+    }
+    // a reader warp: lane 0 waits and takes, every lane gets the id
+    __device__ __forceinline__ bool take_warp(int &u, int lane, volatile int *abort, uint64_t limit_ns)
+    {
+        int got = 0, v = 0;
+        if (lane == 0) {
+            got = mbar_wait_bounded(smem_u32(&full[slot]), phase, abort, limit_ns) ? 1 : 0;
+            if (got) {
+                v = ids[slot];
+                mbar_arrive(smem_u32(&empty[slot]));
+            }
+        }
+        got = __shfl_sync(0xffffffffu, got, 0);
+        u = __shfl_sync(0xffffffffu, v, 0);
+        advance();
+        return got != 0;
+    }
 };
 
 // Largest e in [0, E) with tp[e] * scale <= u (tp non-decreasing, tp[0] = 0).
@@ -426,22 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load in flight, and its phase parity
         bool ok = true;
-        int uslot = 0;
-        uint32_t uphase = 0;
+        UnitRing ring(s_unit, bar_ufull, bar_uempty);
         int u = blockIdx.x;
         while (true) {
-            if (dynamic && lane == 0) {
-                if (mbar_wait_bounded(smem_u32(&bar_uempty[uslot]), uphase ^ 1u, abort_flag, args.wait_limit_ns)) {
-                    s_unit[uslot] = ok ? u : total_units;
-                    mbar_arrive(smem_u32(&bar_ufull[uslot]));
-                } else {
-                    ok = false;
-                }
-                if (++uslot == kUnitRing) {
-                    uslot = 0;
-                    uphase ^= 1u;
-                }
-            }
+            if (dynamic && lane == 0 && !ring.publish(ok ? u : total_units, abort_flag, args.wait_limit_ns))
+                ok = false;
             ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
             if (!ok || u >= total_units)
                 break;
@@ -512,21 +560,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            int uslot = 0;
-            uint32_t uphase = 0;
+            UnitRing ring(s_unit, bar_ufull, bar_uempty);
             for (int local = 0; ok; ++local) {
                 int u = static_cast<int>(blockIdx.x + local * gridDim.x);
-                if (dynamic) {
-                    if (!mbar_wait_bounded(smem_u32(&bar_ufull[uslot]), uphase, abort_flag, args.wait_limit_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    u = s_unit[uslot];
-                    mbar_arrive(smem_u32(&bar_uempty[uslot]));
-                    if (++uslot == kUnitRing) {
-                        uslot = 0;
-                        uphase ^= 1u;
-                    }
+                if (dynamic && !ring.take(u, abort_flag, args.wait_limit_ns)) {
+                    ok = false;
+                    break;
                 }
                 if (u >= total_units)
                     break;
@@ -580,29 +619,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
         const int q = warp - 4;  // TMEM lanes [32q, 32q + 32)
-        int uslot = 0;
-        uint32_t uphase = 0;
+        UnitRing ring(s_unit, bar_ufull, bar_uempty);
         for (int local = 0;; ++local) {
             int u = static_cast<int>(blockIdx.x + local * gridDim.x);
-            if (dynamic) {
-                int got = 0;
-                if (lane == 0) {
-                    got = mbar_wait_bounded(smem_u32(&bar_ufull[uslot]), uphase, abort_flag, args.wait_limit_ns) ? 1
-                                                                                                                  : 0;
-                    if (got) {
-                        u = s_unit[uslot];
-                        mbar_arrive(smem_u32(&bar_uempty[uslot]));
-                    }
-                }
-                got = __shfl_sync(kFull, got, 0);
-                u = __shfl_sync(kFull, u, 0);
-                if (++uslot == kUnitRing) {
-                    uslot = 0;
-                    uphase ^= 1u;
-                }
-                if (!got)
-                    break;
-            }
+            if (dynamic && !ring.take_warp(u, lane, abort_flag, args.wait_limit_ns))
+                break;
             if (u >= total_units)
                 break;
             const Unit t = decode_unit<kSmallM, kTileRows, C::kOutCols>(u / kSplitK, s_off, s_tp, E, NT);
@@ -1040,24 +1061,13 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
         bool ok = true;
-        int uslot = 0;
-        uint32_t uphase = 0;
+        UnitRing ring(s_unit, bar_ufull, bar_uempty);
         int u = blockIdx.x;
         const bool dynamic = units1 > static_cast<int>(gridDim.x);
         while (true) {
-            if (lane == 0) {
-                if (mbar_wait_bounded(smem_u32(&bar_uempty[uslot]), uphase ^ 1u, abort_flag, A1.wait_limit_ns)) {
-                    s_unit[uslot] = ok ? u : total_units;
-                    mbar_arrive(smem_u32(&bar_ufull[uslot]));
-                } else {
-                    ok = false;
-                }
-            }
+            if (lane == 0 && !ring.publish(ok ? u : total_units, abort_flag, A1.wait_limit_ns))
+                ok = false;
             ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
-            if (++uslot == kUnitRing) {
-                uslot = 0;
-                uphase ^= 1u;
-            }
             if (!ok || u >= total_units)
                 break;
             // the unit after this one: asked for after the release above, read after this unit's loads
@@ -1177,18 +1187,12 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
             int slot = 0;
             uint32_t slot_phase = 0;
             bool ok = true;
-            int uslot = 0;
-            uint32_t uphase = 0;
+            UnitRing ring(s_unit, bar_ufull, bar_uempty);
             for (int local = 0; ok; ++local) {
-                if (!mbar_wait_bounded(smem_u32(&bar_ufull[uslot]), uphase, abort_flag, A1.wait_limit_ns)) {
+                int u = total_units;
+                if (!ring.take(u, abort_flag, A1.wait_limit_ns)) {
                     ok = false;
                     break;
-                }
-                const int u = s_unit[uslot];
-                mbar_arrive(smem_u32(&bar_uempty[uslot]));
-                if (++uslot == kUnitRing) {
-                    uslot = 0;
-                    uphase ^= 1u;
                 }
                 if (u >= total_units)
                     break;
@@ -1284,24 +1288,10 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
         int slot = 0;
         uint32_t slot_phase = 0;
         bool ok = true;
-        int uslot = 0;
-        uint32_t uphase = 0;
+        UnitRing ring(s_unit, bar_ufull, bar_uempty);
         while (ok) {
-            int u = total_units, got = 0;
-            if (lane == 0) {
-                got = mbar_wait_bounded(smem_u32(&bar_ufull[uslot]), uphase, abort_flag, A1.wait_limit_ns) ? 1 : 0;
-                if (got) {
-                    u = s_unit[uslot];
-                    mbar_arrive(smem_u32(&bar_uempty[uslot]));
-                }
-            }
-            got = __shfl_sync(kFull, got, 0);
-            u = __shfl_sync(kFull, u, 0);
-            if (++uslot == kUnitRing) {
-                uslot = 0;
-                uphase ^= 1u;
-            }
-            if (!got || u >= total_units)
+            int u = total_units;
+            if (!ring.take_warp(u, lane, abort_flag, A1.wait_limit_ns) || u >= total_units)
                 break;
             const bool up = u < units1;
             const int steps = up ? kb1 : (kb2 + 1) / 2;
@@ -1379,24 +1369,10 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
         const int q = warp - 4;
-        int uslot = 0;
-        uint32_t uphase = 0;
+        UnitRing ring(s_unit, bar_ufull, bar_uempty);
         for (int local = 0;; ++local) {
-            int u = total_units, got = 0;
-            if (lane == 0) {
-                got = mbar_wait_bounded(smem_u32(&bar_ufull[uslot]), uphase, abort_flag, A1.wait_limit_ns) ? 1 : 0;
-                if (got) {
-                    u = s_unit[uslot];
-                    mbar_arrive(smem_u32(&bar_uempty[uslot]));
-                }
-            }
-            got = __shfl_sync(kFull, got, 0);
-            u = __shfl_sync(kFull, u, 0);
-            if (++uslot == kUnitRing) {
-                uslot = 0;
-                uphase ^= 1u;
-            }
-            if (!got || u >= total_units)
+            int u = total_units;
+            if (!ring.take_warp(u, lane, abort_flag, A1.wait_limit_ns) || u >= total_units)
                 break;
             const bool up = u < units1;
             const int v = up ? u : u - units1;
