@@ -85,6 +85,19 @@ def test_dispatch_dropped_and_invalid_ids(B, T):
     assert B.moe_last_device_error(ws) == 0
 
 
+@pytest.mark.parametrize("T,k,E", [(3000, 4, 1000), (2500, 8, 48), (4096, 2, 33), (1100, 1, 1), (9000, 8, 700)])
+def test_dispatch_many_blocks_any_expert_count(B, T, k, E):
+    """Multi-block dispatch (count, scan, scatter) at expert counts from 1 to
+    1000, powers of two or not, against the oracle, bit-exact."""
+    rng = np.random.default_rng(T + E)
+    ids_np = np.stack([rng.choice(E, size=k, replace=False) if E >= k else rng.integers(0, E, size=k)
+                       for _ in range(T)]).astype(np.int32)
+    p = B.Problem.make(T, E, k, 256, 128)
+    offs, perm, inv, _, ws = run_dispatch(B, p, torch.from_numpy(ids_np).cuda())
+    check_dispatch_exact(ids_np, E, offs, perm, inv)
+    assert int(offs[-1]) == T * k and B.moe_last_device_error(ws) == 0
+
+
 def test_dispatch_one_hot_expert_many_blocks(B):
     # 5000 slots all on expert 2: spans several dispatch blocks; stability = identity order
     T, k, E = 5000, 1, 4
