@@ -134,12 +134,15 @@ typedef enum moe_weight_layout {
  *           GEMMs read them: for each 128-row tile (rows counted over all
  *           experts), each 128-wide K block: 128 rows x 4 bytes, the scales of
  *           the row's four 32-element sub-blocks; scale code = e + 127.
- * moe_forward reads MXFP8 weights on the M-small path (a = T_max*k/E <= 16,
- * the HBM-bound decode shapes, where the weights are nearly all the bytes):
- * it streams the 1-byte codes and expands X * P to bf16 on the chip, exactly,
- * then multiplies by the bf16 activations as for bf16 weights. Activations,
- * h and the output stay bf16 (SiLU(gate)*up rounded to bf16 as before), so
- * the result is the bf16 forward on the dequantized weights. Other paths and
+ * moe_forward reads MXFP8 weights on the M-small path, which MOE_PATH_AUTO
+ * takes for this layout at every batch size (token tiles of 16, 32 or 64
+ * rows by a = T_max*k/E): it streams the 1-byte codes and expands X * P to
+ * bf16 on the chip, exactly, then multiplies by the bf16 activations as for
+ * bf16 weights. Activations, h and the output stay bf16 (SiLU(gate)*up
+ * rounded to bf16 as before), so the result is the bf16 forward on the
+ * dequantized weights. Each token tile of an expert expands its weight tiles
+ * again, so batches with many rows per expert (a >= 256) run slower than
+ * with bf16 weights on the tiled path. A tiled path asked for explicitly and
  * moe_expert_compute return MOE_ERR_UNSUPPORTED for this layout. Weights must
  * be finite with every block maximum in [2^-110, 2^24). */
 

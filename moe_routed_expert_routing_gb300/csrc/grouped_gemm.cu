@@ -789,6 +789,10 @@ struct FusedArgs {
     int32_t *perm_out;             // [cap] for the caller
     __nv_bfloat16 *out;            // [T_max, H]
     int32_t *done;                 // CTAs through with their GEMM units, zero at launch and at exit
+    // MXFP8, separate form: the gate-up activation rows come from a sorted
+    // copy (x_sorted, one 2-D TMA box of kTileRows rows per 64-wide K block)
+    // instead of tile::gather4 from x through perm
+    int act_sorted;
 };
 
 // Local dispatch of all routed slots inside one CTA (every CTA of the
@@ -1080,7 +1084,7 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                               : decode_unit<true, kTileRows, 128>(v / kSplitDown, s_off, s_tp, E, NT2);
             const int kb0 = up ? 0 : (v % kSplitDown) * kb2;
             const int steps = up ? kb1 : (kb2 + 1) / 2;   // down: two K blocks per stage
-            if (up) {
+            if (up && !fa.act_sorted) {
                 for (int i = lane; i < kTileRows; i += 32)
                     s_rows[i] = i < t.rows ? (kMega ? s_perm[t.row0 + i] : __ldg(A1.perm + t.row0 + i)) / A1.k : 0;
                 __syncwarp();
@@ -1119,11 +1123,16 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                         bulk_load(sc_dst + 512, fa.sc13 + (((wr + A1.up_row_offset) / 128) * kbt + st) * 512, 512,
                                   full, pol_w);
 #pragma unroll
-                        for (int j = 0; j < 2; ++j)
+                        for (int j = 0; j < 2; ++j) {
+                            if (fa.act_sorted) {   // the tile's rows of x_sorted, one box (the same bytes)
+                                tma_load_2d(a_dst + j * C::kActSlot, &tm_x, full, st * 128 + 64 * j, t.row0, pol_a);
+                            } else {
 #pragma unroll
-                            for (int q = 0; q < kTileRows / 4; ++q)
-                                tma_gather4(a_dst + j * C::kActSlot + q * 512, &tm_x, full, st * 128 + 64 * j,
-                                            reinterpret_cast<const int4 *>(s_rows)[q], pol_a);
+                                for (int q = 0; q < kTileRows / 4; ++q)
+                                    tma_gather4(a_dst + j * C::kActSlot + q * 512, &tm_x, full, st * 128 + 64 * j,
+                                                reinterpret_cast<const int4 *>(s_rows)[q], pol_a);
+                            }
+                        }
                     } else if (kFp8) {
                         const int nkb = (2 * st + 1 < kb2) ? 2 : 1;
                         mbar_arrive_expect_tx(full, nkb * (C::kWBytes / 2 + 512 + 2 * C::kActSlot));
@@ -2106,10 +2115,14 @@ cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *r
     const bool maps = kFp8 ? make_map_codes(&tm_w13, up.w, rows13, static_cast<uint64_t>(up.K)) &&
                                  make_map_codes(&tm_w2, down.w, rows2, static_cast<uint64_t>(down.K))
                            : make_weight_map(&tm_w13, up) && make_weight_map(&tm_w2, down);
-    if (!maps || !make_map(&tm_x, up.act, static_cast<uint64_t>(up.act_rows), static_cast<uint64_t>(up.K), 1) ||
+    // gathered rows: a one-row box for tile::gather4; sorted rows (MXFP8,
+    // separate form): a box of the tile's rows
+    const uint32_t x_box = up.gather ? 1u : static_cast<uint32_t>(kTileRows);
+    if (!maps || !make_map(&tm_x, up.act, static_cast<uint64_t>(up.act_rows), static_cast<uint64_t>(up.K), x_box) ||
         !make_map(&tm_h, down.act, static_cast<uint64_t>(down.cap), static_cast<uint64_t>(down.K), kTileRows))
         return cudaErrorInvalidValue;
     FusedArgs fa = {};
+    fa.act_sorted = up.gather ? 0 : 1;
     fa.up = make_args(up);
     fa.down = make_args(down);
     fa.ready = ready;
@@ -2187,12 +2200,14 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, int num_sms, cudaStream_t 
 cudaError_t launch_fused_small(const GemmProblem &up, const GemmProblem &down, int32_t *ready, int32_t *counters,
                                int num_sms, cudaStream_t stream, const MegaParams *mega)
 {
-    if (!up.small_m || !down.small_m || !up.gated || down.gated || !up.gather || up.tile_rows != down.tile_rows ||
-        !ready || !counters || (down.split_k != 1 && down.split_k != 2 && down.split_k != 4))
+    // rows gathered from x through perm, or (MXFP8 weights, separate form) a sorted copy
+    if (!up.small_m || !down.small_m || !up.gated || down.gated || up.tile_rows != down.tile_rows || !ready ||
+        !counters || (down.split_k != 1 && down.split_k != 2 && down.split_k != 4) ||
+        (!up.gather && (mega || !up.w_mxfp8)))
         return cudaErrorInvalidValue;
     if (mega ? (!mega->ids || !mega->topk_w || !mega->expert_offsets_out || !mega->perm_out || !mega->out ||
                 mega->T_max < 1)
-             : !up.perm)
+             : (up.gather && !up.perm))
         return cudaErrorInvalidValue;
     if (up.w_mxfp8 != down.w_mxfp8)
         return cudaErrorInvalidValue;

@@ -121,8 +121,12 @@ void resolve(const moe_problem_t &p, int *path, int *tile_rows)
     // M-small up to 16 routed rows per expert on average; single-CTA 128-row
     // tiles below 256 (a 256-row pair tile would mostly multiply padding rows:
     // measured 26% slower on 32 rows per expert); CTA pairs from 256 rows.
+    // MXFP8 weights: the M-small path at every batch size (its fused kernel
+    // is the one that expands them).
     if (chosen == MOE_PATH_AUTO)
-        chosen = avg_rows <= 16.0 ? MOE_PATH_SMALL_M : (avg_rows < 256.0 ? MOE_PATH_TILED_1CTA : MOE_PATH_TILED);
+        chosen = (avg_rows <= 16.0 || p.weight_layout == MOE_WEIGHTS_MXFP8)
+                     ? MOE_PATH_SMALL_M
+                     : (avg_rows < 256.0 ? MOE_PATH_TILED_1CTA : MOE_PATH_TILED);
     *path = chosen;
     if (chosen == MOE_PATH_TILED || chosen == MOE_PATH_TILED_1CTA)
         *tile_rows = 128;
@@ -311,6 +315,17 @@ bool fused_mlp_of(const moe_problem_t &p, int path, int tile_rows)
     return path == MOE_PATH_SMALL_M && (tile_rows == 16 || p.weight_layout == MOE_WEIGHTS_MXFP8);
 }
 
+// moe_forward's gate-up GEMM gathers its activation rows from x itself
+// (tile::gather4 through perm), with no x_sorted and no gather kernel: the
+// M-small path, except MXFP8 weights on token tiles of 32 or more rows, whose
+// stages hold two 64-wide K blocks of the tile (16 or 32 gather4 each, where
+// the TMA issue rate sets the pace: the tiled paths read a materialised
+// x_sorted for the same reason).
+bool gemm_gathers_rows(const moe_problem_t &p, int path, int tile_rows)
+{
+    return path == MOE_PATH_SMALL_M && !(p.weight_layout == MOE_WEIGHTS_MXFP8 && tile_rows >= 32);
+}
+
 // MXFP8 weights are read by the M-small path only.
 moe_status_t check_layout_path(const moe_problem_t &p)
 {
@@ -344,7 +359,7 @@ int forward_launches(const moe_problem_t &p)
         return 1;
     const long long R = static_cast<long long>(p.T_max) * p.k;
     int n = R <= kDispatchSlotsPerBlock ? 1 : 3;            // dispatch
-    n += path == MOE_PATH_SMALL_M ? 0 : 1;                  // row gather (fused into the M-small GEMM)
+    n += gemm_gathers_rows(p, path, tile_rows) ? 0 : 1;     // row gather (or fused into the gate-up GEMM)
     n += fused_mlp_of(p, path, tile_rows) ? 1 : 2;
     return n + 1;                                           // combine
 }
@@ -437,7 +452,7 @@ moe_status_t moe_resolve_profile(const moe_problem_t *problem, moe_profile_t *pr
     profile->tile_rows = tile_rows;
     profile->down_split_k = down_split_k(*problem, path, tile_rows, sms);
     profile->pdl = use_pdl(*problem) ? 1 : 0;
-    profile->fused_gather = path == MOE_PATH_SMALL_M ? 1 : 0;
+    profile->fused_gather = gemm_gathers_rows(*problem, path, tile_rows) ? 1 : 0;
     profile->cta_pair = path == MOE_PATH_TILED ? 1 : 0;
     profile->fused_mlp = fused_mlp_of(*problem, path, tile_rows) ? 1 : 0;
     profile->megakernel = use_megakernel(*problem) ? 1 : 0;
@@ -581,7 +596,7 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
     // itself (tile::gather4, at most 16 per stage). The tiled paths read a
     // materialised x_sorted: at 32 gather4 per 128-row stage the TMA issue rate,
     // not the data, limited the gate-up GEMM (4.5x slower on the large shape).
-    const bool fused_gather = path == MOE_PATH_SMALL_M;
+    const bool fused_gather = gemm_gathers_rows(p, path, tile_rows);
     if (!fused_gather)
         st = cuda_status(launch_gather_rows(x, perm, expert_offsets, p.E, p.k, p.H, capacity_of(p), x_sorted, sms, s,
                                             use_pdl(p)));

@@ -99,13 +99,15 @@ def test_quantizer_matches_oracle_decode_shape_sampled(B):
 
 # (T, E, k, H, I, form): tile 16 with the down GEMM in 2 K parts (AUTO: three
 # kernels), in 4 K parts (three kernels, then one), tile 16 unsplit, tile 16
-# unsplit as one kernel, tile 32, tile 64
+# unsplit as one kernel, tile 32, tile 64, tile 64 with several token tiles
+# per expert (128 rows per expert: bf16 weights would take a tiled path there,
+# MXFP8 stays on the M-small path at every batch size)
 CASES = [(1, 64, 4, 512, 256, 0), (1, 64, 6, 512, 512, 0), (1, 64, 6, 512, 512, 2), (8, 64, 4, 4096, 256, 0),
-         (8, 64, 4, 4096, 256, 2), (64, 32, 4, 512, 384, 0), (100, 32, 4, 512, 256, 0)]
+         (8, 64, 4, 4096, 256, 2), (64, 32, 4, 512, 384, 0), (100, 32, 4, 512, 256, 0), (512, 16, 4, 512, 512, 0)]
 
 
 @pytest.mark.parametrize("case", CASES, ids=["t16_split2", "t16_split4", "t16_split4_one_kernel", "t16",
-                                             "t16_one_kernel", "t32", "t64"])
+                                             "t16_one_kernel", "t32", "t64", "t64_many_tiles"])
 def test_mxfp8_forward_equals_bf16_forward_on_dequantized(B, case):
     T, E, k, H, I, form = case
     wl = wlm.custom("mxf", T, E, k, H, I, seed=T + E + H)
@@ -117,7 +119,7 @@ def test_mxfp8_forward_equals_bf16_forward_on_dequantized(B, case):
     prof = B.moe_resolve_profile(p_mx)
     assert prof["path"] == 2 and prof["fused_mlp"] == 1
     # MXFP8 and bf16 weights split the down GEMM's K alike (128-wide blocks)
-    assert prof["down_split_k"] == B.moe_resolve_profile(B.Problem.make(T, E, k, H, I, forward_form=form))[
+    assert prof["down_split_k"] == B.moe_resolve_profile(B.Problem.make(T, E, k, H, I, forward_form=form, path=2))[
         "down_split_k"]
     if I == 512 and T == 1:
         assert prof["down_split_k"] == 4
@@ -125,7 +127,7 @@ def test_mxfp8_forward_equals_bf16_forward_on_dequantized(B, case):
     W13_d = dequantized_device(q13, s13, W13.shape)
     W2_d = dequantized_device(q2, s2, W2.shape)
     outs = []
-    for p, a, b in [(p_mx, W13_mx, W2_mx), (B.Problem.make(T, E, k, H, I, forward_form=form), W13_d, W2_d)]:
+    for p, a, b in [(p_mx, W13_mx, W2_mx), (B.Problem.make(T, E, k, H, I, forward_form=form, path=2), W13_d, W2_d)]:
         bufs = B.Buffers(p)
         B.moe_forward(p, x, ids, w, a, b, bufs.expert_offsets, bufs.perm, bufs.out, bufs.ws)
         torch.cuda.synchronize()
@@ -179,10 +181,19 @@ def test_mxfp8_forward_scale_extremes(B):
 
 
 def test_mxfp8_refused_outside_the_m_small_path(B):
-    p = B.Problem.make(2048, 384, 6, 7168, 3072, weight_layout=B.MOE_WEIGHTS_MXFP8)
-    with pytest.raises(B.MoeError) as ei:
-        B.moe_resolve_profile(p)
-    assert ei.value.status == 5
+    """AUTO takes the M-small path for MXFP8 weights at any batch size; a tiled
+    path asked for explicitly, and moe_expert_compute, refuse the layout."""
+    auto = B.moe_resolve_profile(B.Problem.make(2048, 384, 6, 7168, 3072, weight_layout=B.MOE_WEIGHTS_MXFP8))
+    assert auto["path"] == 2 and auto["tile_rows"] == 64 and auto["fused_mlp"] == 1
+    # 64-row token tiles read a sorted copy of x (a gather kernel first): dispatch (3), gather, GEMMs, combine
+    assert auto["fused_gather"] == 0 and auto["kernel_launches"] == 6
+    dec = B.moe_resolve_profile(B.Problem.make(8, 384, 6, 7168, 3072, weight_layout=B.MOE_WEIGHTS_MXFP8))
+    assert dec["tile_rows"] == 16 and dec["fused_gather"] == 1 and dec["kernel_launches"] == 3
+    for path in (1, 3):
+        p = B.Problem.make(2048, 384, 6, 7168, 3072, weight_layout=B.MOE_WEIGHTS_MXFP8, path=path)
+        with pytest.raises(B.MoeError) as ei:
+            B.moe_resolve_profile(p)
+        assert ei.value.status == 5
     q = B.Problem.make(8, 64, 4, 512, 256, weight_layout=B.MOE_WEIGHTS_MXFP8)
     bufs = B.Buffers(q)
     W = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
