@@ -315,15 +315,22 @@ bool fused_mlp_of(const moe_problem_t &p, int path, int tile_rows)
     return path == MOE_PATH_SMALL_M && (tile_rows == 16 || p.weight_layout == MOE_WEIGHTS_MXFP8);
 }
 
+bool use_megakernel(const moe_problem_t &p);
+
 // moe_forward's gate-up GEMM gathers its activation rows from x itself
 // (tile::gather4 through perm), with no x_sorted and no gather kernel: the
-// M-small path, except MXFP8 weights on token tiles of 32 or more rows, whose
-// stages hold two 64-wide K blocks of the tile (16 or 32 gather4 each, where
-// the TMA issue rate sets the pace: the tiled paths read a materialised
-// x_sorted for the same reason).
+// M-small path, except MXFP8 weights in the three-kernel form. Their stages
+// hold two 64-wide K blocks of the token tile (8, 16 or 32 gather4), which
+// the TMA issues beside the code tiles and scale blocks; a sorted copy read
+// with one box per K block measured faster at every tile height (in one
+// process, bit-identical: decode T=8 679.4 vs 718.6 us, T=1 118.2 vs 119.3;
+// Zipf small batch 1859.5 vs 2191.0; prefill 6267.3 vs 9831.6). The tiled
+// paths read a materialised x_sorted for the same reason. The one-kernel
+// form dispatches inside its CTAs and keeps the gather.
 bool gemm_gathers_rows(const moe_problem_t &p, int path, int tile_rows)
 {
-    return path == MOE_PATH_SMALL_M && !(p.weight_layout == MOE_WEIGHTS_MXFP8 && tile_rows >= 32);
+    (void)tile_rows;
+    return path == MOE_PATH_SMALL_M && !(p.weight_layout == MOE_WEIGHTS_MXFP8 && !use_megakernel(p));
 }
 
 // MXFP8 weights are read by the M-small path only.

@@ -187,8 +187,13 @@ def test_mxfp8_refused_outside_the_m_small_path(B):
     assert auto["path"] == 2 and auto["tile_rows"] == 64 and auto["fused_mlp"] == 1
     # 64-row token tiles read a sorted copy of x (a gather kernel first): dispatch (3), gather, GEMMs, combine
     assert auto["fused_gather"] == 0 and auto["kernel_launches"] == 6
+    # decode-size MXFP8 batches read the sorted copy too (dispatch, gather, GEMMs, combine); the
+    # one-kernel form gathers inside its CTAs
     dec = B.moe_resolve_profile(B.Problem.make(8, 384, 6, 7168, 3072, weight_layout=B.MOE_WEIGHTS_MXFP8))
-    assert dec["tile_rows"] == 16 and dec["fused_gather"] == 1 and dec["kernel_launches"] == 3
+    assert dec["tile_rows"] == 16 and dec["fused_gather"] == 0 and dec["kernel_launches"] == 4
+    one = B.moe_resolve_profile(B.Problem.make(8, 384, 6, 7168, 3072, weight_layout=B.MOE_WEIGHTS_MXFP8,
+                                               forward_form=B.MOE_FORWARD_ONE_KERNEL))
+    assert one["megakernel"] == 1 and one["fused_gather"] == 1 and one["kernel_launches"] == 1
     for path in (1, 3):
         p = B.Problem.make(2048, 384, 6, 7168, 3072, weight_layout=B.MOE_WEIGHTS_MXFP8, path=path)
         with pytest.raises(B.MoeError) as ei:
