@@ -1336,20 +1336,10 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                             const uint32_t sc = (codes4 >> (8 * (c >> 1))) & 0xffu;
                             const bool big = sc > 134u;
                             const uint32_t s1 = ((big ? 254u : sc + 120u) << 7) * 0x00010001u;
-                            // 16-row token tiles: the sign-extending permute (decode T=1 114.0 vs
-                            // 117.6 us, T=8 unchanged); wider tiles keep the multiply-add route (the
-                            // permute measured 3% slower on the Zipf small batch). Same bits.
-                            if constexpr (kTileRows == 16) {
-                                e4m3x4_to_bf16x4_sx(raw.x, s1, out[o + 0], out[o + 1]);
-                                e4m3x4_to_bf16x4_sx(raw.y, s1, out[o + 2], out[o + 3]);
-                                e4m3x4_to_bf16x4_sx(raw.z, s1, out[o + 4], out[o + 5]);
-                                e4m3x4_to_bf16x4_sx(raw.w, s1, out[o + 6], out[o + 7]);
-                            } else {
-                                e4m3x4_to_bf16x4(raw.x, s1, out[o + 0], out[o + 1]);
-                                e4m3x4_to_bf16x4(raw.y, s1, out[o + 2], out[o + 3]);
-                                e4m3x4_to_bf16x4(raw.z, s1, out[o + 4], out[o + 5]);
-                                e4m3x4_to_bf16x4(raw.w, s1, out[o + 6], out[o + 7]);
-                            }
+                            e4m3x4_to_bf16x4(raw.x, s1, out[o + 0], out[o + 1]);
+                            e4m3x4_to_bf16x4(raw.y, s1, out[o + 2], out[o + 3]);
+                            e4m3x4_to_bf16x4(raw.z, s1, out[o + 4], out[o + 5]);
+                            e4m3x4_to_bf16x4(raw.w, s1, out[o + 6], out[o + 7]);
                             if (big) {
                                 const uint32_t s2 = ((sc - 7u) << 7) * 0x00010001u;
 #pragma unroll

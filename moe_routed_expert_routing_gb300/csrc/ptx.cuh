@@ -398,34 +398,22 @@ __device__ __forceinline__ void tmem_wait_st()
 }
 
 // Four E4M3 codes (one 32-bit word, K ascending) times the block scale, as
-// two bf16x2 words (codes 0,1 and 2,3), exactly. A code byte c moved into a
-// 16-bit lane gives the bf16 bits of 2^-120 times its E4M3 value as
-// (c & 0x7f) << 4 | (c & 0x80) << 8 = 16 * (c + 15 * (c & 0x80)): the 4-bit
+// two bf16x2 words (codes 0,1 and 2,3), exactly. A byte permute with sign
+// replication widens each code c to a signed 16-bit v; (v & 0x087f) << 4 then
+// holds c's exponent and mantissa bits in bf16 bits 4..10 and a copy of its
+// sign in bit 15: the bf16 bits of 2^-120 times the E4M3 value. The 4-bit
 // exponent field reads as a bf16 exponent with bias 127 instead of 7, and the
 // subnormal codes land on bf16 subnormals with the same mantissa, so the map
 // is exact for every code the quantizer writes (it never writes NaN). The bf16
 // multiply by `s1` = 2^(e + 120) (bf16x2 bits, e <= 7) is exact while the
-// product stays normal. Per pair of codes: one byte permute and one mask on
-// the integer pipe, two integer multiply-adds and the multiply on the FMA pipe
-// (the route through cvt.f16x2.e4m3x2 and shifts kept the integer pipe busier:
-// in-process A/B, decode T=1 128.7 vs 125.4 us, Zipf small batch 2333.7 vs
-// 2299.8 us, decode T=8 unchanged, outputs bit-identical).
+// product stays normal. Per pair of codes: one permute, one mask and one
+// shift on the integer pipes and the multiply on the FMA pipe. (A route
+// through a zero-extending permute and two integer multiply-adds, in one
+// process, bit-identical: decode T=1 114.0 vs 117.6 us; Zipf small batch
+// 1807.1 vs 1856.5 us and prefill 6102.9 vs 6263.3 us once the token rows
+// came from a sorted copy. Through cvt.f16x2.e4m3x2 and shifts the integer
+// pipe stayed busier still.)
 __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t codes, uint32_t s1, uint32_t &lo, uint32_t &hi)
-{
-    uint32_t a, b;
-    asm("prmt.b32 %0, %1, 0, 0x4140;" : "=r"(a) : "r"(codes));   // (b0, b1) zero-extended
-    asm("prmt.b32 %0, %1, 0, 0x4342;" : "=r"(b) : "r"(codes));   // (b2, b3)
-    a = (a + 15u * (a & 0x00800080u)) << 4;
-    b = (b + 15u * (b & 0x00800080u)) << 4;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(s1));
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(s1));
-}
-
-// The same map from a sign-extending permute: each code widened to a signed
-// 16-bit v gives the bf16 bits of 2^-120 times its value as (v & 0x087f) << 4
-// (exponent and mantissa bits moved 4 places up, a copy of the sign from bit
-// 11 to bit 15). One instruction fewer per pair of codes.
-__device__ __forceinline__ void e4m3x4_to_bf16x4_sx(uint32_t codes, uint32_t s1, uint32_t &lo, uint32_t &hi)
 {
     uint32_t a, b;
     asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(codes));   // (b0, b1), each sign-extended to 16 bits

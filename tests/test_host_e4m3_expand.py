@@ -1,14 +1,15 @@
-"""The bit maps the MXFP8 converter warps use to expand E4M3 codes to bf16,
+"""The bit map the MXFP8 converter warps use to expand E4M3 codes to bf16,
 restated in numpy and checked against the oracle's E4M3 table on every code
 (OCP 8-bit floating point spec, E4M3: bias 7, subnormals 0.mmm x 2^-6, no
 infinities, NaN at S.1111.111, which the quantizer never writes).
 
-Both routes must give the bf16 bits of 2^-120 times the code's value:
-- multiply-add: a code byte c in a 16-bit lane becomes 16 * (c + 15 * (c & 0x80));
-- sign-extending permute: `prmt.b32` with selector nibbles whose bit 3 is set
-  replicates the selected byte's sign bit over the result byte (PTX ISA,
-  prmt default mode), so each code lands in a 16-bit lane as a signed v, and
-  (v & 0x087f) << 4 is the result.
+The map must give the bf16 bits of 2^-120 times the code's value:
+`prmt.b32` with selector nibbles whose bit 3 is set replicates the selected
+byte's sign bit over the result byte (PTX ISA, prmt default mode), so each
+code lands in a 16-bit lane as a signed v, and (v & 0x087f) << 4 is the
+result. The multiply-add map an earlier converter used,
+16 * (c + 15 * (c & 0x80)) for a code byte c in a 16-bit lane, is checked
+too, as a second derivation of the same bits.
 The scale multiply that follows (bf16, by 2^(e + 120)) is exact while the
 product stays normal; that step is checked on the GPU against the oracle."""
 from __future__ import annotations
