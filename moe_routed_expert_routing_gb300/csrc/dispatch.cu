@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_scatter_kernel(
 {
     extern __shared__ int sm[];
     int *cursor = sm;          // [E]   next free row of each expert for this block
-    int *wcnt = sm + E;        // [kWarps][E] slots per expert in each warp, this round
+    int *wcnt = sm + E;        // [kWarps][E] slots per expert in each warp, this pass of 256 slots
     pdl_wait();
     pdl_trigger();
     const int R = dynamic_slots(d_num_tokens, T_max, k);
