@@ -119,14 +119,18 @@ void resolve(const moe_problem_t &p, int *path, int *tile_rows)
     const double avg_rows = static_cast<double>(p.T_max) * p.k / p.E;
     int chosen = p.path;
     // M-small up to 16 routed rows per expert on average; single-CTA 128-row
-    // tiles below 256 (a 256-row pair tile would mostly multiply padding rows:
-    // measured 26% slower on 32 rows per expert); CTA pairs from 256 rows.
+    // tiles below 128 rows; CTA pairs from 128 rows, where experts start to
+    // need a second 128-row tile (and stream their weights twice) while a
+    // pair tile covers 256 rows and runs an expert's last tile of at most 128
+    // rows swapped. Measured at E=384, k=6, H=7168, I=3072, pair vs single-CTA
+    // per call: 64 rows 8163 vs 7717 us, 96 rows 8407 vs 7884, 128 rows 8662
+    // vs 9170, 160 rows 9176 vs 10954.
     // MXFP8 weights: the M-small path at every batch size (its fused kernel
     // is the one that expands them).
     if (chosen == MOE_PATH_AUTO)
         chosen = (avg_rows <= 16.0 || p.weight_layout == MOE_WEIGHTS_MXFP8)
                      ? MOE_PATH_SMALL_M
-                     : (avg_rows < 256.0 ? MOE_PATH_TILED_1CTA : MOE_PATH_TILED);
+                     : (avg_rows < 128.0 ? MOE_PATH_TILED_1CTA : MOE_PATH_TILED);
     *path = chosen;
     if (chosen == MOE_PATH_TILED || chosen == MOE_PATH_TILED_1CTA)
         *tile_rows = 128;
