@@ -71,8 +71,8 @@ typedef enum moe_status {
                                         range of its intermediate y was clipped to +-65504 */
 
 /* Expert-GEMM path. AUTO picks from the static shape, a = T_max*k/E routed
- * rows per expert on average: M-small for a <= 16, single-CTA tiles for
- * 16 < a < 128, CTA-pair tiles for a >= 128 (MXFP8 weights: M-small at
+ * rows per expert on average: M-small for a <= 8, single-CTA tiles for
+ * 8 < a < 128, CTA-pair tiles for a >= 128 (MXFP8 weights: M-small at
  * every a). */
 typedef enum moe_path {
     MOE_PATH_AUTO = 0,

@@ -118,8 +118,12 @@ void resolve(const moe_problem_t &p, int *path, int *tile_rows)
 {
     const double avg_rows = static_cast<double>(p.T_max) * p.k / p.E;
     int chosen = p.path;
-    // M-small up to 16 routed rows per expert on average; single-CTA 128-row
-    // tiles below 128 rows; CTA pairs from 128 rows, where experts start to
+    // M-small up to 8 routed rows per expert on average (16- and 32-row token
+    // tiles; with 64-row tiles the gate-up GEMM's 16 tile::gather4 per stage
+    // set the pace: at E=384, k=6, H=7168, I=3072, M-small vs single-CTA per
+    // call, 8 rows 7065 vs 7062 us, 12 rows 9575 vs 7389, 16 rows 9578 vs
+    // 7427, 24 rows 9644 vs 7498); single-CTA 128-row tiles from there to
+    // 128 rows; CTA pairs from 128 rows, where experts start to
     // need a second 128-row tile (and stream their weights twice) while a
     // pair tile covers 256 rows and runs an expert's last tile of at most 128
     // rows swapped. Measured at E=384, k=6, H=7168, I=3072, pair vs single-CTA
@@ -128,7 +132,7 @@ void resolve(const moe_problem_t &p, int *path, int *tile_rows)
     // MXFP8 weights: the M-small path at every batch size (its fused kernel
     // is the one that expands them).
     if (chosen == MOE_PATH_AUTO)
-        chosen = (avg_rows <= 16.0 || p.weight_layout == MOE_WEIGHTS_MXFP8)
+        chosen = (avg_rows <= 8.0 || p.weight_layout == MOE_WEIGHTS_MXFP8)
                      ? MOE_PATH_SMALL_M
                      : (avg_rows < 128.0 ? MOE_PATH_TILED_1CTA : MOE_PATH_TILED);
     *path = chosen;

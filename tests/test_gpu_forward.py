@@ -177,6 +177,11 @@ def test_launch_profile_table(B):
     large = B.moe_resolve_profile(P(8192, 128, 8, 4096, 1536))
     assert large == dict(path=1, tile_rows=128, down_split_k=1, pdl=0, fused_gather=0, cta_pair=1, fused_mlp=0,
                          megakernel=0, kernel_launches=7)
+    # the boundaries of the rule: M-small up to a = 8, single-CTA tiles below a = 128, CTA pairs from it
+    assert B.moe_resolve_profile(P(512, 384, 6, 7168, 3072))["path"] == 2          # a = 8
+    assert B.moe_resolve_profile(P(768, 384, 6, 7168, 3072))["path"] == 3          # a = 12
+    assert B.moe_resolve_profile(P(6144, 384, 6, 7168, 3072))["path"] == 3         # a = 96
+    assert B.moe_resolve_profile(P(8192, 384, 6, 7168, 3072))["path"] == 1         # a = 128
     # 16-row tiles whose shared-memory dispatch tables do not fit: fused GEMMs, separate dispatch and combine
     wide = B.moe_resolve_profile(P(256, 1024, 8, 512, 256))
     assert wide["fused_mlp"] == 1 and wide["megakernel"] == 0 and wide["kernel_launches"] == 5   # 3 dispatch
