@@ -142,8 +142,9 @@ typedef enum moe_weight_layout {
  * bf16 weights. Activations, h and the output stay bf16 (SiLU(gate)*up
  * rounded to bf16 as before), so the result is the bf16 forward on the
  * dequantized weights. Each token tile of an expert expands its weight tiles
- * again, so batches with many rows per expert (a = 512 measured) run slower
- * than with bf16 weights on the tiled path. A tiled path asked for explicitly and
+ * again, so MXFP8 weights pay off up to about a = 32 (prefill at E=384: 17-19%
+ * faster than bf16 weights) and cost time beyond: a = 64 18% slower, a = 128
+ * 1.75x, a = 512 2.9x. A tiled path asked for explicitly and
  * moe_expert_compute return MOE_ERR_UNSUPPORTED for this layout. Weights must
  * be finite with every block maximum in [2^-110, 2^24). */
 
