@@ -1,9 +1,10 @@
 """The CTA-pair GEMMs on every kind of last row tile: an expert's last tile of
 at most 128 rows runs swapped (weights on the MMA's M side, its rows on N),
 longer ones run as 256-row tiles. Expert row counts are chosen around those
-edges (1, 31/32/33, 63/64/65, 127/128/129, 255/256/257, several tiles, none),
-and the outputs of both GEMMs and of the whole forward are checked against
-the oracle, with H and I multiples of 64 that are not multiples of 128."""
+edges (1, 15/16/17, 31/32/33, 63/64/65, 127/128/129, 200, 239/240/241,
+255/256/257, several tiles ending in 129, 193 or 255 rows, none), and the
+outputs of both GEMMs and of the whole forward are checked against the
+oracle, with H and I multiples of 64 that are not multiples of 128."""
 from __future__ import annotations
 
 import numpy as np
@@ -16,7 +17,8 @@ from parity import assert_within_tolerance
 
 pytestmark = pytest.mark.gpu
 
-COUNTS = [1, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 0, 385, 640]
+COUNTS = [1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 200, 239, 240, 241, 255, 256, 257, 0, 385, 449,
+          511, 640]
 
 
 @pytest.fixture(scope="module")
