@@ -32,29 +32,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 constexpr int kCombineThreads = 128;
 constexpr int kColsPerItem = kCombineThreads * 8;   // one work item = one token x 1024 columns
 
-// Eight consecutive columns of one y row as fp32: two 16-byte loads (fp32 y)
-// or one (fp16 y, widened exactly). A down GEMM that split K leaves fp32 y
-// as `parts` partial rows, `part_stride` elements apart: the row is their
-// sum, taken in part order (((p0 + p1) + p2) + p3), the order in which
-// moe_expert_compute reduces its parts, so every route gives the same bits.
+// Eight consecutive columns of one fp32 y row: two 16-byte loads. (fp16 y is
+// read as raw 16-byte vectors and widened exactly where it is summed; a down
+// GEMM that split K leaves fp32 y as `parts` partial rows, `part_stride`
+// elements apart, summed in part order (((p0 + p1) + p2) + p3), the order in
+// which moe_expert_compute reduces its parts, so every route gives the same
+// bits.)
 __device__ __forceinline__ void load8(const float *y, size_t i, float (&f)[8])
 {
     const float4 a = __ldg(reinterpret_cast<const float4 *>(y + i));
     const float4 b = __ldg(reinterpret_cast<const float4 *>(y + i) + 1);
     f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
     f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
-
-__device__ __forceinline__ void load8(const __half *y, size_t i, float (&f)[8])
-{
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(y + i));
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 p = __half22float2(*reinterpret_cast<const __half2 *>(&u[q]));
-        f[2 * q] = p.x;
-        f[2 * q + 1] = p.y;
-    }
 }
 
 template <typename Y, int kParts>

@@ -37,7 +37,7 @@ __global__ void pack_w13_kernel(const uint4 *__restrict__ W13, uint4 *__restrict
 
 __global__ void pack_w2_kernel(const uint4 *__restrict__ W2, uint4 *__restrict__ out, int E, int H, int I)
 {
-    const int KB = I / 64, NT = H / 128, row_chunks = I / 8;
+    const int KB = I / 64, row_chunks = I / 8;
     const long long total = static_cast<long long>(E) * H * row_chunks;
     for (long long q = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; q < total;
          q += static_cast<long long>(gridDim.x) * blockDim.x) {
