@@ -1889,7 +1889,7 @@ cudaError_t run(const GemmProblem &p, int num_sms, cudaStream_t stream)
 {
     using C = Cfg<kSmallM, kGated, kTileRows, kStages, kSplitK>;
     auto kern = grouped_gemm_kernel<kSmallM, kGated, kTileRows, kStages, kSplitK, kGather>;
-    static int attr_done_for_device = -1;
+    static thread_local int attr_done_for_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -1933,8 +1933,8 @@ cudaError_t run_pair(const GemmProblem &p, int num_sms, cudaStream_t stream)
 {
     using C = PairCfg<kGated, kStages>;
     auto kern = grouped_gemm_pair_kernel<kGated, kStages>;
-    static int attr_done_for_device = -1;
-    static int max_clusters = 0;
+    static thread_local int attr_done_for_device = -1;
+    static thread_local int max_clusters = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -2029,12 +2029,12 @@ long long mega_table_bytes(int E, long long slots) { return 4LL * (2LL * (E + 1)
 
 // Per-block shared memory the device grants (opt-in) minus the static shared
 // memory of the whole-forward kernel and its stages: what is left for the
-// tables. Cached per device; -1 if a query fails.
+// tables. Cached per host thread and device; -1 if a query fails.
 template <int kTileRows, int kStages, bool kFp8>
 long long mega_table_budget()
 {
-    static int cached_dev = -1;
-    static long long cached = -1;
+    static thread_local int cached_dev = -1;
+    static thread_local long long cached = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return -1;
@@ -2085,8 +2085,8 @@ cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *r
             return cudaErrorInvalidValue;
     }
     const int dyn_smem = C::kDynSmem + static_cast<int>(tables);
-    static int attr_done_for_device = -1;
-    static int attr_bytes = 0;
+    static thread_local int attr_done_for_device = -1;
+    static thread_local int attr_bytes = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)

@@ -145,8 +145,8 @@ void resolve(const moe_problem_t &p, int *path, int *tile_rows)
 // The binary carries sm_103a code only: refuse any other device up front.
 moe_status_t check_device()
 {
-    static int checked_device = -1;
-    static bool ok = false;
+    static thread_local int checked_device = -1;
+    static thread_local bool ok = false;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -385,8 +385,8 @@ int forward_launches(const moe_problem_t &p)
 
 int device_sm_count()
 {
-    static int cached_dev = -1;
-    static int cached = 0;
+    static thread_local int cached_dev = -1;
+    static thread_local int cached = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return 0;
