@@ -26,8 +26,12 @@
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls
  *    only enqueue work on it: they never synchronise the host, never read a
  *    device value on the host, and are legal inside CUDA stream capture
- *    (after the first call on a device, which sets up function attributes;
- *    make that first call outside capture).
+ *    (after the first call of the host thread on a device, which sets up
+ *    function attributes; make that first call outside capture).
+ *  - Several host threads may call at once, each with its own workspace and
+ *    its own output buffers (on one stream or several): the library keeps
+ *    its launch caches per host thread and all of a call's device state in
+ *    its workspace.
  *  - Host validation fails closed: a status other than MOE_OK means nothing
  *    was enqueued (DeepGEMM page "MegaMoE: add cluster-paired FP4 weight
  *    packets", Scope and fallback: unsupported shapes fail closed during host
