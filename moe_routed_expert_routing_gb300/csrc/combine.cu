@@ -52,8 +52,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Y *__res
                                                                   const float *__restrict__ w,
                                                                   const int32_t *d_num_tokens, int T_max, int k,
                                                                   int vec_per_row, uint4 *__restrict__ out,
-                                                                  size_t part_stride)
+                                                                  size_t part_stride, bool routing_early)
 {
+    const int groups = (vec_per_row * 8 + kColsPerItem - 1) / kColsPerItem;
+    if (routing_early && threadIdx.x < k && blockIdx.x < static_cast<long long>(T_max) * groups) {
+        // the routing of this block's first item, pulled into L1 ahead of the
+        // wait for y (a token past the device count only costs a prefetch)
+        const size_t slot = static_cast<size_t>(blockIdx.x / groups) * k + threadIdx.x;
+        prefetch_l1(inv + slot);
+        prefetch_l1(w + slot);
+    }
     pdl_wait();
     pdl_trigger();
     int T = T_max;
@@ -61,7 +69,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Y *__res
         T = *d_num_tokens;
         T = T < 0 ? 0 : (T > T_max ? T_max : T);
     }
-    const int groups = (vec_per_row * 8 + kColsPerItem - 1) / kColsPerItem;
     const long long items = static_cast<long long>(T) * groups;
     for (long long item = blockIdx.x; item < items; item += gridDim.x) {
         const int t = static_cast<int>(item / groups);
@@ -104,20 +111,35 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Y *__res
                 }
             }
         } else if (kParts > 1) {
-            // fp32 y in K parts: two routed rows at a time, the 16-byte loads of
-            // all their parts (at most 4) issued together; each row is the sum of
-            // its parts in part order, then weighted and summed in ascending j
-            for (int j0 = 0; j0 < k; j0 += 2) {
-                float4 lo[2][kParts], hi[2][kParts];
-                int row[2];
-                float wj[2];
+            // fp32 y in K parts (decode-size batches, where the combine's
+            // latency is on the call's critical path): with k <= 8 the token's
+            // routing is read once, before any row; then the K parts of four
+            // routed rows are loaded together. Each row is the sum of its parts
+            // in part order, then weighted and summed in ascending j.
+            int rows8[8];
+            float w8[8];
+            const bool k8 = k <= 8;
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    row[q] = (j0 + q < k) ? __ldg(inv_t + j0 + q) : -1;
-                    wj[q] = (j0 + q < k) ? __ldg(w_t + j0 + q) : 0.f;
+            for (int q = 0; q < 8; ++q) {
+                rows8[q] = (k8 && q < k) ? __ldg(inv_t + q) : -1;
+                w8[q] = (k8 && q < k) ? __ldg(w_t + q) : 0.f;
+            }
+            for (int j0 = 0; j0 < k; j0 += 4) {
+                float4 lo[4][kParts], hi[4][kParts];
+                int row[4];
+                float wj[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (k8) {
+                        row[q] = j0 == 0 ? rows8[q] : rows8[4 + q];
+                        wj[q] = j0 == 0 ? w8[q] : w8[4 + q];
+                    } else {
+                        row[q] = (j0 + q < k) ? __ldg(inv_t + j0 + q) : -1;
+                        wj[q] = (j0 + q < k) ? __ldg(w_t + j0 + q) : 0.f;
+                    }
                 }
 #pragma unroll
-                for (int q = 0; q < 2; ++q)
+                for (int q = 0; q < 4; ++q)
 #pragma unroll
                     for (int pp = 0; pp < kParts; ++pp)
                         if (row[q] >= 0) {
@@ -127,7 +149,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Y *__res
                             hi[q][pp] = __ldg(src + 1);
                         }
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
+                for (int q = 0; q < 4; ++q) {
                     if (row[q] < 0)
                         continue;
                     float f[8] = {lo[q][0].x, lo[q][0].y, lo[q][0].z, lo[q][0].w,
@@ -221,7 +243,7 @@ cudaError_t launch_reduce_parts(const float *parts_base, int parts, const int32_
 
 cudaError_t launch_combine(const void *y_sorted, bool y_f16, const int32_t *inv, const float *topk_weights,
                            const int32_t *d_num_tokens, int T_max, int k, int H, void *out, int num_sms,
-                           cudaStream_t stream, bool pdl, int parts, size_t part_stride)
+                           cudaStream_t stream, bool pdl, int parts, size_t part_stride, bool routing_early)
 {
     if (y_f16 && parts != 1)   // fp16 y comes from the tiled paths, whose down GEMM never splits K
         return cudaErrorInvalidValue;
@@ -233,12 +255,13 @@ cudaError_t launch_combine(const void *y_sorted, bool y_f16, const int32_t *inv,
     if (y_f16)
         return launch_k(combine_kernel<__half, 1>, dim3(blocks), dim3(kCombineThreads), 0, stream, pdl,
                         static_cast<const __half *>(y_sorted), inv, topk_weights, d_num_tokens, T_max, k, H / 8,
-                        static_cast<uint4 *>(out), size_t(0));
+                        static_cast<uint4 *>(out), size_t(0), routing_early);
     auto kern = parts == 4 ? combine_kernel<float, 4> : parts == 2 ? combine_kernel<float, 2> : combine_kernel<float, 1>;
     if (parts != 1 && parts != 2 && parts != 4)
         return cudaErrorInvalidValue;
     return launch_k(kern, dim3(blocks), dim3(kCombineThreads), 0, stream, pdl, static_cast<const float *>(y_sorted),
-                    inv, topk_weights, d_num_tokens, T_max, k, H / 8, static_cast<uint4 *>(out), part_stride);
+                    inv, topk_weights, d_num_tokens, T_max, k, H / 8, static_cast<uint4 *>(out), part_stride,
+                    routing_early);
 }
 
 }  // namespace moe

@@ -628,7 +628,7 @@ static moe_status_t forward_impl(const moe_problem_t *problem, const void *x, co
     if (st != MOE_OK || (st = mark(4)) != MOE_OK)
         return st;
     st = cuda_status(launch_combine(y_sorted, y_f16, inv, topk_weights, d_num_tokens, p.T_max, p.k, p.H, out, sms,
-                                    s, use_pdl(p), parts, static_cast<size_t>(capacity_of(p)) * p.H));
+                                    s, use_pdl(p), parts, static_cast<size_t>(capacity_of(p)) * p.H, true));
     if (st != MOE_OK)
         return st;
     return mark(5);

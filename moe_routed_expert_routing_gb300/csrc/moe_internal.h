@@ -28,14 +28,17 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // it on the stream is still finishing (cudaLaunchAttributeProgrammaticStream-
 // Serialization): it runs its prologue, then waits (griddepcontrol.wait) for
 // the previous grid's completion and memory before touching any global data,
-// and releases its own dependents (griddepcontrol.launch_dependents). Every
-// kernel waits before it finishes, so completion stays transitive along the
-// stream; without the attribute both instructions are no-ops. The host turns
+// and releases its own dependents (griddepcontrol.launch_dependents), only
+// after that wait. Every kernel waits before it finishes, so completion stays
+// transitive along the stream, and when a kernel starts, every kernel two or
+// more launches back has completed; without the attribute both instructions
+// are no-ops. The host turns
 // it on for the M-small (decode) path only: measured in one process, it saves
 // ~8 us per decode step and costs ~90 us per large-batch step, where the early
 // dependents share the SMs with the persistent GEMM.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l1(const void *p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
@@ -109,9 +112,13 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *perm, const int32_t
 // y_sorted is fp32, or fp16 when y_f16 is set (moe_forward's tiled paths).
 // fp32 y may be `parts` partial buffers of a down GEMM that split K,
 // part_stride elements apart: each row is their sum in part order.
+// routing_early: inv was written at least two launches back on this stream
+// (moe_forward) and the token count and weights are inputs, so the kernel
+// may pull a block's routing into L1 before its dependency wait.
 cudaError_t launch_combine(const void *y_sorted, bool y_f16, const int32_t *inv, const float *topk_weights,
                            const int32_t *d_num_tokens, int T_max, int k, int H, void *out, int num_sms,
-                           cudaStream_t stream, bool pdl, int parts = 1, size_t part_stride = 0);
+                           cudaStream_t stream, bool pdl, int parts = 1, size_t part_stride = 0,
+                           bool routing_early = false);
 
 // y_sorted[r] = ((p0 + p1) + p2) + p3 over the `parts` fp32 partial buffers of
 // [cap, H] starting at parts_base, for r < expert_offsets[E].
