@@ -1084,7 +1084,34 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                               : decode_unit<true, kTileRows, 128>(v / kSplitDown, s_off, s_tp, E, NT2);
             const int kb0 = up ? 0 : (v % kSplitDown) * kb2;
             const int steps = up ? kb1 : (kb2 + 1) / 2;   // down: two K blocks per stage
-            if (up && !fa.act_sorted) {
+            // bf16 gate-up units gathering from x: the first stage's weights do not
+            // depend on the tile's rows, so lane 0 requests them while the lanes
+            // read the rows' slots (the stage completes on the same count)
+            bool pre = false;
+            if (!kFp8 && up && !fa.act_sorted) {
+                static_assert(kFp8 || kTileRows <= 32, "one row per lane");
+                const int slot = lane < t.rows && lane < kTileRows
+                                     ? (kMega ? s_perm[t.row0 + lane] : __ldg(A1.perm + t.row0 + lane))
+                                     : 0;
+                if (lane == 0 && ok && steps > 0) {
+                    if (mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, abort_flag, A1.wait_limit_ns)) {
+                        const uint32_t full = smem_u32(&bar_full[stage]);
+                        const uint32_t w_dst = smem_u32(smem + stage * C::kStageBytes);
+                        mbar_arrive_expect_tx(full, C::kWBytes + C::kActSlot);
+                        const int wr = t.e * A1.w_rows_per_expert + t.n0;
+                        const int2 g = weight_coords(A1, true, wr, 0);
+                        const int2 w = weight_coords(A1, true, wr + A1.up_row_offset, 0);
+                        tma_load_2d(w_dst, &tm_w13, full, g.x, g.y, pol_w);
+                        tma_load_2d(w_dst + 128 * 128, &tm_w13, full, w.x, w.y, pol_w);
+                        pre = true;
+                    } else {
+                        ok = false;
+                    }
+                }
+                if (lane < kTileRows)
+                    s_rows[lane] = slot / A1.k;
+                __syncwarp();
+            } else if (up && !fa.act_sorted) {
                 for (int i = lane; i < kTileRows; i += 32)
                     s_rows[i] = i < t.rows ? (kMega ? s_perm[t.row0 + i] : __ldg(A1.perm + t.row0 + i)) / A1.k : 0;
                 __syncwarp();
@@ -1104,7 +1131,9 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                     fence_proxy_async_global();
                 }
                 for (int st = 0; ok && st < steps; ++st) {
-                    if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, abort_flag, A1.wait_limit_ns)) {
+                    const bool pre_st = pre && st == 0;   // this stage's slot and weights already taken
+                    if (!pre_st &&
+                        !mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, abort_flag, A1.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -1147,12 +1176,14 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
                                         pol_a);
                         }
                     } else if (up) {
-                        mbar_arrive_expect_tx(full, C::kWBytes + C::kActSlot);
-                        const int wr = t.e * A1.w_rows_per_expert + t.n0;
-                        const int2 g = weight_coords(A1, true, wr, st);
-                        const int2 w = weight_coords(A1, true, wr + A1.up_row_offset, st);
-                        tma_load_2d(w_dst, &tm_w13, full, g.x, g.y, pol_w);
-                        tma_load_2d(w_dst + 128 * 128, &tm_w13, full, w.x, w.y, pol_w);
+                        if (!pre_st) {
+                            mbar_arrive_expect_tx(full, C::kWBytes + C::kActSlot);
+                            const int wr = t.e * A1.w_rows_per_expert + t.n0;
+                            const int2 g = weight_coords(A1, true, wr, st);
+                            const int2 w = weight_coords(A1, true, wr + A1.up_row_offset, st);
+                            tma_load_2d(w_dst, &tm_w13, full, g.x, g.y, pol_w);
+                            tma_load_2d(w_dst + 128 * 128, &tm_w13, full, w.x, w.y, pol_w);
+                        }
 #pragma unroll
                         for (int q = 0; q < kTileRows / 4; ++q)
                             tma_gather4(a_dst + q * 512, &tm_x, full, st * kBK,
