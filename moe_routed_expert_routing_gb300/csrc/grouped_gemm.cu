@@ -282,6 +282,63 @@ __device__ __forceinline__ void build_tile_prefix(const int *s_off, int *s_tp, i
         s_tp[E] = carry;
 }
 
+// The same prefix by the whole block, for the decode kernel whose prologue is
+// on the call's critical path: every warp scans its own 32-expert chunks at
+// once, one warp scans the chunk totals (s_chunk, ceil(E / 32) entries), and
+// every thread adds its chunk's offset. Ends with the block synchronised.
+template <int kThreads>
+__device__ __forceinline__ void build_tile_prefix_block(const int *s_off, int *s_tp, int *s_chunk, int E,
+                                                        int tile_rows)
+{
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nchunks = (E + 31) / 32;
+    for (int c = warp; c < nchunks; c += kThreads / 32) {
+        const int e = c * 32 + lane;
+        int tiles = 0;
+        if (e < E) {
+            int n = s_off[e + 1] - s_off[e];
+            n = n < 0 ? 0 : n;
+            tiles = (n + tile_rows - 1) / tile_rows;
+        }
+        int v = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(kFull, v, o);
+            if (lane >= o)
+                v += n;
+        }
+        if (e < E)
+            s_tp[e] = v - tiles;   // exclusive inside the chunk
+        if (lane == 31)
+            s_chunk[c] = v;        // the chunk's total
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < nchunks; base += 32) {
+            const int c = base + lane;
+            const int total = c < nchunks ? s_chunk[c] : 0;
+            int v = total;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(kFull, v, o);
+                if (lane >= o)
+                    v += n;
+            }
+            if (c < nchunks)
+                s_chunk[c] = carry + v - total;
+            carry += __shfl_sync(kFull, v, 31);
+        }
+        if (lane == 0)
+            s_tp[E] = carry;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads)
+        s_tp[e] += s_chunk[e >> 5];
+    __syncthreads();
+}
+
 // Epilogue of a 128-row tiled unit: this thread owns accumulator row `row`
 // (TMEM lane base already in t_row); the warp's 32 rows are consecutive.
 // Gate-up: columns [0,128) gate, [128,256) up -> bf16 SiLU(gate)*up into h.
@@ -987,6 +1044,7 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
     __shared__ int s_last;
     __shared__ int s_off_static[kStaticTable];
     __shared__ int s_tp_static[kStaticTable];
+    __shared__ int s_chunk[(kMaxExperts + 31) / 32];   // tile prefix: the 32-expert chunks' offsets
 
     const GemmArgs &A1 = fa.up;
     const GemmArgs &A2 = fa.down;
@@ -1043,8 +1101,7 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
             s_off[i] = A1.expert_offsets[i];
     }
     __syncthreads();
-    if (warp == 3)
-        build_tile_prefix(s_off, s_tp, E, kTileRows, lane);
+    build_tile_prefix_block<kThreads>(s_off, s_tp, s_chunk, E, kTileRows);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
