@@ -2235,16 +2235,7 @@ cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *r
     // the device's occupancy for this kernel
     const long long tiles = (static_cast<long long>(up.cap) + kTileRows - 1) / kTileRows + up.E;
     const long long max_units = tiles * ((up.n_out + 127) / 128 + ((down.n_out + 127) / 128) * kSplitDown);
-    // The dispatch block before this kernel and one of its CTAs cannot share
-    // an SM (shared memory), and the launch waits until the whole grid fits.
-    // Where the gate-up units fit one wave on one SM fewer (a few tokens;
-    // bf16, three-kernel form) the grid leaves that SM to the dispatch, so the
-    // kernel starts, and runs its prologue, under it. Measured at one token,
-    // E=384, H=7168, I=3072, in one process, outputs bit-identical: 127.4 vs
-    // 128.3 us per call; at eight tokens the SM is worth more (+0.4 us).
-    const long long tiles_bound = (up.cap < up.E ? up.cap : up.E) + up.cap / kTileRows;
-    const long long units1_bound = tiles_bound * ((up.n_out + 127) / 128);
-    const int grid_sms = (!kMega && !kFp8 && num_sms > 1 && units1_bound <= num_sms - 1) ? num_sms - 1 : num_sms;
+    const int grid_sms = fused_grid_sms(kMega, kFp8, up.cap, up.E, up.n_out, kTileRows, num_sms);
     const long long want = max_units < grid_sms ? (max_units < 1 ? 1 : max_units) : grid_sms;
     return launch_k_coresident(kern, want, dim3(C::kThreadsCta), dyn_smem, stream, up.pdl, num_sms, tm_x, tm_w13,
                                tm_h, tm_w2, fa);

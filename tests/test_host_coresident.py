@@ -4,7 +4,9 @@ against the occupancy the device reports and launched cooperatively; when
 not even one CTA fits on an SM the launch is refused before it is made,
 instead of starting a grid whose waits could only run out.
 
-The decision is `moe::coresident_grid` in csrc/moe_internal.h; this test
+The decision is `moe::coresident_grid` in csrc/moe_internal.h, with
+`moe::fused_grid_sms` (the fused decode kernel leaves one SM to the dispatch
+block where its gate-up units fit one wave on one SM fewer); this test
 compiles a small host program against that header with nvcc and runs it.
 """
 from __future__ import annotations
@@ -38,6 +40,27 @@ int main()
         const int g = moe::coresident_grid(c.want, c.per_sm, c.sms);
         if (g != c.grid) {
             std::printf("want=%lld per_sm=%d sms=%d: grid %d, expected %d\n", c.want, c.per_sm, c.sms, g, c.grid);
+            ++bad;
+        }
+    }
+    // the fused decode kernel's grid: one SM left to the dispatch where the
+    // gate-up units (row tiles bound x ceil(I / 128)) fit one wave on one SM fewer
+    struct Fused { bool mega, fp8; long long cap; int E, I, tile_rows, sms, grid_sms; };
+    const Fused fused[] = {
+        {false, false, 6, 384, 3072, 16, 152, 151},      // one token, k=6: 6 row tiles x 24 = 144 units
+        {false, false, 48, 384, 3072, 16, 152, 152},     // eight tokens: (48 + 3) x 24 units
+        {true, false, 6, 384, 3072, 16, 152, 152},       // one-kernel form: no dispatch kernel before it
+        {false, true, 6, 384, 3072, 16, 152, 152},       // MXFP8 weights: the full grid
+        {false, false, 8, 384, 2304, 16, 152, 151},      // 8 x 18 = 144 units
+        {false, false, 8, 384, 2432, 16, 152, 152},      // 8 x 19 = 152 units: more than 151
+        {false, false, 6, 4, 3072, 16, 152, 151},        // more slots than experts: min(cap, E) row tiles
+        {false, false, 6, 384, 3072, 16, 1, 1},          // a single SM keeps it
+    };
+    for (const Fused &f : fused) {
+        const int g = moe::fused_grid_sms(f.mega, f.fp8, f.cap, f.E, f.I, f.tile_rows, f.sms);
+        if (g != f.grid_sms) {
+            std::printf("fused mega=%d fp8=%d cap=%lld E=%d I=%d sms=%d: %d SMs, expected %d\n", f.mega, f.fp8,
+                        f.cap, f.E, f.I, f.sms, g, f.grid_sms);
             ++bad;
         }
     }
