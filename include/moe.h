@@ -103,7 +103,9 @@ typedef struct moe_problem {
  * moe_resolve_profile return MOE_ERR_UNSUPPORTED for a problem that is not
  * decode-size or whose tables do not fit that kernel's shared memory.
  * SEPARATE: dispatch, the two fused GEMMs and the combine as three kernels
- * chained by programmatic dependent launch. AUTO: SEPARATE (measured at one
+ * chained by programmatic dependent launch (for a few tokens with bf16
+ * weights the GEMM kernel also dispatches the slots itself, with the same
+ * result, so that it need not wait for the dispatch kernel). AUTO: SEPARATE (measured at one
  * token, E=384, H=7168, I=3072, down GEMM in 4 K parts: 129.6 vs 131.5 us
  * with bf16 weights, 117.3 vs 121.8 us with MXFP8 weights). Other problems
  * ignore the field. */

@@ -846,6 +846,12 @@ struct FusedArgs {
     int32_t *perm_out;             // [cap] for the caller
     __nv_bfloat16 *out;            // [T_max, H]
     int32_t *done;                 // CTAs through with their GEMM units, zero at launch and at exit
+    // 1: the call's dispatch kernel runs beside this kernel (it writes
+    // expert_offsets, perm and inv for the caller and the combine) and the
+    // combine kernel after it: no in-kernel combine, and no wait for the
+    // dispatch before the GEMM units (this kernel's own local dispatch of the
+    // same slots gives the same tables)
+    int combine_apart;
     // MXFP8, separate form: the gate-up activation rows come from a sorted
     // copy (x_sorted, one 2-D TMA box of kTileRows rows per 64-wide K block)
     // instead of tile::gather4 from x through perm
@@ -862,6 +868,7 @@ struct FusedArgs {
 template <int kThreads>
 __device__ int cta_dispatch(const FusedArgs &fa, int E, int *s_off, int *s_cur, int *s_perm, int *s_inv)
 {
+    const bool write_outputs = !fa.combine_apart;   // else the dispatch kernel beside writes them
     static_assert(4 * kThreads >= kMaxExperts, "the scan covers four experts per thread");
     __shared__ int s_warp_sum[kThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -882,7 +889,7 @@ __device__ int cta_dispatch(const FusedArgs &fa, int E, int *s_off, int *s_cur, 
         else if (e != -1)
             bad = true;
     }
-    if (bad && blockIdx.x == 0)
+    if (bad && blockIdx.x == 0 && write_outputs)
         atomicOr(fa.up.err, MOE_DEVERR_BAD_EXPERT_ID);
     __syncthreads();
     // exclusive scan over experts, four consecutive experts per thread (E <= 1024)
@@ -942,7 +949,7 @@ __device__ int cta_dispatch(const FusedArgs &fa, int E, int *s_off, int *s_cur, 
         }
     }
     __syncthreads();
-    if (blockIdx.x == 0) {
+    if (blockIdx.x == 0 && write_outputs) {
         for (int i = tid; i <= E; i += kThreads)
             fa.expert_offsets_out[i] = s_off[i];
         for (int r = tid; r < s_off[E]; r += kThreads)
@@ -1091,7 +1098,10 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
         tmem_alloc(smem_u32(&s_tmem_base), C::kTmemCols);
         tmem_relinquish();
     }
-    pdl_wait();
+    // With the dispatch kernel beside it, the kernel needs nothing the
+    // dispatch writes: it waits for it only before releasing its dependents.
+    if (!(kMega && fa.combine_apart))
+        pdl_wait();
     if (kMega) {
         const int T = cta_dispatch<kThreads>(fa, E, s_off, s_tp, s_perm, s_inv);
         if (threadIdx.x == 0)
@@ -1533,7 +1543,7 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
     }
-    if (kMega) {
+    if (kMega && !fa.combine_apart) {
         // every CTA counts itself once on `done`, after all its units (its
         // epilogue threads fenced their y stores before the barrier above;
         // also after giving up, so that the others need not wait the limit);
@@ -1570,6 +1580,8 @@ __global__ void __launch_bounds__(FusedCfg<kTileRows, kStages, kFp8>::kThreadsCt
             *fa.exits = 0;
         }
     }
+    if (kMega && fa.combine_apart)
+        pdl_wait();   // the dispatch kernel beside is complete before any dependent starts
     pdl_trigger();
     if (threadIdx.x == 0 && s_abort)
         atomicOr(A1.err, MOE_DEVERR_WAIT_TIMEOUT);
@@ -2229,13 +2241,15 @@ cudaError_t run_fused(const GemmProblem &up, const GemmProblem &down, int32_t *r
         fa.perm_out = mega->perm_out;
         fa.out = static_cast<__nv_bfloat16 *>(mega->out);
         fa.done = counters;
+        fa.combine_apart = mega->combine_apart ? 1 : 0;
     }
     // one CTA per SM, all resident at once (the down units and the combine
     // wait on counts other CTAs publish): a cooperative launch, sized against
     // the device's occupancy for this kernel
     const long long tiles = (static_cast<long long>(up.cap) + kTileRows - 1) / kTileRows + up.E;
     const long long max_units = tiles * ((up.n_out + 127) / 128 + ((down.n_out + 127) / 128) * kSplitDown);
-    const int grid_sms = fused_grid_sms(kMega, kFp8, up.cap, up.E, up.n_out, kTileRows, num_sms);
+    const bool whole_forward = kMega && !(mega && mega->combine_apart);
+    const int grid_sms = fused_grid_sms(whole_forward, kFp8, up.cap, up.E, up.n_out, kTileRows, num_sms);
     const long long want = max_units < grid_sms ? (max_units < 1 ? 1 : max_units) : grid_sms;
     return launch_k_coresident(kern, want, dim3(C::kThreadsCta), dyn_smem, stream, up.pdl, num_sms, tm_x, tm_w13,
                                tm_h, tm_w2, fa);

@@ -192,6 +192,10 @@ struct MegaParams {
     int32_t *expert_offsets_out;   // [E + 1]
     int32_t *perm_out;             // [cap]
     void *out;                     // [T_max, H] bf16
+    // the dispatch kernel runs beside the fused kernel (and writes the tables
+    // above and inv) and the combine kernel after it: the fused kernel only
+    // dispatches locally for its own units
+    bool combine_apart = false;
 };
 
 // Both M-small GEMMs in one persistent launch (gate-up with gathered rows, then
